@@ -1,0 +1,53 @@
+"""The five synthetic workloads the library is measured and checked on.
+
+BigBird-ITC shapes follow the paper's App. E Tab. 8 (block b = 64, g = 2b,
+w = 3b, r = 3b tokens, i.e. 2 global, 3 window and 3 random blocks, n = 4096,
+12 heads) and Longformer's Sec. 3.1 (window 512, i.e. 256 tokens each side,
+global attention on a few chosen positions). The long and padded variants
+stretch the same pattern to n = 16384 and n = 65536.
+"""
+
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str            # "bigbird" or "longformer"
+    B: int
+    H: int
+    n: int
+    d: int
+    dtype: str           # "bf16" or "fp32"
+    sigma: float = 1.0
+    b: int = 64
+    g: int = 2
+    w: int = 3
+    r: int = 3
+    window: int = 0
+    n_global: int = 0
+    padded: bool = False
+    seed: int = 0
+    cfg_id: int = 0
+    tol_max: float = 2e-2
+    tol_mean: float = 2e-3
+
+
+WORKLOADS = {
+    "bigbird_fp32_n1024": Workload(
+        "bigbird_fp32_n1024", "bigbird", B=1, H=1, n=1024, d=64, dtype="fp32",
+        cfg_id=1, tol_max=1e-4, tol_mean=1e-5),
+    "bigbird_bf16_n4096": Workload(
+        "bigbird_bf16_n4096", "bigbird", B=8, H=12, n=4096, d=64, dtype="bf16", cfg_id=2),
+    "longformer_bf16_n4096": Workload(
+        "longformer_bf16_n4096", "longformer", B=4, H=12, n=4096, d=64, dtype="bf16",
+        window=512, n_global=16, cfg_id=3),
+    "bigbird_bf16_n16384_padded": Workload(
+        "bigbird_bf16_n16384_padded", "bigbird", B=2, H=16, n=16384, d=64, dtype="bf16",
+        padded=True, cfg_id=4),
+    "bigbird_bf16_n65536_d128": Workload(
+        "bigbird_bf16_n65536_d128", "bigbird", B=1, H=16, n=65536, d=128, dtype="bf16",
+        sigma=0.5, b=128, cfg_id=5),
+}
+
+HEADLINE = "bigbird_bf16_n4096"

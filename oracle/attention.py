@@ -1,0 +1,203 @@
+"""Masked dense softmax attention in float64: the oracle's definition of the
+BigBird and Longformer forward passes (test infrastructure, CPU only).
+
+What is computed (per batch entry beta and head h):
+
+    S       = Q K^T / sqrt(d)                                  (Longformer Sec. 3.1, Eq. 1)
+    M[i, j] = allowed(i, j) and valid(j) and valid(i)          (BigBird Sec. 2, Eq. AT: the
+                                                                neighbourhood N(i) of graph D)
+    P[i, :] = softmax of S[i, :] over {j : M[i, j]}
+    O[i, :] = sum_j P[i, j] V[j, :]   if row i has an allowed key, else 0
+
+No blocking, no fusion, no reordering: the explicit n x n (or rows x n) boolean
+mask is built from the pattern's definition and applied to the dense score
+matrix. BigBird App. D (Fig. 6 caption) states that its blockified product
+yields exactly the sparse matrix of its Fig. 3(d); a faster implementation must
+therefore equal this masked dense computation up to rounding.
+
+Readings where the pages are silent or garbled (all recorded in the design notes):
+  * BigBird global blocks are blocks 0..g-1 (ITC: existing tokens made global,
+    blog Sec. 2.3 "e.g. the first 128 tokens"); g, w, r are counted in blocks.
+  * The BigBird window reaches w // 2 blocks each side and is clipped at the
+    sequence ends (no circular wrap); Longformer reaches window // 2 tokens each
+    side, also clipped.
+  * Key padding (valid = key_mask) removes keys; padded query rows are zero.
+  * A row with no allowed valid key outputs zeros.
+"""
+
+import math
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Attention patterns (boolean "allowed" masks)
+# ---------------------------------------------------------------------------
+
+def bigbird_block_allowed(nb, g, w, rand_row):
+    """Block-level neighbourhood of BigBird-ITC, bool [nb, nb].
+
+    ``rand_row`` is one head's random table [nb, r] (-1 = no block). Query block
+    qb attends key block kb when (BigBird Sec. 2 / blog Sec. 2.1-2.3):
+      * qb is a global block (qb < g): global tokens attend everything;
+      * kb is a global block (kb < g): everything attends global tokens;
+      * |qb - kb| <= w // 2: the sliding window of w blocks;
+      * kb is one of qb's random blocks.
+    """
+    half = w // 2
+    allowed = np.zeros((nb, nb), dtype=bool)
+    for qb in range(nb):
+        randoms = set(int(x) for x in rand_row[qb] if x >= 0)
+        for kb in range(nb):
+            if qb < g:
+                allowed[qb, kb] = True
+            elif kb < g:
+                allowed[qb, kb] = True
+            elif abs(qb - kb) <= half:
+                allowed[qb, kb] = True
+            elif kb in randoms:
+                allowed[qb, kb] = True
+    return allowed
+
+
+def bigbird_allowed(n, b, g, w, rand_row, rows=None):
+    """Token-level BigBird mask, bool [len(rows), n]: token i sees token j iff
+    block i // b sees block j // b (blockified pattern, BigBird App. D)."""
+    nb = n // b
+    blk = bigbird_block_allowed(nb, g, w, rand_row)
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    cols = np.arange(n)
+    return blk[rows[:, None] // b, cols[None, :] // b]
+
+
+def longformer_allowed(n, window, global_idx, rows=None):
+    """Longformer mask, bool [len(rows), n] (Longformer Sec. 3.1).
+
+    Token i sees token j when i or j carries global attention (symmetric: a
+    global token attends all tokens and all tokens attend it), or when
+    |i - j| <= window // 2 (window / 2 tokens on each side, clipped at the ends).
+    """
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    cols = np.arange(n)
+    is_global = np.zeros(n, dtype=bool)
+    is_global[np.asarray(global_idx, dtype=np.int64)] = True
+    band = np.abs(rows[:, None] - cols[None, :]) <= window // 2
+    return band | is_global[rows][:, None] | is_global[None, :]
+
+
+# ---------------------------------------------------------------------------
+# Masked softmax attention
+# ---------------------------------------------------------------------------
+
+def masked_softmax_probs(q, k, mask):
+    """P = softmax over the allowed keys of (q k^T / sqrt(d)), float64.
+
+    q: [m, d], k: [n, d], mask: bool [m, n]. Rows without an allowed key are 0.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    d = q.shape[1]
+    s = (q @ k.T) / math.sqrt(d)
+    s = np.where(mask, s, -np.inf)
+    any_allowed = mask.any(axis=1)
+    row_max = np.where(any_allowed, s.max(axis=1, initial=-np.inf), 0.0)
+    e = np.where(mask, np.exp(s - row_max[:, None]), 0.0)
+    denom = e.sum(axis=1)
+    denom = np.where(any_allowed, denom, 1.0)
+    return e / denom[:, None]
+
+
+def masked_attention(q, k, v, mask):
+    """O = P V for P = masked_softmax_probs(q, k, mask); float64 [m, d]."""
+    p = masked_softmax_probs(q, k, mask)
+    return p @ np.asarray(v, dtype=np.float64)
+
+
+def _apply_validity(mask, rows, key_valid):
+    if key_valid is None:
+        return mask
+    key_valid = np.asarray(key_valid, dtype=bool)
+    return mask & key_valid[None, :] & key_valid[rows][:, None]
+
+
+def _as_f64(x):
+    """Upcast exactly to float64 (accepts numpy arrays or CPU torch tensors)."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def oracle_bigbird(Q, K, V, b, g, w, rand_table, key_mask=None, rows=None,
+                   row_chunk=1024):
+    """BigBird-ITC attention forward, float64 [B, H, len(rows), d].
+
+    Q, K, V: [B, H, n, d] (any float type; upcast exactly). rand_table:
+    int [H, n // b, r], shared by all batch entries. key_mask: [B, n], nonzero =
+    valid token, or None. rows: query rows to compute (default all).
+    """
+    Q, K, V = _as_f64(Q), _as_f64(K), _as_f64(V)
+    rand_table = np.asarray(rand_table)
+    B, H, n, d = Q.shape
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    out = np.zeros((B, H, len(rows), d), dtype=np.float64)
+    for h in range(H):
+        blk = bigbird_block_allowed(n // b, g, w, rand_table[h])
+        for beta in range(B):
+            kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+            for c0 in range(0, len(rows), row_chunk):
+                rr = rows[c0:c0 + row_chunk]
+                mask = blk[rr[:, None] // b, np.arange(n)[None, :] // b]
+                mask = _apply_validity(mask, rr, kv)
+                out[beta, h, c0:c0 + len(rr)] = masked_attention(
+                    Q[beta, h, rr], K[beta, h], V[beta, h], mask)
+    return out
+
+
+def oracle_longformer(Q, K, V, window, global_idx, key_mask=None, rows=None,
+                      row_chunk=1024):
+    """Longformer sliding-window + global attention forward, float64."""
+    Q, K, V = _as_f64(Q), _as_f64(K), _as_f64(V)
+    B, H, n, d = Q.shape
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    out = np.zeros((B, H, len(rows), d), dtype=np.float64)
+    for beta in range(B):
+        kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+        for c0 in range(0, len(rows), row_chunk):
+            rr = rows[c0:c0 + row_chunk]
+            mask = _apply_validity(longformer_allowed(n, window, global_idx, rr), rr, kv)
+            for h in range(H):
+                out[beta, h, c0:c0 + len(rr)] = masked_attention(
+                    Q[beta, h, rr], K[beta, h], V[beta, h], mask)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Work accounting: attended (valid query, allowed valid key) pairs
+# ---------------------------------------------------------------------------
+
+def bigbird_attended_pairs(n, b, g, w, rand_table, key_mask=None, B=1):
+    """Number of True entries of M summed over batch entries and heads."""
+    rand_table = np.asarray(rand_table)
+    H = rand_table.shape[0]
+    total = 0
+    for h in range(H):
+        blk = bigbird_block_allowed(n // b, g, w, rand_table[h])
+        for beta in range(B):
+            if key_mask is None:
+                total += int(blk.sum()) * b * b
+            else:
+                kv = np.asarray(key_mask[beta]) != 0
+                per_blk = kv.reshape(n // b, b).sum(axis=1).astype(np.int64)
+                total += int(per_blk @ blk.astype(np.int64) @ per_blk)
+    return total
+
+
+def longformer_attended_pairs(n, window, global_idx, key_mask=None, B=1, H=1):
+    total = 0
+    for beta in range(B):
+        kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+        for c0 in range(0, n, 1024):
+            rr = np.arange(c0, min(n, c0 + 1024))
+            total += int(_apply_validity(
+                longformer_allowed(n, window, global_idx, rr), rr, kv).sum())
+    return total * H

@@ -1,0 +1,316 @@
+"""Pins of the float64 oracle to facts fixed outside the oracle itself.
+
+Each test checks the oracle against a published value, a closed form, an
+invariant stated by the pages, a special case that reduces to a library
+routine (torch's float64 scaled_dot_product_attention on the CPU), or a
+scalar brute force written differently from the oracle's vectorised code.
+"""
+
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import (
+    bigbird_allowed,
+    bigbird_attended_pairs,
+    bigbird_random_table,
+    longformer_allowed,
+    longformer_attended_pairs,
+    masked_attention,
+    masked_softmax_probs,
+    oracle_bigbird,
+    oracle_longformer,
+    splitmix64_stream,
+)
+from oracle.attention import bigbird_block_allowed
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _sdpa(q, k, v, mask=None):
+    """torch float64 scaled dot-product attention (library routine)."""
+    q, k, v = (torch.as_tensor(np.asarray(x, dtype=np.float64)) for x in (q, k, v))
+    m = None if mask is None else torch.as_tensor(mask)
+    return torch.nn.functional.scaled_dot_product_attention(
+        q[None], k[None], v[None], attn_mask=m).numpy()[0]
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------- SplitMix64
+
+def test_splitmix64_published_vector():
+    lines = [l.split("#")[0].strip() for l in open(os.path.join(GOLDEN, "splitmix64_seed1234567.txt"))]
+    lines = [l for l in lines if l]
+    seed = int(lines[0].split()[1])
+    expected = [int(x) for x in lines[1:]]
+    assert splitmix64_stream(seed, len(expected)) == expected
+
+
+# ------------------------------------------------------------ random table
+
+def _brute_candidates(nb, g, w, j):
+    every = set(range(nb))
+    glob = set(range(g))
+    window = {k for k in every if -(w // 2) <= k - j <= w // 2}
+    return every - glob - window
+
+
+TABLE_CASES = [
+    (0, 2, 1024, 64, 2, 3, 3),
+    (7, 3, 512, 16, 1, 5, 4),
+    (123, 1, 256, 8, 3, 7, 2),
+    (99, 2, 128, 16, 0, 1, 2),
+    (5, 2, 256, 32, 2, 3, 9),   # fewer candidates than r on some rows
+    (11, 1, 192, 64, 1, 3, 3),  # nb = 3: no candidates at all
+]
+
+
+@pytest.mark.parametrize("seed,H,n,b,g,w,r", TABLE_CASES)
+def test_random_table_invariants(seed, H, n, b, g, w, r):
+    t = bigbird_random_table(seed, H, n, b, g, w, r)
+    nb = n // b
+    assert t.shape == (H, nb, r) and t.dtype == np.int32
+    for h in range(H):
+        for j in range(nb):
+            row = [int(x) for x in t[h, j]]
+            if j < g:
+                assert row == [-1] * r, "global rows draw nothing"
+                continue
+            cand = _brute_candidates(nb, g, w, j)
+            k = min(r, len(cand))
+            chosen = row[:k]
+            assert row[k:] == [-1] * (r - k)
+            assert chosen == sorted(chosen)
+            assert len(set(chosen)) == k, "distinct"
+            assert set(chosen) <= cand, "outside global and window, in range"
+
+
+def test_random_table_determinism_and_sensitivity():
+    a = bigbird_random_table(0, 4, 4096, 64, 2, 3, 3)
+    b = bigbird_random_table(0, 4, 4096, 64, 2, 3, 3)
+    c = bigbird_random_table(1, 4, 4096, 64, 2, 3, 3)
+    assert np.array_equal(a, b)
+    assert not np.array_equal(a, c)
+    for h in range(1, 4):
+        assert not np.array_equal(a[0], a[h]), "per-head tables differ"
+
+
+def test_random_table_sampling_is_uniform():
+    # Partial Fisher-Yates picks each candidate with probability k / m.
+    nb, g, w, r, j = 12, 1, 3, 3, 6
+    m = len(_brute_candidates(nb, g, w, j))
+    counts = np.zeros(nb)
+    trials = 3000
+    for seed in range(trials):
+        t = bigbird_random_table(seed, 1, nb * 8, 8, g, w, r)
+        for kb in t[0, j]:
+            counts[kb] += 1
+    cand = sorted(_brute_candidates(nb, g, w, j))
+    expect = trials * r / m
+    assert counts[[k for k in range(nb) if k not in cand]].sum() == 0
+    chi2 = float((((counts[cand] - expect) ** 2) / expect).sum())
+    assert chi2 < 30.0, chi2  # 7 degrees of freedom; p < 1e-4 above 30
+
+
+# ------------------------------------------------------------ BigBird mask
+
+def _brute_bigbird_neigh(nb, g, w, rand_row, qb):
+    if qb < g:
+        return set(range(nb))
+    half = w // 2
+    s = set(range(g))
+    s |= set(range(max(0, qb - half), min(nb, qb + half + 1)))
+    s |= {int(x) for x in rand_row[qb] if x >= 0}
+    return s
+
+
+@pytest.mark.parametrize("seed,H,n,b,g,w,r", TABLE_CASES[:5])
+def test_bigbird_mask_matches_enumeration(seed, H, n, b, g, w, r):
+    t = bigbird_random_table(seed, H, n, b, g, w, r)
+    nb = n // b
+    for h in range(H):
+        m = bigbird_allowed(n, b, g, w, t[h])
+        for i in range(0, n, max(1, b // 3)):
+            neigh = _brute_bigbird_neigh(nb, g, w, t[h], i // b)
+            expect = np.array([(j // b) in neigh for j in range(n)])
+            assert np.array_equal(m[i], expect), (h, i)
+
+
+def test_bigbird_global_and_window_invariants():
+    n, b, g, w, r = 2048, 64, 2, 5, 3
+    nb = n // b
+    t = bigbird_random_table(3, 1, n, b, g, w, r)
+    blk = bigbird_block_allowed(nb, g, w, t[0])
+    assert blk[:g].all(), "global blocks attend everything"
+    assert blk[:, :g].all(), "everything attends global blocks"
+    half = w // 2
+    for j in range(g, nb):
+        nonrand = blk[j].copy()
+        for kb in t[0, j]:
+            if kb >= 0:
+                nonrand[kb] = False
+        nonrand[:g] = False
+        idx = np.nonzero(nonrand)[0]
+        lo, hi = max(j - half, 0), min(j + half, nb - 1)
+        window = [k for k in range(lo, hi + 1) if k >= g]
+        assert list(idx) == window, "window is exactly the clipped +-w//2 band"
+
+
+def test_bigbird_coverage_equals_full_attention():
+    # r >= nb: every block is drawn, the pattern is complete -> textbook attention.
+    B, H, n, d, b = 1, 2, 256, 16, 32
+    t = bigbird_random_table(1, H, n, b, 1, 1, n // b)
+    assert bigbird_allowed(n, b, 1, 1, t[0]).all()
+    Q, K, V = _rand((B, H, n, d), 1), _rand((B, H, n, d), 2), _rand((B, H, n, d), 3)
+    out = oracle_bigbird(Q, K, V, b, 1, 1, t)
+    for h in range(H):
+        np.testing.assert_allclose(out[0, h], _sdpa(Q[0, h], K[0, h], V[0, h]), rtol=0, atol=1e-12)
+
+
+def test_bigbird_block_diagonal_equals_per_block_attention():
+    # g = 0, w = 1, r = 0: each query block sees only itself (BigBird App. D Eq. 13).
+    B, H, n, d, b = 2, 1, 256, 32, 64
+    t = bigbird_random_table(0, H, n, b, 0, 1, 0)
+    Q, K, V = _rand((B, H, n, d), 4), _rand((B, H, n, d), 5), _rand((B, H, n, d), 6)
+    out = oracle_bigbird(Q, K, V, b, 0, 1, t)
+    for beta in range(B):
+        for j in range(n // b):
+            s = slice(j * b, (j + 1) * b)
+            ref = _sdpa(Q[beta, 0, s], K[beta, 0, s], V[beta, 0, s])
+            np.testing.assert_allclose(out[beta, 0, s], ref, rtol=0, atol=1e-12)
+
+
+def test_bigbird_matches_sdpa_with_explicit_mask_and_padding():
+    # Key padding: padded query rows are exactly 0; the valid region equals
+    # library attention on the truncated sequence under the same pattern.
+    B, H, n, d, b, g, w, r = 2, 2, 512, 32, 32, 2, 3, 3
+    t = bigbird_random_table(9, H, n, b, g, w, r)
+    Q, K, V = _rand((B, H, n, d), 7), _rand((B, H, n, d), 8), _rand((B, H, n, d), 9)
+    lengths = [301, 512]
+    km = np.zeros((B, n), dtype=np.uint8)
+    for beta, L in enumerate(lengths):
+        km[beta, :L] = 1
+    out = oracle_bigbird(Q, K, V, b, g, w, t, key_mask=km)
+    for beta, L in enumerate(lengths):
+        assert np.all(out[beta, :, L:] == 0.0)
+        for h in range(H):
+            allowed = bigbird_allowed(n, b, g, w, t[h])[:L, :L]
+            ref = _sdpa(Q[beta, h, :L], K[beta, h, :L], V[beta, h, :L], mask=allowed)
+            np.testing.assert_allclose(out[beta, h, :L], ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ Longformer
+
+def test_longformer_mask_invariants():
+    n, window = 300, 40
+    G = [0, 5, 123, 299]
+    m = longformer_allowed(n, window, G)
+    for i in range(n):
+        for j in range(n):
+            expect = (i in G) or (j in G) or abs(i - j) <= window // 2
+            assert m[i, j] == expect
+    assert m[G].all() and m[:, G].all(), "global attention is symmetric"
+
+
+def test_longformer_wide_window_equals_full_attention():
+    B, H, n, d = 1, 2, 200, 16
+    Q, K, V = _rand((B, H, n, d), 10), _rand((B, H, n, d), 11), _rand((B, H, n, d), 12)
+    out = oracle_longformer(Q, K, V, 2 * n, [3])
+    for h in range(H):
+        np.testing.assert_allclose(out[0, h], _sdpa(Q[0, h], K[0, h], V[0, h]), rtol=0, atol=1e-12)
+
+
+def test_longformer_matches_sdpa_with_band_mask():
+    B, H, n, d, window = 1, 1, 384, 32, 64
+    G = [0, 1, 200]
+    Q, K, V = _rand((B, H, n, d), 13), _rand((B, H, n, d), 14), _rand((B, H, n, d), 15)
+    out = oracle_longformer(Q, K, V, window, G)
+    i = np.arange(n)
+    band = np.abs(i[:, None] - i[None, :]) <= window // 2
+    band[G, :] = True
+    band[:, G] = True
+    np.testing.assert_allclose(out[0, 0], _sdpa(Q[0, 0], K[0, 0], V[0, 0], mask=band), rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ softmax core
+
+def test_softmax_rows_sum_to_one_and_single_key():
+    rng = np.random.default_rng(0)
+    m, n, d = 40, 70, 16
+    q, k, v = rng.standard_normal((m, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    mask = rng.random((m, n)) < 0.3
+    mask[0] = False
+    p = masked_softmax_probs(q, k, mask)
+    sums = p.sum(axis=1)
+    assert abs(sums[0]) == 0.0, "a row without keys is all zero"
+    assert np.all(np.abs(sums[1:][mask[1:].any(axis=1)] - 1.0) < 1e-12)
+    assert np.all(p[~mask] == 0.0)
+    single = np.zeros((m, n), dtype=bool)
+    pick = rng.integers(0, n, size=m)
+    single[np.arange(m), pick] = True
+    np.testing.assert_allclose(masked_attention(q, k, v, single), v[pick], rtol=0, atol=0)
+
+
+def test_scalar_bruteforce_attention():
+    # Pure-Python loops with math.exp, written without numpy's vector ops.
+    rng = np.random.default_rng(1)
+    n, d, b, g, w, r = 24, 4, 4, 1, 3, 1
+    t = bigbird_random_table(17, 1, n, b, g, w, r)
+    q, k, v = rng.standard_normal((n, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    out = oracle_bigbird(q[None, None], k[None, None], v[None, None], b, g, w, t)[0, 0]
+    nb = n // b
+    for i in range(n):
+        neigh = _brute_bigbird_neigh(nb, g, w, t[0], i // b)
+        keys = [j for j in range(n) if j // b in neigh]
+        scores = [sum(q[i, c] * k[j, c] for c in range(d)) / math.sqrt(d) for j in keys]
+        mx = max(scores)
+        ex = [math.exp(s - mx) for s in scores]
+        tot = sum(ex)
+        ref = [sum(ex[a] * v[keys[a], c] for a in range(len(keys))) / tot for c in range(d)]
+        np.testing.assert_allclose(out[i], ref, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ work counts
+
+def _golden_counts():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "pair_counts.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            rows.append(line.split())
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_counts(), ids=lambda r: "-".join(r[:2]))
+def test_pair_counts_match_closed_form(row):
+    if row[0] == "bigbird":
+        n, b, g, w, r, expect = map(int, row[1:])
+        t = bigbird_random_table(0, 1, n, b, g, w, r)
+        assert bigbird_attended_pairs(n, b, g, w, t) == expect
+        if n <= 4096:
+            assert int(bigbird_allowed(n, b, g, w, t[0]).sum()) == expect
+    else:
+        n, window, ng, expect = map(int, row[1:])
+        assert longformer_attended_pairs(n, window, list(range(ng))) == expect
+
+
+def test_padded_pair_count_matches_mask():
+    n, b, g, w, r = 1024, 64, 2, 3, 3
+    t = bigbird_random_table(0, 2, n, b, g, w, r)
+    km = np.zeros((2, n), dtype=np.uint8)
+    km[0, :700] = 1
+    km[1, ::3] = 1
+    total = 0
+    for h in range(2):
+        for beta in range(2):
+            valid = km[beta] != 0
+            m = bigbird_allowed(n, b, g, w, t[h]) & valid[None, :] & valid[:, None]
+            total += int(m.sum())
+    assert bigbird_attended_pairs(n, b, g, w, t, key_mask=km, B=2) == total
