@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Throughput of the sparse-attention forward on GB300.
+
+One step = one `bigbird_attn_fwd` (or `longformer_attn_fwd`) call over the
+whole synthetic workload (default: BigBird-ITC, B=8, H=12, n=4096, d=64,
+b=64, g=2, w=3, r=3, bf16). Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Metric: useful TFLOP/s = 4*d * attended (valid query, allowed valid key)
+pairs / time. Inputs are resident in HBM before the timed region; L2 is
+flushed (256 MiB write) between timed steps, outside the timed events.
+`e2e` repeats the measurement through the same API with pinned HOST buffers,
+the host->device copies of Q, K, V and the device->host copy of O inside the
+timed region. `--impl reference` times the float64 CPU oracle instead.
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
+collective on the data path); the step time is the max over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_sparse_long_bigbird_gb300.workloads import HEADLINE, WORKLOADS  # noqa: E402
+
+METRIC = "useful TFLOP/s and tokens/s of sparse attn fwd at n=4096, % of bf16 tensor peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+TC_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_attn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline time budget")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(per_rank_ms, flops_per_rank_step, tokens_per_rank_step):
+    """Whole-job throughput: work of all ranks over the slowest rank's step time."""
+    world = len(per_rank_ms)
+    t = max(per_rank_ms) * 1e-3
+    return {
+        "ms_per_step": max(per_rank_ms),
+        "tflops": world * flops_per_rank_step / t / 1e12,
+        "tokens_per_s": world * tokens_per_rank_step / t,
+    }
+
+
+def shard_units(n_units, world, rank):
+    """Contiguous share of `n_units` independent (batch, head) units for `rank`."""
+    base, extra = divmod(n_units, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def read_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        entries = json.load(f)
+    sha = file_sha(TC_SOURCE)
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source_sha") == sha:
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_id)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_problem(wl, rank=0):
+    """Seeded synthetic inputs on the CPU, plus the useful-work count of one step."""
+    import torch
+
+    import block_sparse_long_bigbird_gb300 as sa
+    from block_sparse_long_bigbird_gb300 import accounting
+    from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv
+
+    Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, wl.dtype, sigma=wl.sigma, cfg_id=wl.cfg_id + 100 * rank)
+    km = make_key_mask(wl.B, wl.n) if wl.padded else None
+    prob = {"Q": Q, "K": K, "V": V, "key_mask": km}
+    if wl.kind == "bigbird":
+        table = sa.build_bigbird_pattern(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+        prob["table"] = table
+        if km is None:
+            pairs = accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, table.numpy()) * wl.B
+        else:
+            pairs = accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, table.numpy(), km.numpy())
+    else:
+        gidx = torch.arange(wl.n_global, dtype=torch.int32)
+        prob["gidx"] = gidx
+        pairs = accounting.longformer_pairs(wl.n, wl.window, gidx.numpy(),
+                                            None if km is None else km.numpy()) * wl.H
+        if km is None:
+            pairs *= wl.B
+    tokens = wl.B * wl.n if km is None else int(km.sum())
+    prob["pairs"] = pairs
+    prob["flops"] = 4.0 * wl.d * pairs
+    prob["tokens"] = tokens
+    return prob
+
+
+def call(wl, dev_t, out, stream=None):
+    import block_sparse_long_bigbird_gb300 as sa
+
+    if wl.kind == "bigbird":
+        sa.bigbird_attn_fwd(dev_t["Q"], dev_t["K"], dev_t["V"], wl.b, wl.g, wl.w, wl.r, dev_t["table"],
+                            dev_t.get("key_mask"), out=out, stream=stream)
+    else:
+        sa.longformer_attn_fwd(dev_t["Q"], dev_t["K"], dev_t["V"], wl.window, dev_t["gidx"],
+                               dev_t.get("key_mask"), out=out, stream=stream)
+
+
+def cpu_oracle_sample(wl, prob, budget_s):
+    """Time the float64 oracle on whole heads of the workload until `budget_s` is used."""
+    import numpy as np
+
+    from block_sparse_long_bigbird_gb300 import accounting
+    from oracle import oracle_bigbird, oracle_longformer
+
+    Q, K, V, km = prob["Q"], prob["K"], prob["V"], prob["key_mask"]
+    heads = [(beta, h) for beta in range(wl.B) for h in range(wl.H)]
+    done, flops = 0, 0.0
+    t0 = time.perf_counter()
+    for beta, h in heads:
+        sl = (slice(beta, beta + 1), slice(h, h + 1))
+        kmb = None if km is None else km[beta:beta + 1].numpy()
+        if wl.kind == "bigbird":
+            tab = prob["table"].numpy()[h:h + 1]
+            oracle_bigbird(Q[sl], K[sl], V[sl], wl.b, wl.g, wl.w, tab, key_mask=kmb)
+            flops += 4.0 * wl.d * accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, tab, kmb)
+        else:
+            oracle_longformer(Q[sl], K[sl], V[sl], wl.window, prob["gidx"].numpy(), key_mask=kmb)
+            flops += 4.0 * wl.d * accounting.longformer_pairs(wl.n, wl.window, prob["gidx"].numpy(), kmb)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        cores = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {len(heads)} (batch, head) pairs, all rows, float64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = WORKLOADS[args.workload]
+    prob = make_problem(wl)
+    budget = max(0.5, min(args.cpu_seconds, 120.0) / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, prob, 0.0)
+    vals, times = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = cpu_oracle_sample(wl, prob, budget)
+        times.append(time.perf_counter() - t0)
+        vals.append(r["value"])
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                         "sample": "per step: " + r["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    cfg = {"workload": f"{wl.name}: {wl.kind} B={wl.B} H={wl.H} n={wl.n} d={wl.d}",
+           "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "dtype": wl.dtype,
+           "l2": "flushed between timed steps (256 MiB write), inputs resident in HBM"}
+    if wl.kind == "bigbird":
+        cfg.update({"b": wl.b, "g": wl.g, "w": wl.w, "r": wl.r, "pattern_seed": wl.seed})
+    else:
+        cfg.update({"window": wl.window, "n_global": wl.n_global})
+    if wl.padded:
+        cfg["key_padding"] = "lengths ~ U[n/2, n] (seed 2000)"
+    return cfg
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import block_sparse_long_bigbird_gb300 as sa
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    wl = WORKLOADS[args.workload]
+    prob = make_problem(wl, rank)
+    dev_t = {k: v.to(dev) for k, v in prob.items() if hasattr(v, "to") and v is not None}
+    out = torch.empty_like(dev_t["Q"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        call(wl, dev_t, out)
+    torch.cuda.synchronize(dev)
+    status = sa.get_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after warm-up: {status}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    gpu_id = local
+    try:
+        gpu_id = torch.cuda.get_device_properties(dev).uuid
+        gpu_id = "GPU-" + str(gpu_id) if not str(gpu_id).startswith("GPU-") else str(gpu_id)
+    except Exception:
+        pass
+    barrier()
+    launches = 0
+    with ClockSampler(gpu_id) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            call(wl, dev_t, out)
+            ends[i].record(stream)
+            launches += sa.last_launch_count()
+        barrier()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    my_ms = sum(ms) / len(ms)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
+        gathered = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(gathered, t)
+        per_rank = [float(x.item()) for x in gathered]
+    else:
+        per_rank = [my_ms]
+    agg = aggregate(per_rank, prob["flops"], prob["tokens"])
+    status = sa.get_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timed steps: {status}")
+
+    peaks, peak_src = read_peaks()
+    kernel_tflops = prob["flops"] / (my_ms * 1e-3) / 1e12
+    kernel_name = "bigbird_tc_fwd" if wl.kind == "bigbird" else "longformer_tc_fwd"
+    traffic = read_traffic(kernel_name, wl.name)
+    roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)", "kernel": kernel_name,
+                "algorithmic_flops_per_launch": prob["flops"]}
+    hbm_bytes = 4 * wl.B * wl.H * wl.n * wl.d * (2 if wl.dtype == "bf16" else 4)
+    roofline["hbm_frac_of_min_bytes"] = hbm_bytes / (my_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
+
+    e2e = None
+    if not args.no_e2e:
+        host = {k: prob[k].pin_memory() for k in ("Q", "K", "V")}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        e_ms = []
+        for i in range(max(2, args.warmup) + args.steps):
+            flush.fill_(i & 0xFF)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for k in ("Q", "K", "V"):
+                dev_t[k].copy_(host[k], non_blocking=True)
+            call(wl, dev_t, out)
+            out_h.copy_(out, non_blocking=True)
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= max(2, args.warmup):
+                e_ms.append(s.elapsed_time(e))
+        e_t = sum(e_ms) / len(e_ms)
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([e_t], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_t = float(t.item())
+        e2e = {"value": world * prob["flops"] / (e_t * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e_t,
+               "h2d_bytes_per_step": sum(prob[k].numel() * prob[k].element_size() for k in ("Q", "K", "V")),
+               "d2h_bytes_per_step": out.numel() * out.element_size()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(wl, prob, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": agg["tflops"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": agg["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic (seeded torch.randn inputs, pattern seed 0)",
+            "config": workload_config(wl),
+            "tokens_per_s": agg["tokens_per_s"],
+            "useful_gflop_per_step": prob["flops"] / 1e9,
+            "frac_of_bf16_peak": agg["tflops"] / world / peaks["bf16_tflops"],
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks.summary(),
+            "per_step_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,71 @@
+"""Useful-work accounting for the sparse-attention forward.
+
+Useful FLOPs = 4 * d per attended pair (a valid query and an allowed valid
+key): 2 d for the score Q_i . K_j and 2 d for accumulating P_ij V_j. The pair
+count follows the patterns' definitions ("Big Bird" Sec. 2 / App. D;
+"Longformer" Sec. 3.1) at block granularity for BigBird and row by row for
+Longformer; it is host-side bookkeeping and never enters a kernel.
+"""
+
+import numpy as np
+
+
+def bigbird_block_sets(nb, g, w, rand_row):
+    """Sorted key-block list of every query block of one head."""
+    half = w // 2
+    sets = []
+    for j in range(nb):
+        if j < g:
+            sets.append(np.arange(nb))
+            continue
+        s = set(range(min(g, nb)))
+        s.update(range(max(0, j - half), min(nb, j + half + 1)))
+        s.update(int(x) for x in rand_row[j] if 0 <= x < nb)
+        sets.append(np.array(sorted(s)))
+    return sets
+
+
+def bigbird_pairs(n, b, g, w, table, key_mask=None):
+    """Attended pairs summed over batch entries and heads.
+
+    table: int [H, n // b, r]; key_mask: uint8/bool [B, n] or None (then B = 1
+    and the caller multiplies by the batch size).
+    """
+    table = np.asarray(table)
+    H, nb = table.shape[0], n // b
+    masks = [None] if key_mask is None else [np.asarray(m) != 0 for m in key_mask]
+    total = 0
+    for h in range(H):
+        sets = bigbird_block_sets(nb, g, w, table[h])
+        for valid in masks:
+            if valid is None:
+                total += sum(len(s) for s in sets) * b * b
+            else:
+                per_blk = valid.reshape(nb, b).sum(axis=1).astype(np.int64)
+                total += int(sum(per_blk[j] * per_blk[s].sum() for j, s in enumerate(sets)))
+    return total
+
+
+def longformer_pairs(n, window, global_idx, key_mask=None):
+    """Attended pairs of one head summed over batch entries (B = 1 if no mask)."""
+    half = window // 2
+    G = np.unique(np.asarray(global_idx, dtype=np.int64))
+    is_g = np.zeros(n, dtype=bool)
+    is_g[G] = True
+    masks = [np.ones(n, dtype=bool)] if key_mask is None else [np.asarray(m) != 0 for m in key_mask]
+    total = 0
+    for valid in masks:
+        cum = np.concatenate([[0], np.cumsum(valid)])
+        gv = np.cumsum(np.concatenate([[0], (is_g & valid).astype(np.int64)]))
+        n_valid = int(cum[-1])
+        for i in range(n):
+            if not valid[i]:
+                continue
+            if is_g[i]:
+                total += n_valid
+                continue
+            lo, hi = max(0, i - half), min(n - 1, i + half)
+            band = int(cum[hi + 1] - cum[lo])
+            outside = int(gv[n] - (gv[hi + 1] - gv[lo]))  # valid globals outside the band
+            total += band + outside
+    return total

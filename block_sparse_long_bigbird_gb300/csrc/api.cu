@@ -1,0 +1,273 @@
+// Host side of the C ABI: argument validation, kernel selection, the device
+// status word, scratch (workspace) management and options.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+// Per-device latched status (OR of sa::DeviceStatusBits). Every device that
+// loads the library holds its own copy of this module variable.
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    unsigned int *status = nullptr;  // device address of g_device_status
+    int cc_major = 0, cc_minor = 0, num_sms = 0;
+    void *ws = nullptr;  // library-owned scratch
+    size_t ws_bytes = 0;
+    void *user_ws = nullptr;  // caller-owned scratch (sa_set_workspace)
+    size_t user_ws_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::atomic<int> g_force_simt{0};
+std::atomic<long long> g_wait_limit{1ll << 22};
+std::atomic<int> g_max_splits{16};
+std::atomic<int> g_grid_ctas{0};
+thread_local int g_last_launches = 0;
+
+sa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
+
+// Returns the state of the current device, initialising it on first use.
+sa_status current_device(int *dev_out, DeviceState **st_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+    DeviceState &st = g_devices[dev];
+    if (!st.ready) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return SA_ERR_CUDA;
+        st.status = static_cast<unsigned int *>(addr);
+        if (cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SA_ERR_CUDA;
+        st.ready = true;
+    }
+    *dev_out = dev;
+    *st_out = &st;
+    return SA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sa_status check_tensors(const void *Q, const void *K, const void *V, const void *O) {
+    if (!Q || !K || !V || !O) return SA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SA_ERR_INVALID_ARG;
+    if (O == Q || O == K || O == V) return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+bool size_ok(int B, int H, int n, int d) {
+    if (B < 1 || H < 1 || n < 1) return false;
+    if (d != 64 && d != 128) return false;
+    // Offsets are computed in 64-bit, but per-head row counts and grid sizes are 32-bit.
+    if ((long long)B * H > (1ll << 30)) return false;
+    return true;
+}
+
+sa_status bigbird_args_ok(int B, int H, int n, int d, int b, int g, int w, int r, const int32_t *rand_idx) {
+    if (!size_ok(B, H, n, d)) return SA_ERR_INVALID_ARG;
+    if (b != 64 && b != 128) return SA_ERR_INVALID_ARG;
+    if (n % b != 0) return SA_ERR_INVALID_ARG;
+    if (g < 0 || g > n / b) return SA_ERR_INVALID_ARG;
+    if (w < 1 || (w % 2) == 0) return SA_ERR_INVALID_ARG;
+    if (r < 0 || (r > 0 && !rand_idx)) return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+sa_status longformer_args_ok(int B, int H, int n, int d, int window, const int32_t *global_idx, int n_global) {
+    if (!size_ok(B, H, n, d)) return SA_ERR_INVALID_ARG;
+    if (window < 0 || (window % 2) != 0) return SA_ERR_INVALID_ARG;
+    if (n_global < 0 || n_global > n || (n_global > 0 && !global_idx)) return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+sa::TcConfig tc_config(const DeviceState *st) {
+    sa::TcConfig cfg;
+    const int grid = g_grid_ctas.load();
+    cfg.grid_ctas = grid > 0 ? grid : (st ? st->num_sms : 148);
+    cfg.max_splits = g_max_splits.load();
+    cfg.wait_limit = g_wait_limit.load();
+    return cfg;
+}
+
+// Scratch for one call: the caller's region if one is set, else the
+// library-owned region, grown (and zeroed) on demand.
+sa_status get_workspace(DeviceState &st, size_t need, void **ptr) {
+    if (need == 0) {
+        *ptr = nullptr;
+        return SA_OK;
+    }
+    if (st.user_ws) {
+        if (st.user_ws_bytes < need) return SA_ERR_INVALID_ARG;
+        *ptr = st.user_ws;
+        return SA_OK;
+    }
+    if (st.ws_bytes < need) {
+        // Every call that used the old region was issued before this one; a
+        // device-wide sync makes the free safe whatever streams they ran on.
+        if (st.ws) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return SA_ERR_CUDA;
+            cudaFree(st.ws);
+            st.ws = nullptr;
+            st.ws_bytes = 0;
+        }
+        const size_t bytes = (need + 0xFFFFF) & ~(size_t)0xFFFFF;
+        if (cudaMalloc(&st.ws, bytes) != cudaSuccess) return SA_ERR_CUDA;
+        if (cudaMemset(st.ws, 0, bytes) != cudaSuccess) return SA_ERR_CUDA;
+        st.ws_bytes = bytes;
+    }
+    *ptr = st.ws;
+    return SA_OK;
+}
+
+sa_status run(const sa::Problem &prob_in, sa_dtype dtype, cudaStream_t stream) {
+    int dev = 0;
+    DeviceState *st = nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    sa_status s = current_device(&dev, &st);
+    if (s != SA_OK) return s;
+    if (st->cc_major != 10 || st->cc_minor != 3) return SA_ERR_UNSUPPORTED;
+    sa::Problem prob = prob_in;
+    prob.status = st->status;
+    int launches = 0;
+    cudaError_t e;
+    if (dtype == SA_FP32 || g_force_simt.load()) {
+        e = sa::launch_simt(prob, dtype, stream, &launches);
+    } else {
+        const sa::TcConfig cfg = tc_config(st);
+        void *ws = nullptr;
+        const size_t need = sa::tc_workspace_bytes(prob, cfg);
+        s = get_workspace(*st, need, &ws);
+        if (s != SA_OK) return s;
+        e = sa::launch_tc(prob, cfg, ws, need, stream, &launches);
+        if (e == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return SA_ERR_CUDA;
+    g_last_launches = launches;
+    return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sa_status bigbird_attn_fwd(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
+                           int b, int g, int w, int r, const int32_t *rand_idx, const uint8_t *key_mask,
+                           sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    sa_status s = check_tensors(Q, K, V, O);
+    if (s != SA_OK) return s;
+    s = bigbird_args_ok(B, H, n, d, b, g, w, r, rand_idx);
+    if (s != SA_OK) return s;
+    sa::Problem p = {};
+    p.kind = sa::kBigBird;
+    p.Q = Q; p.K = K; p.V = V; p.O = O;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.b = b; p.g = g; p.w = w; p.r = r;
+    p.rand_idx = r > 0 ? rand_idx : nullptr;
+    p.key_mask = key_mask;
+    return run(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
+                              int window, const int32_t *global_idx, int n_global, const uint8_t *key_mask,
+                              sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    sa_status s = check_tensors(Q, K, V, O);
+    if (s != SA_OK) return s;
+    s = longformer_args_ok(B, H, n, d, window, global_idx, n_global);
+    if (s != SA_OK) return s;
+    sa::Problem p = {};
+    p.kind = sa::kLongformer;
+    p.Q = Q; p.K = K; p.V = V; p.O = O;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.window = window;
+    p.global_idx = n_global > 0 ? global_idx : nullptr;
+    p.n_global = n_global;
+    p.key_mask = key_mask;
+    return run(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g) {
+    if (!size_ok(B, H, n, d) || (b != 64 && b != 128) || n % b != 0 || g < 0 || g > n / b) return 0;
+    sa::Problem p = {};
+    p.kind = sa::kBigBird;
+    p.B = B; p.H = H; p.n = n; p.d = d; p.b = b; p.g = g; p.w = 1;
+    return sa::tc_workspace_bytes(p, tc_config(nullptr));
+}
+
+size_t sa_longformer_workspace_bytes(int B, int H, int n, int d, int n_global) {
+    if (!size_ok(B, H, n, d) || n_global < 0 || n_global > n) return 0;
+    sa::Problem p = {};
+    p.kind = sa::kLongformer;
+    p.B = B; p.H = H; p.n = n; p.d = d; p.n_global = n_global;
+    return sa::tc_workspace_bytes(p, tc_config(nullptr));
+}
+
+sa_status sa_set_workspace(void *dev_ptr, size_t bytes) {
+    if ((reinterpret_cast<uintptr_t>(dev_ptr) & 255u) != 0) return SA_ERR_INVALID_ARG;
+    if (!dev_ptr && bytes > 0) return SA_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceState *st = nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    sa_status s = current_device(&dev, &st);
+    if (s != SA_OK) return s;
+    st->user_ws = dev_ptr;
+    st->user_ws_bytes = dev_ptr ? bytes : 0;
+    return SA_OK;
+}
+
+sa_status sa_get_last_device_status(sa_stream_t stream) {
+    int dev = 0;
+    DeviceState *st = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        sa_status s = current_device(&dev, &st);
+        if (s != SA_OK) return s;
+    }
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SA_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SA_ERR_CUDA;
+    }
+    if (word & sa::kDevTimeout) return SA_ERR_TIMEOUT;
+    if (word & sa::kDevBadIndex) return SA_ERR_BAD_INDEX;
+    return SA_OK;
+}
+
+const char *sa_status_string(sa_status status) {
+    switch (status) {
+        case SA_OK: return "SA_OK";
+        case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG";
+        case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED";
+        case SA_ERR_CUDA: return "SA_ERR_CUDA";
+        case SA_ERR_TIMEOUT: return "SA_ERR_TIMEOUT";
+        case SA_ERR_BAD_INDEX: return "SA_ERR_BAD_INDEX";
+    }
+    return "SA_ERR_UNKNOWN";
+}
+
+sa_status sa_set_option(int option, int64_t value) {
+    switch (option) {
+        case SA_OPT_FORCE_SIMT: g_force_simt = value != 0; return SA_OK;
+        case SA_OPT_WAIT_LIMIT: g_wait_limit = value > 0 ? (long long)value : (1ll << 22); return SA_OK;
+        case SA_OPT_MAX_SPLITS: g_max_splits = value < 1 ? 1 : (value > 64 ? 64 : (int)value); return SA_OK;
+        case SA_OPT_GRID_CTAS: g_grid_ctas = value < 0 ? 0 : (int)value; return SA_OK;
+    }
+    return SA_ERR_INVALID_ARG;
+}
+
+int sa_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sparse_attn.h"
+
+namespace sa {
+
+enum PatternKind { kBigBird = 0, kLongformer = 1 };
+
+// Device status bits latched by kernels (OR-ed into the per-device word).
+enum DeviceStatusBits : unsigned int {
+    kDevTimeout = 1u << 0,
+    kDevBadIndex = 1u << 1,
+};
+
+// One attention call, as validated by the host API.
+struct Problem {
+    int kind;
+    const void *Q, *K, *V;
+    void *O;
+    int B, H, n, d;
+    // BigBird-ITC
+    int b, g, w, r;
+    const int32_t *rand_idx;
+    // Longformer
+    int window;
+    const int32_t *global_idx;
+    int n_global;
+    // both
+    const uint8_t *key_mask;
+    unsigned int *status;  // device status word
+};
+
+// Exact SIMT kernels (fp32 arithmetic; bf16 or fp32 storage).
+cudaError_t launch_simt(const Problem &p, sa_dtype dtype, cudaStream_t stream, int *launches);
+
+// Tensor-core (tcgen05/TMEM/TMA) kernels for bf16.
+struct TcConfig {
+    int grid_ctas;     // persistent grid size
+    int max_splits;    // split-KV upper bound for global row tiles
+    long long wait_limit;
+};
+size_t tc_workspace_bytes(const Problem &p, const TcConfig &cfg);
+cudaError_t launch_tc(const Problem &p, const TcConfig &cfg, void *workspace, size_t ws_bytes,
+                      cudaStream_t stream, int *launches);
+
+}  // namespace sa

@@ -1,0 +1,189 @@
+/*
+ * sparse_attn.h - C ABI of the GB300 (sm_103a) sparse long-sequence attention
+ * forward library: BigBird-ITC block-sparse attention and Longformer
+ * sliding-window + global attention.
+ *
+ * What is computed (both patterns), per batch entry beta and head h:
+ *
+ *     O[i,:] = sum_{j in N(i)} softmax_j( Q[i,:] . K[j,:] / sqrt(d) ) V[j,:]
+ *
+ * i.e. the generalised attention Attn_D of "Big Bird: Transformers for
+ * Longer Sequences", Sec. 2, Eq. (AT), for one head and without the residual
+ * term, with the scaled dot-product form of "Longformer: The Long-Document
+ * Transformer", Sec. 3.1, Eq. (1). N(i) is the pattern's neighbourhood of
+ * query i intersected with the valid (unpadded) keys. A padded query row, or
+ * a row whose neighbourhood holds no valid key, is written as zeros.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors Q, K, V, O are device pointers to contiguous row-major
+ *    [B][H][n][d] arrays, d innermost, 16-byte aligned, all of the same dtype
+ *    (sa_dtype). O must not alias Q, K or V.
+ *  - The caller owns every buffer it passes; the library never frees caller
+ *    memory and keeps no pointer to it after the call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). The returned status reports argument errors found on the host
+ *    before anything is launched, and launch errors. Conditions the device
+ *    detects (an out-of-range index in a table, a pipeline wait that ran past
+ *    its bound) are latched in a per-device status word; read and clear it
+ *    with sa_get_last_device_status().
+ *  - Results are deterministic: identical inputs give bitwise-identical O
+ *    (no floating-point atomics; split reductions merge in a fixed order).
+ *  - The device that runs a call is the calling thread's current CUDA device.
+ */
+#ifndef SPARSE_ATTN_H
+#define SPARSE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque stream handle, ABI-identical to cudaStream_t. */
+typedef struct CUstream_st *sa_stream_t;
+
+typedef enum {
+    SA_OK = 0,
+    SA_ERR_INVALID_ARG = 1, /* a size, a flag or a pointer is outside the contract */
+    SA_ERR_UNSUPPORTED = 2, /* valid arguments this build does not run (e.g. no sm_103a device) */
+    SA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a kernel launch failed */
+    SA_ERR_TIMEOUT = 4,     /* device: a bounded pipeline wait expired; the kernel exited cleanly */
+    SA_ERR_BAD_INDEX = 5    /* device: rand_idx / global_idx held an out-of-range or unsorted entry */
+} sa_status;
+
+typedef enum {
+    SA_BF16 = 0, /* bf16 inputs/outputs; fp32 softmax and accumulation (tensor cores) */
+    SA_FP32 = 1  /* fp32 inputs/outputs; fp32 arithmetic throughout (no TF32) */
+} sa_dtype;
+
+/*
+ * build_bigbird_pattern - host-only. Draw BigBird's per-head random key blocks.
+ *
+ * Source: "Big Bird", Sec. 2 (random attention: each query attends r random
+ * keys) and App. E Tab. 8 (r = 3b tokens, i.e. r blocks of size b); the blog
+ * summary of BigBird, Sec. 2.1 and Sec. 4.2(3). The pages name no generator,
+ * so the draw is fixed here: one SplitMix64 stream (Steele, Lea & Flood 2014)
+ * started at `seed`; rows visited h = 0..H-1, then j = g..nb-1 (nb = n / b);
+ * the candidates of row j are the ascending key blocks kb in [0, nb) with
+ * kb >= g and |kb - j| > w / 2 (m of them); k = min(r, m) partial
+ * Fisher-Yates draws, draw t swapping position t with t + (u mod (m - t));
+ * the k chosen blocks are stored sorted ascending, then -1 up to r. Global
+ * rows (j < g) hold -1 only.
+ *
+ * out_host: caller-owned HOST buffer of H * (n / b) * r int32, layout [H][nb][r].
+ * Errors: SA_ERR_INVALID_ARG if out_host is NULL, H < 1, b < 1, n < b,
+ * n % b != 0, g < 0, g > nb, w < 1, w even, or r < 0.
+ */
+sa_status build_bigbird_pattern(uint64_t seed, int H, int n, int b, int g, int w, int r,
+                                int32_t *out_host);
+
+/*
+ * bigbird_attn_fwd - BigBird-ITC block-sparse attention forward.
+ *
+ * Source: "Big Bird", Sec. 2 (Eq. AT; random, window and global components),
+ * App. D (blockified pattern on blocks of b tokens, Eq. 13 and Fig. 6: the
+ * block-sparse product equals the sparse matrix of Fig. 3(d)), App. E Tab. 8
+ * (ITC: g = 2b, w = 3b, r = 3b tokens); blog summary Sec. 2.1-2.3.
+ *
+ * Query block qb = i / b sees key block kb = j / b iff qb < g (global rows
+ * attend everything), or kb < g (everyone attends the global blocks), or
+ * |qb - kb| <= w / 2 (window of w blocks, clipped at the sequence ends), or kb
+ * is listed in rand_idx[h][qb][:].
+ *
+ * Sizes: B, H >= 1; d in {64, 128}; b in {64, 128}; n a multiple of b;
+ * 0 <= g <= n / b; w odd and >= 1; r >= 0.
+ * rand_idx: DEVICE int32 [H][n/b][r] (e.g. from build_bigbird_pattern, copied
+ *   to the device), shared by all batch entries; -1 entries are ignored. May
+ *   be NULL when r == 0. An entry outside [-1, n/b) is skipped and latches
+ *   SA_ERR_BAD_INDEX.
+ * key_mask: DEVICE uint8 [B][n], nonzero = valid token, or NULL (all valid).
+ * dtype: SA_BF16 (tensor-core path) or SA_FP32 (exact fp32 SIMT path).
+ * Scratch: global query blocks may be split across CTAs (split-KV) with a
+ *   fixed-order merge; their partials live in the workspace (see
+ *   sa_bigbird_workspace_bytes / sa_set_workspace).
+ * Errors: SA_ERR_INVALID_ARG for any size or pointer outside the contract,
+ *   SA_ERR_UNSUPPORTED if the current device is not sm_103, SA_ERR_CUDA if a
+ *   launch fails.
+ */
+sa_status bigbird_attn_fwd(const void *Q, const void *K, const void *V, void *O,
+                           int B, int H, int n, int d, int b, int g, int w, int r,
+                           const int32_t *rand_idx, const uint8_t *key_mask,
+                           sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * longformer_attn_fwd - Longformer sliding-window + symmetric global attention.
+ *
+ * Source: "Longformer", Sec. 3.1 (sliding window: window / 2 tokens on each
+ * side; global attention is symmetric: a global token attends every token and
+ * every token attends it) and Eq. (1); Sec. 3.2 / App. A (banded product).
+ *
+ * Token i sees token j iff i or j is global, or |i - j| <= window / 2.
+ *
+ * Sizes: B, H >= 1; n >= 1; d in {64, 128}; window even and >= 0.
+ * global_idx: DEVICE int32 [n_global], strictly increasing positions in
+ *   [0, n); may be NULL when n_global == 0. Entries that break the order or
+ *   the range are skipped and latch SA_ERR_BAD_INDEX.
+ * n_global: 0 <= n_global <= n.
+ * key_mask: DEVICE uint8 [B][n] or NULL, as for bigbird_attn_fwd.
+ * Errors: as for bigbird_attn_fwd.
+ */
+sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void *O,
+                              int B, int H, int n, int d, int window,
+                              const int32_t *global_idx, int n_global,
+                              const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * Scratch (workspace) sizing. The split-KV partials of the global rows and the
+ * kernel's work counters need device scratch. By default the library allocates
+ * it once per device (cudaMalloc, zeroed) and grows it on demand; a caller that
+ * manages memory itself passes a region with sa_set_workspace instead.
+ * Returns the bytes one call with these sizes needs (0 if the sizes are invalid).
+ */
+size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g);
+size_t sa_longformer_workspace_bytes(int B, int H, int n, int d, int n_global);
+
+/*
+ * sa_set_workspace - use a caller-owned, device-resident scratch region on the
+ * current device (dev_ptr 256-byte aligned, `bytes` large enough for the
+ * calls that follow). The region must start zeroed; the library leaves its
+ * counters at zero after every call that completes. Pass NULL/0 to go back to
+ * the library-owned scratch. Calls sharing one region must be stream-ordered.
+ * Errors: SA_ERR_INVALID_ARG for a misaligned pointer or NULL with bytes > 0.
+ */
+sa_status sa_set_workspace(void *dev_ptr, size_t bytes);
+
+/*
+ * sa_get_last_device_status - synchronise `stream`, then read and clear the
+ * current device's latched device status (SA_OK, SA_ERR_TIMEOUT or
+ * SA_ERR_BAD_INDEX). Returns SA_ERR_CUDA if the synchronisation fails.
+ */
+sa_status sa_get_last_device_status(sa_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *sa_status_string(sa_status status);
+
+/*
+ * Options (process-wide; set them before issuing calls):
+ *  SA_OPT_FORCE_SIMT   value != 0: run bf16 calls on the exact SIMT kernels
+ *                      instead of the tensor-core kernels (a cross-check path).
+ *  SA_OPT_WAIT_LIMIT   iteration bound of every pipeline wait in the
+ *                      tensor-core kernels (default 1<<22, about a second);
+ *                      value <= 0 restores the default.
+ *  SA_OPT_MAX_SPLITS   upper bound on split-KV chunks per global row tile
+ *                      (default 16, 1 disables splitting).
+ *  SA_OPT_GRID_CTAS    persistent-grid size (0 = one CTA per SM).
+ * Returns SA_ERR_INVALID_ARG for an unknown option.
+ */
+enum { SA_OPT_FORCE_SIMT = 1, SA_OPT_WAIT_LIMIT = 2, SA_OPT_MAX_SPLITS = 3, SA_OPT_GRID_CTAS = 4 };
+sa_status sa_set_option(int option, int64_t value);
+
+/* Number of kernel launches issued by the calling thread's last successful
+ * attention call (for launch accounting). */
+int sa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTN_H */

@@ -1,0 +1,104 @@
+"""Shared helpers for the GPU parity tests: run a case through the C ABI and
+compare with the float64 oracle on the same seeded inputs."""
+
+import numpy as np
+import torch
+
+import block_sparse_long_bigbird_gb300 as sa
+from block_sparse_long_bigbird_gb300.inputs import make_qkv
+from oracle import oracle_bigbird, oracle_longformer
+
+PATHS = ["simt", "tc"]
+
+
+def set_path(path):
+    sa.set_option(sa.SA_OPT_FORCE_SIMT, 1 if path == "simt" else 0)
+
+
+def gpu_bigbird(Q, K, V, b, g, w, r, table, key_mask=None, path="tc"):
+    dev = torch.device("cuda:0")
+    set_path(path)
+    try:
+        O = sa.bigbird_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), b, g, w, r,
+                                table.to(dev) if r > 0 else None,
+                                None if key_mask is None else key_mask.to(dev))
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    return O
+
+
+def gpu_longformer(Q, K, V, window, gidx, key_mask=None, path="tc"):
+    dev = torch.device("cuda:0")
+    set_path(path)
+    try:
+        O = sa.longformer_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), window,
+                                   None if gidx is None else gidx.to(dev),
+                                   None if key_mask is None else key_mask.to(dev))
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    return O
+
+
+def assert_close(got, ref, tol_max, tol_mean, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= tol_max and err.mean() <= tol_mean, \
+        f"{what}: max|err| {err.max():.3e} (tol {tol_max}), mean|err| {err.mean():.3e} (tol {tol_mean})"
+    return err.max(), err.mean()
+
+
+def bigbird_case(B, H, n, d, b, g, w, r, dtype="bf16", sigma=1.0, cfg_id=50, key_mask=None,
+                 seed=0, path="tc", rows=None, heads=None, tol=(2e-2, 2e-3)):
+    """Run BigBird on the GPU and compare (all rows, or `rows` of the `heads` (beta, h) pairs)."""
+    Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
+    table = sa.build_bigbird_pattern(seed, H, n, b, g, w, r)
+    O = gpu_bigbird(Q, K, V, b, g, w, r, table, key_mask, path).float().cpu()
+    heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
+    for beta, h in heads:
+        km = None if key_mask is None else key_mask[beta:beta + 1].numpy()
+        ref = oracle_bigbird(Q[beta:beta + 1, h:h + 1], K[beta:beta + 1, h:h + 1], V[beta:beta + 1, h:h + 1],
+                             b, g, w, table.numpy()[h:h + 1], key_mask=km, rows=rows)[0, 0]
+        got = O[beta, h].numpy() if rows is None else O[beta, h].numpy()[np.asarray(rows)]
+        assert_close(got, ref, *tol, what=f"bigbird beta={beta} h={h}")
+        if key_mask is not None:
+            pad = np.nonzero(key_mask[beta].numpy() == 0)[0]
+            if rows is not None:
+                pad = np.intersect1d(pad, np.asarray(rows))
+            assert np.all(O[beta, h].numpy()[pad] == 0.0), "padded query rows must be exactly 0"
+    return O
+
+
+def longformer_case(B, H, n, d, window, gidx, dtype="bf16", cfg_id=60, key_mask=None, path="tc",
+                    rows=None, heads=None, tol=(2e-2, 2e-3)):
+    Q, K, V = make_qkv(B, H, n, d, dtype, cfg_id=cfg_id)
+    O = gpu_longformer(Q, K, V, window, gidx, key_mask, path).float().cpu()
+    heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
+    g_np = np.zeros(0, dtype=np.int64) if gidx is None else gidx.numpy()
+    for beta, h in heads:
+        km = None if key_mask is None else key_mask[beta:beta + 1].numpy()
+        ref = oracle_longformer(Q[beta:beta + 1, h:h + 1], K[beta:beta + 1, h:h + 1], V[beta:beta + 1, h:h + 1],
+                                window, g_np, key_mask=km, rows=rows)[0, 0]
+        got = O[beta, h].numpy() if rows is None else O[beta, h].numpy()[np.asarray(rows)]
+        assert_close(got, ref, *tol, what=f"longformer beta={beta} h={h}")
+        if key_mask is not None:
+            pad = np.nonzero(key_mask[beta].numpy() == 0)[0]
+            if rows is not None:
+                pad = np.intersect1d(pad, np.asarray(rows))
+            assert np.all(O[beta, h].numpy()[pad] == 0.0), "padded query rows must be exactly 0"
+    return O
+
+
+def sampled_bigbird_rows(n, b, g, n_random_blocks=8, seed=0):
+    """Global rows, first/second-to-last/last query blocks and seeded random blocks."""
+    nb = n // b
+    rng = np.random.default_rng(seed)
+    blocks = set(range(min(g, nb))) | {min(g, nb - 1), nb - 2, nb - 1}
+    blocks |= set(int(x) for x in rng.choice(np.arange(nb), size=min(n_random_blocks, nb), replace=False))
+    return np.concatenate([np.arange(j * b, (j + 1) * b) for j in sorted(blocks) if 0 <= j < nb])

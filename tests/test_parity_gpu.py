@@ -1,0 +1,206 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the float64 oracle.
+
+Tolerances: bf16 inputs max|err| <= 2e-2 and mean|err| <= 2e-3; fp32 inputs
+max|err| <= 1e-4. Every case runs on both kernel families: "tc" (the bf16
+tcgen05 pipeline; fp32 always runs on SIMT) and "simt" (the exact SIMT kernels).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_long_bigbird_gb300 as sa
+from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv, make_random_key_mask
+from block_sparse_long_bigbird_gb300.workloads import WORKLOADS
+from parity_util import (PATHS, bigbird_case, gpu_bigbird, longformer_case, sampled_bigbird_rows)
+
+pytestmark = pytest.mark.gpu
+
+FP32_TOL = (1e-4, 1e-5)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    sa._lib.lib()
+    yield
+    sa.set_option(sa.SA_OPT_FORCE_SIMT, 0)
+
+
+# ------------------------------------------------------------- BigBird, small full compares
+
+BIGBIRD_SMALL = [
+    # B, H, n,    d,   b,   g, w, r
+    (2, 3, 512, 64, 64, 2, 3, 3),
+    (1, 2, 192, 64, 64, 1, 3, 3),      # nb = 3: odd block count, no random candidates
+    (1, 2, 1024, 128, 128, 2, 3, 3),
+    (1, 1, 768, 128, 64, 1, 5, 2),
+    (1, 2, 1024, 64, 128, 2, 3, 3),
+    (2, 1, 640, 64, 64, 0, 1, 0),      # block-diagonal (App. D Eq. 13)
+    (1, 1, 512, 64, 64, 1, 1, 8),      # r >= nb: full attention
+    (1, 2, 2048, 64, 64, 3, 7, 4),
+    (1, 1, 1280, 64, 64, 2, 3, 3),     # nb = 20
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", BIGBIRD_SMALL, ids=lambda c: "B{}H{}n{}d{}b{}g{}w{}r{}".format(*c))
+def test_bigbird_small(case, path):
+    bigbird_case(*case, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_fp32_config(path):
+    wl = WORKLOADS["bigbird_fp32_n1024"]
+    bigbird_case(wl.B, wl.H, wl.n, wl.d, wl.b, wl.g, wl.w, wl.r, dtype="fp32", cfg_id=wl.cfg_id,
+                 path=path, tol=FP32_TOL)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_fp32_d128(path):
+    bigbird_case(1, 2, 1024, 128, 128, 2, 3, 3, dtype="fp32", path=path, tol=FP32_TOL)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_prefix_padding(path):
+    B, n = 3, 1024
+    km = make_key_mask(B, n, seed=7)
+    bigbird_case(B, 2, n, 64, 64, 2, 3, 3, key_mask=km, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_random_padding(path):
+    B, n = 2, 1024
+    km = make_random_key_mask(B, n, seed=8, p_valid=0.7)
+    bigbird_case(B, 2, n, 64, 64, 2, 3, 3, key_mask=km, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_fully_padded_sequence(path):
+    B, n = 2, 512
+    km = torch.ones(B, n, dtype=torch.uint8)
+    km[1] = 0
+    km[0, 300:] = 0
+    bigbird_case(B, 1, n, 64, 64, 2, 3, 3, key_mask=km, path=path)
+
+
+# ------------------------------------------------------------- Longformer, small full compares
+
+LONGFORMER_SMALL = [
+    # B, H, n,    d,  window, globals
+    (1, 2, 1000, 64, 64, [0, 5, 500, 999]),
+    (2, 1, 512, 64, 0, []),
+    (1, 1, 256, 64, 1024, [3]),
+    (1, 2, 1024, 128, 256, [0, 1, 2, 3]),
+    (1, 1, 2048, 64, 512, list(range(16))),
+    (1, 1, 777, 64, 100, [776]),
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", LONGFORMER_SMALL, ids=lambda c: "B{}H{}n{}d{}win{}".format(*c[:5]))
+def test_longformer_small(case, path):
+    B, H, n, d, window, G = case
+    gidx = torch.tensor(G, dtype=torch.int32) if G else None
+    longformer_case(B, H, n, d, window, gidx, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_many_globals_and_padding(path):
+    from block_sparse_long_bigbird_gb300.inputs import make_global_positions
+
+    B, n = 2, 1536
+    gidx = make_global_positions(n, 150, seed=5)
+    km = make_key_mask(B, n, seed=9)
+    longformer_case(B, 1, n, 64, 128, gidx, key_mask=km, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_fp32(path):
+    gidx = torch.tensor([0, 100], dtype=torch.int32)
+    longformer_case(1, 1, 640, 64, 64, gidx, dtype="fp32", path=path, tol=FP32_TOL)
+
+
+# ------------------------------------------------------------- full-size workloads (sampled rows)
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_n4096_workload(path):
+    wl = WORKLOADS["bigbird_bf16_n4096"]
+    rows = sampled_bigbird_rows(wl.n, wl.b, wl.g, seed=1)
+    bigbird_case(wl.B, wl.H, wl.n, wl.d, wl.b, wl.g, wl.w, wl.r, cfg_id=wl.cfg_id, path=path,
+                 rows=rows, heads=[(0, 0), (3, 7), (7, 11)])
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_n4096_workload(path):
+    wl = WORKLOADS["longformer_bf16_n4096"]
+    gidx = torch.arange(wl.n_global, dtype=torch.int32)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([np.arange(0, 300), np.arange(wl.n - 300, wl.n),
+                                     rng.choice(wl.n, 600, replace=False)]))
+    longformer_case(wl.B, wl.H, wl.n, wl.d, wl.window, gidx, cfg_id=wl.cfg_id, path=path, rows=rows,
+                    heads=[(0, 0), (1, 5), (3, 11)])
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_n16384_padded_workload(path):
+    wl = WORKLOADS["bigbird_bf16_n16384_padded"]
+    km = make_key_mask(wl.B, wl.n)
+    rows = sampled_bigbird_rows(wl.n, wl.b, wl.g, seed=3)
+    bigbird_case(wl.B, wl.H, wl.n, wl.d, wl.b, wl.g, wl.w, wl.r, cfg_id=wl.cfg_id, key_mask=km, path=path,
+                 rows=rows, heads=[(0, 0), (1, 15)])
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_n65536_d128_workload(path):
+    wl = WORKLOADS["bigbird_bf16_n65536_d128"]
+    rows = sampled_bigbird_rows(wl.n, wl.b, wl.g, n_random_blocks=4, seed=4)
+    bigbird_case(wl.B, wl.H, wl.n, wl.d, wl.b, wl.g, wl.w, wl.r, sigma=wl.sigma, cfg_id=wl.cfg_id,
+                 path=path, rows=rows, heads=[(0, 0), (0, 13)])
+
+
+# ------------------------------------------------------------- properties
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_deterministic(path):
+    wl = WORKLOADS["bigbird_bf16_n4096"]
+    Q, K, V = make_qkv(2, wl.H, wl.n, wl.d, "bf16", cfg_id=wl.cfg_id)
+    table = sa.build_bigbird_pattern(0, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+    O1 = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path=path)
+    O2 = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path=path)
+    assert torch.equal(O1, O2)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bad_random_index_latches_status(path):
+    B, H, n, d, b, g, w, r = 1, 1, 512, 64, 64, 2, 3, 3
+    Q, K, V = (t.cuda() for t in make_qkv(B, H, n, d, "bf16", cfg_id=70))
+    table = sa.build_bigbird_pattern(0, H, n, b, g, w, r)
+    table[0, 5, 1] = 1000  # out of [-1, nb): skipped by the kernel, latched as SA_ERR_BAD_INDEX
+    sa.set_option(sa.SA_OPT_FORCE_SIMT, 1 if path == "simt" else 0)
+    try:
+        sa.bigbird_attn_fwd(Q, K, V, b, g, w, r, table.cuda())
+        assert sa.get_last_device_status() == sa._lib.SA_ERR_BAD_INDEX
+        assert sa.get_last_device_status() == 0  # reading clears it
+    finally:
+        sa.set_option(sa.SA_OPT_FORCE_SIMT, 0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_unsorted_global_index_latches_status(path):
+    Q, K, V = (t.cuda() for t in make_qkv(1, 1, 512, 64, "bf16", cfg_id=71))
+    gidx = torch.tensor([5, 3, 600], dtype=torch.int32).cuda()
+    sa.set_option(sa.SA_OPT_FORCE_SIMT, 1 if path == "simt" else 0)
+    try:
+        sa.longformer_attn_fwd(Q, K, V, 64, gidx)
+        assert sa.get_last_device_status() == sa._lib.SA_ERR_BAD_INDEX
+    finally:
+        sa.set_option(sa.SA_OPT_FORCE_SIMT, 0)
+
+
+def test_tc_and_simt_agree_closely():
+    wl = WORKLOADS["bigbird_bf16_n4096"]
+    Q, K, V = make_qkv(1, 4, wl.n, wl.d, "bf16", cfg_id=72)
+    table = sa.build_bigbird_pattern(0, 4, wl.n, wl.b, wl.g, wl.w, wl.r)
+    a = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path="tc").float()
+    b = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path="simt").float()
+    assert (a - b).abs().max().item() <= 2e-2
