@@ -32,7 +32,7 @@ struct SplitMix64 {
 
 extern "C" sa_status build_bigbird_pattern(uint64_t seed, int H, int n, int b, int g, int w, int r,
                                            int32_t *out_host) {
-    if (!out_host || H < 1 || b < 1 || n < b || n % b != 0 || g < 0 || w < 1 || (w % 2) == 0 || r < 0)
+    if ((!out_host && r > 0) || H < 1 || b < 1 || n < b || n % b != 0 || g < 0 || w < 1 || (w % 2) == 0 || r < 0)
         return SA_ERR_INVALID_ARG;
     const int nb = n / b;
     if (g > nb) return SA_ERR_INVALID_ARG;

@@ -71,8 +71,9 @@ typedef enum {
  * the k chosen blocks are stored sorted ascending, then -1 up to r. Global
  * rows (j < g) hold -1 only.
  *
- * out_host: caller-owned HOST buffer of H * (n / b) * r int32, layout [H][nb][r].
- * Errors: SA_ERR_INVALID_ARG if out_host is NULL, H < 1, b < 1, n < b,
+ * out_host: caller-owned HOST buffer of H * (n / b) * r int32, layout [H][nb][r]
+ *   (may be NULL when r == 0: there is nothing to write).
+ * Errors: SA_ERR_INVALID_ARG if out_host is NULL with r > 0, H < 1, b < 1, n < b,
  * n % b != 0, g < 0, g > nb, w < 1, w even, or r < 0.
  */
 sa_status build_bigbird_pattern(uint64_t seed, int H, int n, int b, int g, int w, int r,
