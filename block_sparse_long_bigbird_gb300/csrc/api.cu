@@ -241,7 +241,15 @@ sa_status sa_get_last_device_status(sa_stream_t stream) {
         const unsigned int zero = 0;
         if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SA_ERR_CUDA;
     }
-    if (word & sa::kDevTimeout) return SA_ERR_TIMEOUT;
+    if (word & sa::kDevTimeout) {
+        // An aborted kernel may leave scheduler or split-merge counters set:
+        // zero the scratch so the next call starts clean.
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (st->ws && cudaMemset(st->ws, 0, st->ws_bytes) != cudaSuccess) return SA_ERR_CUDA;
+        if (st->user_ws && cudaMemset(st->user_ws, 0, st->user_ws_bytes) != cudaSuccess) return SA_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return SA_ERR_CUDA;
+        return SA_ERR_TIMEOUT;
+    }
     if (word & sa::kDevBadIndex) return SA_ERR_BAD_INDEX;
     return SA_OK;
 }
