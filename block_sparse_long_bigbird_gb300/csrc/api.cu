@@ -21,8 +21,10 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0, num_sms = 0;
     void *ws = nullptr;  // library-owned scratch
     size_t ws_bytes = 0;
+    size_t ws_clean = 0;  // [0, ws_clean) of `ws` is known to be zero between calls
     void *user_ws = nullptr;  // caller-owned scratch (sa_set_workspace)
     size_t user_ws_bytes = 0;
+    size_t user_ws_clean = 0;
 };
 
 std::mutex g_mutex;
@@ -124,6 +126,7 @@ sa_status get_workspace(DeviceState &st, size_t need, void **ptr) {
         if (cudaMalloc(&st.ws, bytes) != cudaSuccess) return SA_ERR_CUDA;
         if (cudaMemset(st.ws, 0, bytes) != cudaSuccess) return SA_ERR_CUDA;
         st.ws_bytes = bytes;
+        st.ws_clean = bytes;
     }
     *ptr = st.ws;
     return SA_OK;
@@ -148,8 +151,18 @@ sa_status run(const sa::Problem &prob_in, sa_dtype dtype, cudaStream_t stream) {
         const size_t need = sa::tc_workspace_bytes(prob, cfg);
         s = get_workspace(*st, need, &ws);
         if (s != SA_OK) return s;
+        // The kernel needs its counters zero at entry. A call leaves its own
+        // counters zero but writes split partials past them, and the next call
+        // (another shape) may place counters over those bytes: clear them then.
+        size_t *clean = (ws == st->user_ws) ? &st->user_ws_clean : &st->ws_clean;
+        const size_t counters = sa::tc_workspace_counter_bytes(prob, cfg);
+        if (ws && counters > *clean) {
+            if (cudaMemsetAsync(ws, 0, counters, stream) != cudaSuccess) return SA_ERR_CUDA;
+            *clean = counters;
+        }
         e = sa::launch_tc(prob, cfg, ws, need, stream, &launches);
         if (e == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
+        if (e == cudaSuccess && need > counters) *clean = counters;  // partials dirty [counters, need)
     }
     if (e != cudaSuccess) return SA_ERR_CUDA;
     g_last_launches = launches;
@@ -223,6 +236,7 @@ sa_status sa_set_workspace(void *dev_ptr, size_t bytes) {
     if (s != SA_OK) return s;
     st->user_ws = dev_ptr;
     st->user_ws_bytes = dev_ptr ? bytes : 0;
+    st->user_ws_clean = st->user_ws_bytes;  // the caller hands it over zeroed
     return SA_OK;
 }
 
@@ -247,6 +261,8 @@ sa_status sa_get_last_device_status(sa_stream_t stream) {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (st->ws && cudaMemset(st->ws, 0, st->ws_bytes) != cudaSuccess) return SA_ERR_CUDA;
         if (st->user_ws && cudaMemset(st->user_ws, 0, st->user_ws_bytes) != cudaSuccess) return SA_ERR_CUDA;
+        st->ws_clean = st->ws_bytes;
+        st->user_ws_clean = st->user_ws_bytes;
         if (cudaDeviceSynchronize() != cudaSuccess) return SA_ERR_CUDA;
         return SA_ERR_TIMEOUT;
     }

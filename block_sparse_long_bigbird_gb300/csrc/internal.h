@@ -44,6 +44,9 @@ struct TcConfig {
     long long wait_limit;
 };
 size_t tc_workspace_bytes(const Problem &p, const TcConfig &cfg);
+// Leading bytes of the tensor-core scratch that must be zero when a call
+// starts (scheduler and merge counters).
+size_t tc_workspace_counter_bytes(const Problem &p, const TcConfig &cfg);
 cudaError_t launch_tc(const Problem &p, const TcConfig &cfg, void *workspace, size_t ws_bytes,
                       cudaStream_t stream, int *launches);
 

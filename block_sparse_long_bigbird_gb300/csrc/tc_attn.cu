@@ -891,6 +891,12 @@ size_t tc_workspace_bytes(const Problem &p, const TcConfig &cfg) {
     return ws_layout(bigbird_geometry(p, cfg), p.d).total;
 }
 
+size_t tc_workspace_counter_bytes(const Problem &p, const TcConfig &cfg) {
+    if (p.kind != kBigBird) return 256;
+    const WsLayout L = ws_layout(bigbird_geometry(p, cfg), p.d);
+    return L.part_o ? L.part_o : L.total;
+}
+
 cudaError_t launch_tc(const Problem &p, const TcConfig &cfg, void *ws, size_t ws_bytes, cudaStream_t stream,
                       int *launches) {
     *launches = 0;

@@ -204,3 +204,12 @@ def test_tc_and_simt_agree_closely():
     a = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path="tc").float()
     b = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path="simt").float()
     assert (a - b).abs().max().item() <= 2e-2
+
+
+def test_scratch_reuse_across_shapes():
+    # Calls of different shapes share the library-owned scratch: split partials
+    # of one call must not leak into the merge counters of the next.
+    shapes = [(1, 2, 16384, 64, 64), (1, 2, 16384, 128, 128), (2, 2, 8192, 64, 64), (1, 3, 16384, 128, 128)]
+    for (B, H, n, d, b) in shapes:
+        rows = np.concatenate([np.arange(0, 2 * b), np.arange(n - b, n)])
+        bigbird_case(B, H, n, d, b, 2, 3, 3, cfg_id=81, path="tc", rows=rows, heads=[(0, 0), (B - 1, H - 1)])
