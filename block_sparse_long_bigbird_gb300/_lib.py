@@ -45,7 +45,9 @@ SIGNATURES = {
     "sa_status_string": (ctypes.c_char_p, [_I]),
     "sa_set_option": (_I, [_I, ctypes.c_int64]),
     "sa_last_launch_count": (_I, []),
+    "bigbird_attn_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP]),
 }
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _lib = None

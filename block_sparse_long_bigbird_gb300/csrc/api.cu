@@ -295,3 +295,70 @@ sa_status sa_set_option(int option, int64_t value) {
 int sa_last_launch_count(void) { return g_last_launches; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// bigbird_attn_fwd_noalloc: the BigBird forward for callers that may not
+// allocate device memory (see sparse_attn.h). Its scratch is the fixed array
+// below instead of a cudaMalloc'ed region.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on each device. The array's host-side
+// name is only a stand-in: a kernel must be given this address instead.
+void *g_noalloc_addr[kMaxDevices];
+
+// Looks the address up once per device, with that device current.
+sa_status noalloc_scratch(int dev, void **out) {
+    if (!g_noalloc_addr[dev]) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) return SA_ERR_CUDA;
+        g_noalloc_addr[dev] = addr;
+    }
+    *out = g_noalloc_addr[dev];
+    return SA_OK;
+}
+
+}  // namespace
+
+extern "C" sa_status bigbird_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O, int B, int H,
+                                              int n, int d, int b, int g, int w, int r, const int32_t *rand_idx,
+                                              const uint8_t *key_mask, sa_stream_t stream) {
+    sa_status s = check_tensors(Q, K, V, O);
+    if (s != SA_OK) return s;
+    s = bigbird_args_ok(B, H, n, d, b, g, w, r, rand_idx);
+    if (s != SA_OK) return s;
+    sa::Problem p = {};
+    p.kind = sa::kBigBird;
+    p.Q = Q; p.K = K; p.V = V; p.O = O;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.b = b; p.g = g; p.w = w; p.r = r;
+    p.rand_idx = r > 0 ? rand_idx : nullptr;
+    p.key_mask = key_mask;
+    // The scratch need depends only on the sizes and the split option: reject
+    // oversize calls before touching the device.
+    const sa::TcConfig size_cfg = tc_config(nullptr);
+    const size_t need = sa::tc_workspace_bytes(p, size_cfg);
+    if (need > SA_NOALLOC_SCRATCH_BYTES) return SA_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    DeviceState *st = nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    s = current_device(&dev, &st);
+    if (s != SA_OK) return s;
+    if (st->cc_major != 10 || st->cc_minor != 3) return SA_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    s = noalloc_scratch(dev, &scratch);
+    if (s != SA_OK) return s;
+    p.status = st->status;
+    const sa::TcConfig cfg = tc_config(st);
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t zero_bytes = sa::tc_workspace_counter_bytes(p, cfg);
+    if (cudaMemsetAsync(scratch, 0, zero_bytes, cs) != cudaSuccess) return SA_ERR_CUDA;
+    int launches = 0;
+    const cudaError_t e = sa::launch_tc(p, cfg, scratch, need, cs, &launches);
+    if (e == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return SA_ERR_CUDA;
+    g_last_launches = launches;
+    return SA_OK;
+}

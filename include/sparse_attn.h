@@ -183,6 +183,41 @@ sa_status sa_set_option(int option, int64_t value);
  * attention call (for launch accounting). */
 int sa_last_launch_count(void);
 
+/*
+ * bigbird_attn_fwd_noalloc - bigbird_attn_fwd for callers that must not
+ * allocate device memory. (The pages have no counterpart: this is a
+ * deployment variant of the same computation.)
+ *
+ * Who needs it: bigbird_attn_fwd sizes its scratch on the first call and
+ * grows it with cudaMalloc later, and cudaMalloc may synchronise the whole
+ * device and can fail once memory is fragmented. Some callers cannot accept
+ * that: serving processes that reserve device memory at start-up and forbid
+ * allocation on the request path, and plugins hosted by a framework that owns
+ * the device's memory and does not let extensions allocate. This entry point
+ * never calls cudaMalloc, cudaFree or any allocating routine. Its scratch is
+ * one array of SA_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU
+ * that loads the library holds that array until the process exits.
+ *
+ * Arguments, layout, numerics and results are those of bigbird_attn_fwd with
+ * dtype SA_BF16 (the tensor-core path); there is no dtype argument.
+ * Set-up: the first call on a device looks up the array's device address on
+ * that device (cudaGetSymbolAddress), so make that first call before any
+ * stream capture begins. Each call first clears the array's counters with
+ * cudaMemsetAsync on `stream`.
+ * Sharing: all calls on a device share the one array, which keeps the last
+ * call's contents. Calls ordered on one stream are safe; calls that overlap
+ * on the GPU (different streams without ordering, or several host threads)
+ * race on the array and give wrong results.
+ * Errors: as bigbird_attn_fwd, plus SA_ERR_UNSUPPORTED, before any work is
+ * queued, when the call needs more scratch than SA_NOALLOC_SCRATCH_BYTES
+ * (sa_bigbird_workspace_bytes gives the need; it grows with B*H*g*b*d*n).
+ */
+#define SA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+sa_status bigbird_attn_fwd_noalloc(const void *Q, const void *K, const void *V, void *O,
+                                   int B, int H, int n, int d, int b, int g, int w, int r,
+                                   const int32_t *rand_idx, const uint8_t *key_mask,
+                                   sa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,89 @@
+"""bigbird_attn_fwd_noalloc: the BigBird forward for callers that must not
+allocate device memory.
+
+A serving process that reserves its device memory at start-up, or a plugin
+whose host framework owns the GPU's memory, cannot let the library call
+cudaMalloc on its request path. The no-allocation entry point runs the same
+tensor-core kernel with its scratch in a fixed array compiled into the
+library. These tests call it through the C ABI and compare it with
+bigbird_attn_fwd on the same inputs, twice in a row (the array keeps the
+previous call's contents, so the second call checks that the counters are
+cleared and reused correctly).
+
+This file is named to be collected last, so a run that stops at the first
+failure has already run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_long_bigbird_gb300 as sa
+from block_sparse_long_bigbird_gb300 import _lib
+from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv
+
+TOL_MAX, TOL_MEAN = 2e-2, 2e-3
+
+
+def _noalloc(Q, K, V, O, b, g, w, r, table, key_mask):
+    B, H, n, d = Q.shape
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ptr = lambda t: ctypes.c_void_p(0 if t is None else t.data_ptr())  # noqa: E731
+    return _lib.lib().bigbird_attn_fwd_noalloc(ptr(Q), ptr(K), ptr(V), ptr(O), B, H, n, d, b, g, w, r,
+                                               ptr(table), ptr(key_mask), stream)
+
+
+CASES = [
+    # B, H, n,     d,   b,   padded
+    (2, 4, 4096, 64, 64, False),    # one unit per tile, scheduler counters only
+    (1, 2, 16384, 64, 64, True),    # global tiles split in two: partials + merge counters
+    (1, 2, 16384, 128, 128, False),  # d = 128, split global tiles
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}H{}n{}d{}b{}{}".format(*c[:5], "pad" if c[5] else ""))
+def test_noalloc_matches_bigbird_attn_fwd(case):
+    B, H, n, d, b, padded = case
+    g, w, r = 2, 3, 3
+    dev = torch.device("cuda:0")
+    Qc, Kc, Vc = make_qkv(B, H, n, d, "bf16", cfg_id=80)
+    Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
+    table = sa.build_bigbird_pattern(0, H, n, b, g, w, r).to(dev)
+    km = make_key_mask(B, n, seed=11).to(dev) if padded else None
+    need = sa.bigbird_workspace_bytes(B, H, n, d, b, g)
+    assert 0 < need <= _lib.NOALLOC_SCRATCH_BYTES
+
+    ref = sa.bigbird_attn_fwd(Q, K, V, b, g, w, r, table, km)
+    torch.cuda.synchronize()
+    assert sa.get_last_device_status() == 0
+    ref = ref.float()
+    for call in range(2):
+        O = torch.full_like(Q, float("nan"))
+        st = _noalloc(Q, K, V, O, b, g, w, r, table, km)
+        assert st == _lib.SA_OK, _lib.STATUS_NAMES.get(st, st)
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+        err = (O.float() - ref).abs()
+        assert torch.isfinite(O.float()).all(), f"call {call}: non-finite output"
+        assert err.max().item() <= TOL_MAX and err.mean().item() <= TOL_MEAN, \
+            f"call {call}: max {err.max().item():.3e} mean {err.mean().item():.3e}"
+        if km is not None:
+            pad = (km == 0)[:, None, :, None].expand_as(O)
+            assert (O[pad] == 0).all(), "padded query rows must be exactly 0"
+
+
+def test_noalloc_rejects_oversize_before_touching_the_device():
+    # 8 x 16 heads of n = 65536, d = 128 need ~137 MB of split partials, far
+    # beyond the fixed array. The check runs on the host before any CUDA call,
+    # so the (never dereferenced) pointers below are safe even without a GPU.
+    fake = 0x7f0000000000
+    lib = _lib.lib()
+    need = lib.sa_bigbird_workspace_bytes(8, 16, 65536, 128, 128, 2)
+    assert need > _lib.NOALLOC_SCRATCH_BYTES
+    st = lib.bigbird_attn_fwd_noalloc(fake, fake + 0x1000000, fake + 0x2000000, fake + 0x3000000,
+                                      8, 16, 65536, 128, 128, 2, 3, 3, fake + 0x4000000, None, None)
+    assert st == _lib.SA_ERR_UNSUPPORTED
+    assert np.isfinite(need)
