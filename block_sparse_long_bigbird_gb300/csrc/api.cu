@@ -30,7 +30,7 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<int> g_force_simt{0};
-std::atomic<long long> g_wait_limit{1ll << 22};
+std::atomic<long long> g_wait_limit{2000000};  // microseconds
 std::atomic<int> g_max_splits{16};
 std::atomic<int> g_grid_ctas{0};
 thread_local int g_last_launches = 0;
@@ -181,6 +181,7 @@ sa_status bigbird_attn_fwd(const void *Q, const void *K, const void *V, void *O,
     if (s != SA_OK) return s;
     s = bigbird_args_ok(B, H, n, d, b, g, w, r, rand_idx);
     if (s != SA_OK) return s;
+    if (!aligned16(key_mask)) return SA_ERR_INVALID_ARG;
     sa::Problem p = {};
     p.kind = sa::kBigBird;
     p.Q = Q; p.K = K; p.V = V; p.O = O;
@@ -285,7 +286,7 @@ const char *sa_status_string(sa_status status) {
 sa_status sa_set_option(int option, int64_t value) {
     switch (option) {
         case SA_OPT_FORCE_SIMT: g_force_simt = value != 0; return SA_OK;
-        case SA_OPT_WAIT_LIMIT: g_wait_limit = value > 0 ? (long long)value : (1ll << 22); return SA_OK;
+        case SA_OPT_WAIT_LIMIT: g_wait_limit = value > 0 ? (long long)value : 2000000; return SA_OK;
         case SA_OPT_MAX_SPLITS: g_max_splits = value < 1 ? 1 : (value > 64 ? 64 : (int)value); return SA_OK;
         case SA_OPT_GRID_CTAS: g_grid_ctas = value < 0 ? 0 : (int)value; return SA_OK;
     }
@@ -328,6 +329,7 @@ extern "C" sa_status bigbird_attn_fwd_noalloc(const void *Q, const void *K, cons
     if (s != SA_OK) return s;
     s = bigbird_args_ok(B, H, n, d, b, g, w, r, rand_idx);
     if (s != SA_OK) return s;
+    if (!aligned16(key_mask)) return SA_ERR_INVALID_ARG;
     sa::Problem p = {};
     p.kind = sa::kBigBird;
     p.Q = Q; p.K = K; p.V = V; p.O = O;

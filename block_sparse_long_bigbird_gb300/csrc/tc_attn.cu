@@ -16,12 +16,16 @@
 //     into `splits` chunks of steps (split-KV); each chunk writes an fp32
 //     partial (m, l, O) and the last chunk to finish a row merges the
 //     partials of that row in chunk order (deterministic, no float atomics).
-// Roles (256 threads): warp 0 schedules units, builds the step lists and
-// issues TMA loads; warp 1 allocates TMEM and issues tcgen05 MMAs (lane 0);
-// warps 4-7 run the softmax (thread t owns query row t = TMEM lane t), the
-// O rescale and the epilogue. Every wait is bounded: on expiry the CTA
-// records SA_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM
-// and exits.
+// Roles (256 threads): warp 0 schedules units, builds the key-block lists and
+// issues TMA loads (K and V in separate rings: a K stage is free once its
+// QK^T completed, a V stage once its PV completed); warp 1 allocates TMEM and
+// issues tcgen05 MMAs (lane 0); warps 4-7 run the softmax (thread t owns query
+// row t = TMEM lane t), the lazy O rescale and the epilogue. S sits in two
+// TMEM buffers; the softmax writes P (bf16) over the first half of its S
+// buffer and the PV product reads A straight from TMEM. O is double buffered
+// in TMEM so a unit's epilogue runs while the next unit computes. Every wait
+// is bounded in time: on expiry the CTA records SA_ERR_TIMEOUT, drains its
+// in-flight copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,17 +45,19 @@ constexpr int kBM = 128;           // query rows per tile = TMEM lanes
 constexpr int kBN = 128;           // keys per step = S tile columns
 constexpr int kThreads = 256;
 constexpr int kNU = 4;             // unit-info ring depth
+constexpr int kSI = 8;             // step-info ring depth
 constexpr int kSoftmaxThread0 = 128;
 constexpr int kTargetChunkSteps = 64;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (factor 256)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzled region
+constexpr uint32_t kSuspendNs = 100000;  // try_wait suspend hint
 
 enum UnitKind { kUnitEnd = 0, kUnitDirect = 1, kUnitSplit = 2 };
 
 struct UnitInfo {
     int kind, bh, q0, n_steps;
-    int tile_slot, chunk, nchunks, step0;  // split bookkeeping; first sweep step
+    int tile_slot, chunk, nchunks, step0;  // split bookkeeping; first sweep step (-1: block list)
     int j0, j1, pad0, pad1;                // BigBird query blocks of the two halves (-1: none)
     int pad[4];
 };
@@ -67,26 +73,32 @@ static_assert(sizeof(StepInfo) == 32, "StepInfo layout");
 
 template <int D>
 struct Cfg {
-    static constexpr int STAGES = (D == 64) ? 3 : 2;
+    static constexpr int KST = (D == 64) ? 4 : 3;  // K stages
+    static constexpr int VST = (D == 64) ? 5 : 3;  // V stages (released later than K)
     static constexpr int NQ = (D == 64) ? 2 : 1;
     static constexpr int TILE_BYTES = 128 * D * 2;  // Q tile / K step / V step
-    static constexpr int P_BYTES = 128 * 128 * 2;
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + NQ * TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
-    static constexpr int P_OFF = V_OFF + STAGES * TILE_BYTES;
-    static constexpr int SMALL_OFF = P_OFF + 2 * P_BYTES;
-    // small area: barriers, TMEM address, abort flag, unit ring, step ring
-    static constexpr int BAR_OFF = SMALL_OFF;
-    static constexpr int MISC_OFF = SMALL_OFF + 512;
-    static constexpr int UNIT_OFF = SMALL_OFF + 576;
+    static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
+    static constexpr int SMALL_OFF = V_OFF + VST * TILE_BYTES;
+    static constexpr int BAR_OFF = SMALL_OFF;          // 64 barriers max
+    static constexpr int MISC_OFF = SMALL_OFF + 512;   // TMEM address, abort flag
+    static constexpr int UNIT_OFF = MISC_OFF + 64;
     static constexpr int STEP_OFF = UNIT_OFF + kNU * 64;
-    static constexpr int SMEM_BYTES = STEP_OFF + STAGES * 32;
+    static constexpr int LIST_OFF = STEP_OFF + kSI * 32;  // producer's block list (32 entries)
+    static constexpr int SMEM_BYTES = LIST_OFF + 32 * 4;
     static constexpr int ALLOC_BYTES = SMEM_BYTES + 1024;  // slack for 1024-B alignment
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t O_COL = 256;
+    static constexpr uint32_t O_COL = 256;  // O buffer ob at O_COL + ob * D
+    // barrier slots
+    static constexpr int B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 8, B_VF = 12, B_VE = 17, B_IF = 22,
+                         B_IE = B_IF + kSI, B_SF = B_IE + kSI, B_PF = B_SF + 2, B_PV = B_PF + 2, B_UF = B_PV + 2,
+                         B_UE = B_UF + kNU, B_DRAIN = B_UE + kNU, B_COUNT = B_DRAIN + 1;
+    static_assert(KST <= 4 && VST <= 5 && NQ <= 2, "ring depths");
+    static_assert(B_COUNT * 8 <= 512, "barrier area");
 };
 static_assert(Cfg<128>::ALLOC_BYTES <= 232448, "d=128 shared memory budget");
+static_assert(Cfg<64>::ALLOC_BYTES <= 232448, "d=64 shared memory budget");
 
 // Host-computed geometry of one call.
 struct Geometry {
@@ -99,7 +111,7 @@ struct Geometry {
     int n_split_units;    // B*H*gtiles*splits
     int total_units;
     float scale_log2;
-    long long wait_limit;
+    unsigned long long wait_ns;
 };
 
 struct Workspace {
@@ -118,57 +130,67 @@ struct Params {
     unsigned *status;
 };
 
-// Barrier slots (8 B each) in the small area.
-enum Bar {
-    B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_VFULL = 7, B_SEMPTY = 10, B_SFULL = 13, B_PFULL = 15,
-    B_PVDONE = 17, B_UFULL = 19, B_UEMPTY = 23, B_DRAIN = 27, B_COUNT = 28
-};
-
 struct Ctl {
     volatile int *abort;
     unsigned *status;
-    long long limit;
+    unsigned long long limit_ns;
 };
 
-// Single-thread bounded wait. Returns false (and leaves) once the CTA aborts.
-__device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, const Ctl &c) {
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Per-thread wait, bounded in time: returns false (and leaves) once the CTA
+// aborts. The first probe has no suspend hint (cheapest when the phase is
+// already complete); later probes sleep in the hardware until the phase
+// completes or the hint expires. No warp-collective operation inside, so
+// lanes of one warp may call it independently.
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Ctl &c) {
     if (mbar_try_wait(bar, parity)) return true;
-    for (long long it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (it >= c.limit) {
+    unsigned long long t0 = 0;
+    while (!try_wait_hint(bar, parity)) {
+        if (*c.abort) return false;
+        const unsigned long long now = global_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > c.limit_ns) {
             *c.abort = 1;
             atomicOr(c.status, kDevTimeout);
             return false;
         }
-        if ((it & 63) == 0 && *c.abort) return false;
     }
+    return true;
 }
-// Warp-uniform bounded wait: lane 0 waits, every lane gets the same answer.
+// Warp-uniform wait: every lane probes the barrier itself (a divergent
+// single-lane wait costs hundreds of cycles to reconverge), then one vote
+// gives all lanes the same answer.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl &c) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_one(bar, parity, c) ? 1 : 0;
-    return __shfl_sync(kFull, ok, 0) != 0;
+    const bool ok = wait_one(bar, parity, c);
+    return __all_sync(kFull, ok);
 }
 // Drain wait used on the abort path (ignores the abort flag, still bounded).
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, long long limit) {
-    for (long long it = 0; it < limit; ++it)
-        if (mbar_try_wait(bar, parity)) return;
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return;
 }
 
 // ---------------------------------------------------------------- producer helpers
-// Per-lane cache of a local tile's random blocks: entries e = lane, lane + 32
-// of the concatenation rand[h][j0][:] ++ rand[h][j1][:]; invalid -> INT_MAX.
-struct RandCache {
-    int v0, v1;
-    int e0, e1;
-};
-
-__device__ __forceinline__ int load_rand(const Params &p, const int32_t *r0, const int32_t *r1, int e, int nb) {
-    const int r = p.geo.r;
-    int v = INT_MAX;
-    if (e < r) v = r0 ? __ldg(r0 + e) : -1;
-    else if (e < 2 * r) v = r1 ? __ldg(r1 + (e - r)) : -1;
-    else return INT_MAX;
+__device__ __forceinline__ int load_rand(const Params &p, const int32_t *row, int e, int nb) {
+    int v = row ? __ldg(row + e) : -1;
     if (v == -1) return INT_MAX;
     if (v < -1 || v >= nb) {
         atomicOr(p.status, kDevBadIndex);
@@ -177,53 +199,36 @@ __device__ __forceinline__ int load_rand(const Params &p, const int32_t *r0, con
     return v;
 }
 
-// Smallest random block > x over both query blocks (warp-uniform result).
-__device__ __forceinline__ int rand_next(const Params &p, const RandCache &rc, const int32_t *r0,
-                                         const int32_t *r1, int x, int nb) {
-    int cand = INT_MAX;
-    if (rc.v0 > x) cand = rc.v0;
-    if (rc.v1 > x && rc.v1 < cand) cand = rc.v1;
-    for (int e = 64 + (threadIdx.x & 31); e < 2 * p.geo.r; e += 32) {
-        const int v = load_rand(p, r0, r1, e, nb);
-        if (v > x && v < cand) cand = v;
-    }
-    return __reduce_min_sync(kFull, cand);
-}
-
-// Is key block kb among the random blocks of query block `which` (0: j0, 1: j1)?
-__device__ __forceinline__ bool rand_has(const Params &p, const RandCache &rc, const int32_t *r0,
-                                         const int32_t *r1, int kb, int which, int nb) {
-    const int r = p.geo.r;
-    const int lo = which * r, hi = lo + r;
-    bool hit = (rc.e0 >= lo && rc.e0 < hi && rc.v0 == kb) || (rc.e1 >= lo && rc.e1 < hi && rc.v1 == kb);
-    for (int e = 64 + (threadIdx.x & 31); e < 2 * r; e += 32)
-        if (e >= lo && e < hi && load_rand(p, r0, r1, e, nb) == kb) hit = true;
+// Is key block kb among the random blocks of `row` (warp-uniform answer)?
+__device__ __forceinline__ bool rand_has(const Params &p, const int32_t *row, int kb) {
+    bool hit = false;
+    if (row)
+        for (int e = threadIdx.x & 31; e < p.geo.r; e += 32) hit |= load_rand(p, row, e, p.geo.nb) == kb;
     return __any_sync(kFull, hit);
 }
 
-// Does query block j (>= 0) see key block kb? `which` selects its random list.
-__device__ __forceinline__ bool block_allowed(const Params &p, const RandCache &rc, const int32_t *r0,
-                                              const int32_t *r1, int j, int which, int kb) {
+// Does query block j (>= 0) see key block kb? `row`: j's random list.
+__device__ __forceinline__ bool block_allowed(const Params &p, const int32_t *row, int j, int kb) {
     const Geometry &G = p.geo;
     if (j < 0) return false;
     if (j < G.g || kb < G.g) return true;
     if (abs(kb - j) <= G.half) return true;
-    return rand_has(p, rc, r0, r1, kb, which, G.nb);
+    return rand_has(p, row, kb);
 }
 
-// Smallest block > x in the union of the tile's key-block lists.
-__device__ __forceinline__ int union_next(const Params &p, const RandCache &rc, const int32_t *r0,
-                                          const int32_t *r1, int lo, int hi, int x) {
-    const Geometry &G = p.geo;
-    int best = G.nb;
-    if (x + 1 < G.g) best = x + 1;
-    const int c = max(x + 1, lo);
-    if (c <= hi && c < best) best = c;
-    const int rn = rand_next(p, rc, r0, r1, x, G.nb);
-    return rn < best ? rn : best;
+// Any valid key in block kb (per-lane check, 16-byte loads; key_mask is
+// 16-byte aligned and every block starts on a multiple of 64 bytes).
+__device__ __forceinline__ bool block_has_valid_lane(const uint8_t *km, int kb, int b) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(km + (size_t)kb * b);
+    uint32_t any = 0;
+    for (int i = 0; i < b / 16; ++i) {
+        const uint4 v = __ldg(src + i);
+        any |= v.x | v.y | v.z | v.w;
+    }
+    return any != 0;
 }
 
-// 64-bit validity of keys [k0, k0 + 64) of sequence `beta` (warp-uniform).
+// 64-bit validity of keys [k0, k0 + 64) (warp-uniform).
 __device__ __forceinline__ uint64_t key_bits64(const uint8_t *km, int k0, int n) {
     const int lane = threadIdx.x & 31;
     const int a = k0 + lane, b = k0 + 32 + lane;
@@ -232,12 +237,72 @@ __device__ __forceinline__ uint64_t key_bits64(const uint8_t *km, int k0, int n)
     return ((uint64_t)hi << 32) | lo;
 }
 
-// Any valid key in block kb?
-__device__ __forceinline__ bool block_has_valid(const Params &p, const uint8_t *km, int kb) {
-    const int b = p.geo.b;
-    bool any = false;
-    for (int t = threadIdx.x & 31; t < b; t += 32) any |= km[kb * b + t] != 0;
-    return __any_sync(kFull, any);
+// Sorted, de-duplicated key-block list of a local tile, built by the whole
+// producer warp: each lane holds one candidate (global block, window block or
+// random block), duplicates and padded blocks drop out, and each survivor's
+// rank among the survivors is its position. list[pos] = block | allow bits
+// (bit 30: query block j0 sees it, bit 31: j1 sees it). Returns the number of
+// blocks, or -1 when the candidates do not fit in one warp.
+__device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1, const int32_t *r0,
+                                                const int32_t *r1, const uint8_t *km, uint32_t *list) {
+    const Geometry &G = p.geo;
+    const int lane = threadIdx.x & 31;
+    const int nglob = min(G.g, G.nb);
+    const int jl = j1 >= 0 ? j1 : j0;
+    const int wlo = max(max(0, j0 - G.half), nglob);
+    const int whi = min(G.nb - 1, jl + G.half);
+    const int wcount = max(0, whi - wlo + 1);
+    const int nr0 = r0 ? G.r : 0, nr1 = r1 ? G.r : 0;
+    const int total = nglob + wcount + nr0 + nr1;
+    if (total > 32) return -1;
+    int v = INT_MAX, src = 0;
+    if (lane < nglob) {
+        v = lane;
+        src = 1;
+    } else if (lane < nglob + wcount) {
+        v = wlo + (lane - nglob);
+        src = 2;
+    } else if (lane < nglob + wcount + nr0) {
+        v = load_rand(p, r0, lane - nglob - wcount, G.nb);
+        src = 3;
+    } else if (lane < total) {
+        v = load_rand(p, r1, lane - nglob - wcount - nr0, G.nb);
+        src = 4;
+    }
+    const unsigned same = __match_any_sync(kFull, v);
+    const bool in_r0 = (__ballot_sync(kFull, src == 3) & same) != 0;
+    const bool in_r1 = (__ballot_sync(kFull, src == 4) & same) != 0;
+    bool valid = v < G.nb && (same & ((1u << lane) - 1u)) == 0;  // first lane holding this block
+    if (valid && km) valid = block_has_valid_lane(km, v, G.b);
+    const bool a0 = valid && (j0 < G.g || v < G.g || abs(v - j0) <= G.half || in_r0);
+    const bool a1 = valid && j1 >= 0 && (j1 < G.g || v < G.g || abs(v - j1) <= G.half || in_r1);
+    const unsigned vm = __ballot_sync(kFull, valid);
+    int pos = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+        const int vj = __shfl_sync(kFull, v, j);
+        pos += ((vm >> j) & 1u) && vj < v;
+    }
+    if (valid) list[pos] = (uint32_t)v | (a0 ? (1u << 30) : 0u) | (a1 ? (1u << 31) : 0u);
+    __syncwarp();
+    return __popc(vm);
+}
+
+// Fallback for very wide patterns: smallest union block > x (warp-uniform).
+__device__ __forceinline__ int union_next_slow(const Params &p, const int32_t *r0, const int32_t *r1, int lo, int hi,
+                                               int x) {
+    const Geometry &G = p.geo;
+    int best = G.nb;
+    if (x + 1 < G.g) best = x + 1;
+    const int c = max(x + 1, lo);
+    if (c <= hi && c < best) best = c;
+    int cand = INT_MAX;
+    for (int e = threadIdx.x & 31; e < 2 * G.r; e += 32) {
+        const int v = e < G.r ? load_rand(p, r0, e, G.nb) : load_rand(p, r1, e - G.r, G.nb);
+        if (v > x && v < cand) cand = v;
+    }
+    cand = __reduce_min_sync(kFull, cand);
+    return cand < best ? cand : best;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -255,35 +320,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
     UnitInfo *ring = reinterpret_cast<UnitInfo *>(smem + C::UNIT_OFF);
     StepInfo *steps = reinterpret_cast<StepInfo *>(smem + C::STEP_OFF);
+    uint32_t *list = reinterpret_cast<uint32_t *>(smem + C::LIST_OFF);
 
     const Geometry &G = p.geo;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const Ctl ctl{abort_flag, p.status, G.wait_limit};
+    const Ctl ctl{abort_flag, p.status, G.wait_ns};
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < C::NQ; ++i) {
-            mbar_init(bar(B_QFULL + i), 1);
-            mbar_init(bar(B_QEMPTY + i), 1);
+            mbar_init(bar(C::B_QF + i), 1);
+            mbar_init(bar(C::B_QE + i), 1);
         }
-        for (int i = 0; i < C::STAGES; ++i) {
-            mbar_init(bar(B_KFULL + i), 1);
-            mbar_init(bar(B_VFULL + i), 1);
-            mbar_init(bar(B_SEMPTY + i), 1);
+        for (int i = 0; i < C::KST; ++i) {
+            mbar_init(bar(C::B_KF + i), 1);
+            mbar_init(bar(C::B_KE + i), 1);
+        }
+        for (int i = 0; i < C::VST; ++i) {
+            mbar_init(bar(C::B_VF + i), 1);
+            mbar_init(bar(C::B_VE + i), 1);
+        }
+        for (int i = 0; i < kSI; ++i) {
+            mbar_init(bar(C::B_IF + i), 1);
+            mbar_init(bar(C::B_IE + i), 4);  // one arrival per softmax warp
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_SFULL + i), 1);
-            mbar_init(bar(B_PFULL + i), 128);
-            mbar_init(bar(B_PVDONE + i), 1);
+            mbar_init(bar(C::B_SF + i), 1);
+            mbar_init(bar(C::B_PF + i), 128);
+            mbar_init(bar(C::B_PV + i), 1);
         }
         for (int i = 0; i < kNU; ++i) {
-            mbar_init(bar(B_UFULL + i), 1);
-            mbar_init(bar(B_UEMPTY + i), 1 + 128);
+            mbar_init(bar(C::B_UF + i), 1);
+            mbar_init(bar(C::B_UE + i), 1 + 128);
         }
-        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(C::B_DRAIN), 1);
         fence_mbar_init();
-        if ((sbase & 1023u) != 0) atomicOr(p.status, kDevTimeout);  // cannot happen: aligned above
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -302,21 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================================================================ producer
         uint32_t g = 0, qcnt = 0;
-        uint32_t kv_arms[C::STAGES] = {};
-        uint32_t q_arms[C::NQ] = {};
+        uint32_t k_arms[C::KST] = {}, v_arms[C::VST] = {}, q_arms[C::NQ] = {};
         bool ok = true;
+        unsigned u_next = 0;
+        if (lane == 0) u_next = atomicAdd(p.ws.counters, 1u);
         for (uint32_t ui_idx = 0; ok; ++ui_idx) {
-            int u = 0;
-            if (lane == 0) u = (int)atomicAdd(p.ws.counters, 1u);
-            u = __shfl_sync(kFull, u, 0);
+            int u = (int)__shfl_sync(kFull, u_next, 0);
+            if (lane == 0 && u < G.total_units) u_next = atomicAdd(p.ws.counters, 1u);  // prefetch the next
             const uint32_t slot = ui_idx % kNU;
-            if (ui_idx >= kNU && !(ok = wait_warp(bar(B_UEMPTY + slot), ((ui_idx / kNU) - 1) & 1, ctl))) break;
+            if (ui_idx >= kNU && !(ok = wait_warp(bar(C::B_UE + slot), ((ui_idx / kNU) - 1) & 1, ctl))) break;
             UnitInfo ui = {};
             if (u >= G.total_units) {
                 ui.kind = kUnitEnd;
                 if (lane == 0) {
                     ring[slot] = ui;
-                    mbar_arrive(bar(B_UFULL + slot));
+                    mbar_arrive(bar(C::B_UF + slot));
                 }
                 break;
             }
@@ -339,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ui.bh = v / per;
                 tile = G.gtiles + (v - ui.bh * per);
                 ui.kind = kUnitDirect;
-                ui.step0 = -1;  // local: sorted union of block lists
+                ui.step0 = -1;
             }
             ui.q0 = tile * kBM;
             if (G.b == 64) {
@@ -354,16 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *r0 = (p.rand_idx && G.r > 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j0) * G.r : nullptr;
             const int32_t *r1 =
                 (p.rand_idx && G.r > 0 && ui.j1 >= 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j1) * G.r : nullptr;
-            RandCache rc;
-            rc.e0 = lane;
-            rc.e1 = lane + 32;
-            rc.v0 = load_rand(p, r0, r1, rc.e0, G.nb);
-            rc.v1 = load_rand(p, r0, r1, rc.e1, G.nb);
-            // union window range of the (one or two) query blocks
+            const int bps = (G.b == 64) ? 2 : 1;  // key blocks per step
             const int jl = ui.j1 >= 0 ? ui.j1 : ui.j0;
             const int wlo = max(0, ui.j0 - G.half), whi = min(G.nb - 1, jl + G.half);
-            const int bps = (G.b == 64) ? 2 : 1;  // key blocks per step
-
+            int nlist = 0;
+            bool slow = false;
             if (ui.step0 < 0) {
                 bool any_row = true;
                 if (km) {
@@ -371,110 +438,147 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && km[ui.q0 + t] != 0;
                     any_row = __any_sync(kFull, a);
                 }
-                int cnt = 0;
                 if (any_row) {
-                    for (int x = union_next(p, rc, r0, r1, wlo, whi, -1); x < G.nb;
-                         x = union_next(p, rc, r0, r1, wlo, whi, x))
-                        if (!km || block_has_valid(p, km, x)) ++cnt;
+                    nlist = build_local_list(p, ui.j0, ui.j1, r0, r1, km, list);
+                    if (nlist < 0) {  // wide pattern: generate the union block by block
+                        slow = true;
+                        nlist = 0;
+                        for (int x = union_next_slow(p, r0, r1, wlo, whi, -1); x < G.nb;
+                             x = union_next_slow(p, r0, r1, wlo, whi, x)) {
+                            bool has = true;
+                            if (km) has = __any_sync(kFull, lane < G.b / 16 &&
+                                                                 [&] {
+                                                                     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+                                                                         km + (size_t)x * G.b) + lane);
+                                                                     return (v.x | v.y | v.z | v.w) != 0;
+                                                                 }());
+                            nlist += has ? 1 : 0;
+                        }
+                    }
                 }
-                ui.n_steps = (cnt + bps - 1) / bps;
+                ui.n_steps = (nlist + bps - 1) / bps;
             }
             if (lane == 0) {
                 ring[slot] = ui;
-                mbar_arrive(bar(B_UFULL + slot));
+                mbar_arrive(bar(C::B_UF + slot));
             }
             if (ui.n_steps == 0) continue;
 
             // ---- Q tile
             const uint32_t qb = qcnt % C::NQ;
-            if (qcnt >= C::NQ && !(ok = wait_warp(bar(B_QEMPTY + qb), ((qcnt / C::NQ) - 1) & 1, ctl))) break;
+            if (qcnt >= C::NQ && !(ok = wait_warp(bar(C::B_QE + qb), ((qcnt / C::NQ) - 1) & 1, ctl))) break;
             if (lane == 0) {
                 const uint32_t dst = sbase + C::Q_OFF + qb * C::TILE_BYTES;
-                mbar_arrive_expect_tx(bar(B_QFULL + qb), C::TILE_BYTES);
+                mbar_arrive_expect_tx(bar(C::B_QF + qb), C::TILE_BYTES);
                 for (int dc = 0; dc < D / 64; ++dc)
                     for (int rh = 0; rh < 2; ++rh)
-                        tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(B_QFULL + qb), dc * 64,
+                        tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF + qb), dc * 64,
                                     ui.q0 + rh * 64, ui.bh);
             }
             ++q_arms[qb];
             ++qcnt;
 
             // ---- key steps
-            int x = -1;  // last block emitted (local units)
+            int x = -1;  // slow path: last block emitted
             for (int t = 0; t < ui.n_steps; ++t, ++g) {
-                const uint32_t st = g % C::STAGES;
-                if (g >= C::STAGES && !(ok = wait_warp(bar(B_SEMPTY + st), ((g / C::STAGES) - 1) & 1, ctl)))
-                    break;
                 StepInfo si;
-                si.masked = 0;
+                si.masked = km ? 1u : 0u;
                 si.allow = 0;
                 si.kmask[0] = si.kmask[1] = ~0ull;
+#pragma unroll
                 for (int s = 0; s < 2; ++s) {
-                    int kb, y;
-                    if (ui.step0 >= 0) {  // full sweep
+                    int kb = -1, y = G.n;
+                    bool a0 = false, a1 = false;
+                    if (ui.step0 >= 0) {  // full sweep of a global tile
                         if (G.b == 64) {
                             kb = 2 * (ui.step0 + t) + s;
-                            y = kb < G.nb ? kb * 64 : G.n;
+                            if (kb >= G.nb) kb = -1;
+                            y = kb >= 0 ? kb * 64 : G.n;
                         } else {
                             kb = ui.step0 + t;
                             y = kb * 128 + s * 64;
                         }
-                        if (kb >= G.nb) kb = -1;
-                    } else if (G.b == 64) {
-                        do {
-                            x = union_next(p, rc, r0, r1, wlo, whi, x);
-                        } while (x < G.nb && km && !block_has_valid(p, km, x));
-                        kb = x < G.nb ? x : -1;
-                        y = kb >= 0 ? kb * 64 : G.n;
-                    } else {
-                        if (s == 0) {
-                            do {
-                                x = union_next(p, rc, r0, r1, wlo, whi, x);
-                            } while (x < G.nb && km && !block_has_valid(p, km, x));
+                        if (kb >= 0) {
+                            a0 = block_allowed(p, r0, ui.j0, kb);
+                            a1 = (G.b == 64) ? block_allowed(p, r1, ui.j1, kb) : a0;
                         }
-                        kb = x < G.nb ? x : -1;
-                        y = kb >= 0 ? kb * 128 + s * 64 : G.n;
+                    } else if (!slow) {
+                        const int li = (G.b == 64) ? 2 * t + s : t;
+                        if (li < nlist) {
+                            const uint32_t e = list[li];
+                            kb = (int)(e & 0x3FFFFFFFu);
+                            a0 = (e >> 30) & 1u;
+                            a1 = (G.b == 64) ? ((e >> 31) & 1u) : a0;
+                            y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                        }
+                    } else {
+                        if (G.b == 64 || s == 0) {
+                            do {
+                                x = union_next_slow(p, r0, r1, wlo, whi, x);
+                            } while (x < G.nb && km &&
+                                     !__any_sync(kFull, lane < G.b / 16 && [&] {
+                                         const uint4 v =
+                                             __ldg(reinterpret_cast<const uint4 *>(km + (size_t)x * G.b) + lane);
+                                         return (v.x | v.y | v.z | v.w) != 0;
+                                     }()));
+                        }
+                        if (x < G.nb) {
+                            kb = x;
+                            a0 = block_allowed(p, r0, ui.j0, kb);
+                            a1 = (G.b == 64) ? block_allowed(p, r1, ui.j1, kb) : a0;
+                            y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                        }
                     }
                     si.y[s] = y;
                     if (kb < 0) continue;
-                    uint64_t bits = ~0ull;
                     if (km) {
-                        bits = key_bits64(km, y, G.n);
-                        si.masked = 1;
+                        const uint64_t bits = key_bits64(km, y, G.n);
                         si.kmask[s] = bits;
+                        if (bits == 0) continue;
                     }
-                    if (bits == 0) continue;
-                    const bool a0 = block_allowed(p, rc, r0, r1, ui.j0, 0, kb);
-                    const bool a1 = (G.b == 64) ? block_allowed(p, rc, r0, r1, ui.j1, 1, kb) : a0;
                     si.allow |= (a0 ? 1u : 0u) << (2 * s);
                     si.allow |= (a1 ? 1u : 0u) << (2 * s + 1);
                 }
+                // step info -> softmax
+                const uint32_t ii = g % kSI;
+                if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
                 if (lane == 0) {
-                    steps[st] = si;
-                    const uint32_t kdst = sbase + C::K_OFF + st * C::TILE_BYTES;
-                    const uint32_t vdst = sbase + C::V_OFF + st * C::TILE_BYTES;
-                    mbar_arrive_expect_tx(bar(B_KFULL + st), C::TILE_BYTES);
+                    steps[ii] = si;
+                    mbar_arrive(bar(C::B_IF + ii));
+                }
+                // K
+                const uint32_t sk = g % C::KST;
+                if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
+                if (lane == 0) {
+                    const uint32_t kdst = sbase + C::K_OFF + sk * C::TILE_BYTES;
+                    mbar_arrive_expect_tx(bar(C::B_KF + sk), C::TILE_BYTES);
                     for (int s = 0; s < 2; ++s)
                         for (int dc = 0; dc < D / 64; ++dc)
-                            tma_load_3d(kdst + dc * kRegionBytes + s * 8192, &tmK, bar(B_KFULL + st), dc * 64,
-                                        si.y[s], ui.bh);
-                    mbar_arrive_expect_tx(bar(B_VFULL + st), C::TILE_BYTES);
-                    for (int s = 0; s < 2; ++s)
-                        for (int dc = 0; dc < D / 64; ++dc)
-                            tma_load_3d(vdst + dc * kRegionBytes + s * 8192, &tmV, bar(B_VFULL + st), dc * 64,
+                            tma_load_3d(kdst + dc * kRegionBytes + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
                                         si.y[s], ui.bh);
                 }
-                ++kv_arms[st];
+                ++k_arms[sk];
+                // V
+                const uint32_t sv = g % C::VST;
+                if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
+                if (lane == 0) {
+                    const uint32_t vdst = sbase + C::V_OFF + sv * C::TILE_BYTES;
+                    mbar_arrive_expect_tx(bar(C::B_VF + sv), C::TILE_BYTES);
+                    for (int s = 0; s < 2; ++s)
+                        for (int dc = 0; dc < D / 64; ++dc)
+                            tma_load_3d(vdst + dc * kRegionBytes + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
+                                        si.y[s], ui.bh);
+                }
+                ++v_arms[sv];
             }
         }
         if (!ok && lane == 0) {  // abort: wait for the copies this CTA still has in flight
-            for (int i = 0; i < C::STAGES; ++i)
-                if (kv_arms[i]) {
-                    wait_drain(bar(B_KFULL + i), (kv_arms[i] - 1) & 1, G.wait_limit);
-                    wait_drain(bar(B_VFULL + i), (kv_arms[i] - 1) & 1, G.wait_limit);
-                }
+            for (int i = 0; i < C::KST; ++i)
+                if (k_arms[i]) wait_drain(bar(C::B_KF + i), (k_arms[i] - 1) & 1, G.wait_ns);
+            for (int i = 0; i < C::VST; ++i)
+                if (v_arms[i]) wait_drain(bar(C::B_VF + i), (v_arms[i] - 1) & 1, G.wait_ns);
             for (int i = 0; i < C::NQ; ++i)
-                if (q_arms[i]) wait_drain(bar(B_QFULL + i), (q_arms[i] - 1) & 1, G.wait_limit);
+                if (q_arms[i]) wait_drain(bar(C::B_QF + i), (q_arms[i] - 1) & 1, G.wait_ns);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
@@ -484,59 +588,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t g = 0, qcnt = 0;
             int pend = -1;
             bool pend_first = false;
+            uint32_t pend_ob = 0;
             bool ok = true;
-            auto issue_pv = [&](uint32_t h, bool first) -> bool {
-                const uint32_t st = h % C::STAGES, pb = h & 1;
-                if (!wait_one(bar(B_PFULL + pb), (h >> 1) & 1, ctl)) return false;
-                if (!wait_one(bar(B_VFULL + st), (h / C::STAGES) & 1, ctl)) return false;
+            auto issue_pv = [&](uint32_t h, bool first, uint32_t ob) -> bool {
+                const uint32_t sv = h % C::VST, pb = h & 1;
+                if (!wait_one(bar(C::B_PF + pb), (h >> 1) & 1, ctl)) return false;
+                if (!wait_one(bar(C::B_VF + sv), (h / C::VST) & 1, ctl)) return false;
                 tc_fence_after();
-                const uint32_t pa = sbase + C::P_OFF + pb * C::P_BYTES;
-                const uint32_t va = sbase + C::V_OFF + st * C::TILE_BYTES;
+                const uint32_t pt = tmem + pb * kBN;  // P_h (bf16 pairs) over S buffer h & 1
+                const uint32_t va = sbase + C::V_OFF + sv * C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t a = desc_sw128(pa + (kk >> 2) * kRegionBytes + (kk & 3) * 32, 16);
                     const uint64_t b = desc_sw128(va + kk * 2048, kRegionBytes);
-                    mma_bf16_ss(tmem + C::O_COL, a, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                    mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
                 }
-                mma_commit(bar(B_SEMPTY + st));
-                mma_commit(bar(B_PVDONE + pb));
+                mma_commit(bar(C::B_VE + sv));
+                mma_commit(bar(C::B_PV + pb));
                 return true;
             };
             for (uint32_t ui_idx = 0; ok; ++ui_idx) {
                 const uint32_t slot = ui_idx % kNU;
-                if (!(ok = wait_one(bar(B_UFULL + slot), (ui_idx / kNU) & 1, ctl))) break;
+                if (!(ok = wait_one(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
                 const int kind = ring[slot].kind;
                 const int n_steps = ring[slot].n_steps;
-                mbar_arrive(bar(B_UEMPTY + slot));
+                mbar_arrive(bar(C::B_UE + slot));
                 if (kind == kUnitEnd) break;
                 if (n_steps == 0) continue;
                 const uint32_t qb = qcnt % C::NQ;
-                if (!(ok = wait_one(bar(B_QFULL + qb), (qcnt / C::NQ) & 1, ctl))) break;
+                const uint32_t ob = qcnt & 1;
+                if (!(ok = wait_one(bar(C::B_QF + qb), (qcnt / C::NQ) & 1, ctl))) break;
                 tc_fence_after();
                 const uint32_t qa = sbase + C::Q_OFF + qb * C::TILE_BYTES;
                 for (int t = 0; t < n_steps; ++t, ++g) {
-                    const uint32_t st = g % C::STAGES, sb = g & 1;
-                    if (!(ok = wait_one(bar(B_KFULL + st), (g / C::STAGES) & 1, ctl))) break;
+                    const uint32_t sk = g % C::KST, sb = g & 1;
+                    if (!(ok = wait_one(bar(C::B_KF + sk), (g / C::KST) & 1, ctl))) break;
                     tc_fence_after();
-                    const uint32_t ka = sbase + C::K_OFF + st * C::TILE_BYTES;
+                    const uint32_t ka = sbase + C::K_OFF + sk * C::TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kRegionBytes + (kk & 3) * 32;
                         mma_bf16_ss(tmem + sb * kBN, desc_sw128(qa + off, 16), desc_sw128(ka + off, 16), idesc_qk,
                                     kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(B_SFULL + sb));
-                    if (t == n_steps - 1) mma_commit(bar(B_QEMPTY + qb));
-                    if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first))) break;
+                    mma_commit(bar(C::B_KE + sk));
+                    mma_commit(bar(C::B_SF + sb));
+                    if (t == n_steps - 1) mma_commit(bar(C::B_QE + qb));
+                    if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
                     pend = (int)g;
                     pend_first = (t == 0);
+                    pend_ob = ob;
                 }
                 ++qcnt;
             }
-            if (ok && pend >= 0) issue_pv((uint32_t)pend, pend_first);
+            if (ok && pend >= 0) issue_pv((uint32_t)pend, pend_first, pend_ob);
             // drain: every MMA issued by this thread has completed once this arrives
-            mma_commit(bar(B_DRAIN));
-            wait_drain(bar(B_DRAIN), 0, G.wait_limit);
+            mma_commit(bar(C::B_DRAIN));
+            wait_drain(bar(C::B_DRAIN), 0, G.wait_ns);
         }
     } else if (warp >= 4) {
         // ================================================================ softmax / epilogue
@@ -544,24 +651,169 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
         const int hf = (G.b == 64) ? (tid >> 6) : 0;
         const float sl2 = G.scale_log2;
-        uint32_t g = 0;
-        for (uint32_t ui_idx = 0;; ++ui_idx) {
+
+        // State of the unit whose epilogue is deferred until the next unit's
+        // first step has been handed to the MMA warp.
+        struct Pend {
+            int kind, bh, q0, tile_slot, chunk, nchunks, have;
+            bool row_valid;
+            float m, l;
+            uint32_t ob, g_last;
+        };
+        Pend pe;
+        pe.kind = kUnitEnd;
+
+        auto epilogue = [&](const Pend &e) -> bool {
+            const int row = e.q0 + tid;
+            const uint32_t oaddr = tmem + lane_base + C::O_COL + e.ob * D;
+            if (e.have) {
+                if (!wait_warp(bar(C::B_PV + (e.g_last & 1)), (e.g_last >> 1) & 1, ctl)) return false;
+                tc_fence_after();
+            }
+            if (e.kind == kUnitDirect) {
+                const float inv = (e.row_valid && e.l > 0.f) ? 1.f / e.l : 0.f;
+                __nv_bfloat16 *orow = p.O + ((size_t)e.bh * G.n + (row < G.n ? row : 0)) * D;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float o[32];
+                    if (e.have) {
+                        tmem_ld32(oaddr + cc * 32, o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                    }
+                    if (row < G.n) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                __nv_bfloat162 b2 =
+                                    __floats2bfloat162_rn(o[q * 8 + 2 * k] * inv, o[q * 8 + 2 * k + 1] * inv);
+                                w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                            *reinterpret_cast<uint4 *>(orow + cc * 32 + q * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
+                return true;
+            }
+            // split chunk: publish this row's partial; the last arrival merges the row
+            const size_t prow = ((size_t)e.tile_slot * G.splits + e.chunk) * kBM + tid;
+            float *po = p.ws.part_o + prow * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float o[32];
+                if (e.have) {
+                    tmem_ld32(oaddr + cc * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    __stcg(reinterpret_cast<float4 *>(po + cc * 32 + q * 4),
+                           make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]));
+            }
+            __stcg(p.ws.part_ml + prow, make_float2(e.row_valid ? e.m : -CUDART_INF_F, e.row_valid ? e.l : 0.f));
+            __threadfence();
+            unsigned *cnt = p.ws.row_cnt + (size_t)e.tile_slot * kBM + tid;
+            const unsigned prev = atomicAdd(cnt, 1u);
+            if (prev != (unsigned)(e.nchunks - 1)) return true;
+            __threadfence();
+            float M = -CUDART_INF_F;
+            for (int c = 0; c < e.nchunks; ++c) {
+                const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
+                M = fmaxf(M, ml.x);
+            }
+            float L = 0.f;
+            float wgt[64];
+            const int nc = e.nchunks < 64 ? e.nchunks : 64;
+            for (int c = 0; c < nc; ++c) {
+                const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
+                wgt[c] = (ml.y == 0.f || M == -CUDART_INF_F) ? 0.f : ex2(ml.x - M);
+                L += wgt[c] * ml.y;
+            }
+            const float inv = (e.row_valid && L > 0.f) ? 1.f / L : 0.f;
+            // merge 32 columns at a time, chunks in fixed order
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float acc[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                for (int c = 0; c < nc; ++c) {
+                    if (wgt[c] == 0.f) continue;
+                    const float *src = p.ws.part_o + (((size_t)e.tile_slot * G.splits + c) * kBM + tid) * D + cc * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
+                        acc[i] = fmaf(wgt[c], v.x, acc[i]);
+                        acc[i + 1] = fmaf(wgt[c], v.y, acc[i + 1]);
+                        acc[i + 2] = fmaf(wgt[c], v.z, acc[i + 2]);
+                        acc[i + 3] = fmaf(wgt[c], v.w, acc[i + 3]);
+                    }
+                }
+                if (row < G.n) {
+                    __nv_bfloat16 *orow = p.O + ((size_t)e.bh * G.n + row) * D + cc * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i + 2 * k] * inv, acc[i + 2 * k + 1] * inv);
+                            w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(orow + i) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+            }
+            atomicExch(cnt, 0u);  // ready for the next call
+            return true;
+        };
+
+        uint32_t g = 0, qcnt = 0;
+        bool ok = true;
+        for (uint32_t ui_idx = 0; ok; ++ui_idx) {
             const uint32_t slot = ui_idx % kNU;
-            if (!wait_warp(bar(B_UFULL + slot), (ui_idx / kNU) & 1, ctl)) break;
+            if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
             const UnitInfo ui = ring[slot];
-            mbar_arrive(bar(B_UEMPTY + slot));
+            mbar_arrive(bar(C::B_UE + slot));
             if (ui.kind == kUnitEnd) break;
             const int beta = ui.bh / G.H;
             const int row = ui.q0 + tid;
             const bool row_valid = row < G.n && (!p.key_mask || p.key_mask[(size_t)beta * G.n + row] != 0);
+            Pend cur;
+            cur.kind = ui.kind;
+            cur.bh = ui.bh;
+            cur.q0 = ui.q0;
+            cur.tile_slot = ui.tile_slot;
+            cur.chunk = ui.chunk;
+            cur.nchunks = ui.nchunks;
+            cur.have = ui.n_steps > 0;
+            cur.row_valid = row_valid;
+            cur.ob = qcnt & 1;
+            if (ui.n_steps == 0) {
+                if (pe.kind != kUnitEnd && !(ok = epilogue(pe))) break;
+                pe.kind = kUnitEnd;
+                cur.m = -CUDART_INF_F;
+                cur.l = 0.f;
+                cur.g_last = 0;
+                if (!(ok = epilogue(cur))) break;
+                continue;
+            }
+            ++qcnt;
             float m_ref = -CUDART_INF_F, l = 0.f;
-            bool ok = true;
+            const uint32_t obase = tmem + lane_base + C::O_COL + cur.ob * D;
             for (int t = 0; t < ui.n_steps; ++t, ++g) {
-                const uint32_t st = g % C::STAGES, sb = g & 1, pb = g & 1;
-                if (!(ok = wait_warp(bar(B_KFULL + st), (g / C::STAGES) & 1, ctl))) break;
-                if (!(ok = wait_warp(bar(B_SFULL + sb), (g >> 1) & 1, ctl))) break;
+                const uint32_t ii = g % kSI, sb = g & 1, pb = g & 1;
+                if (!(ok = wait_warp(bar(C::B_IF + ii), (g / kSI) & 1, ctl))) break;
+                const StepInfo si = steps[ii];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_IE + ii));
+                if (!(ok = wait_warp(bar(C::B_SF + sb), (g >> 1) & 1, ctl))) break;
                 tc_fence_after();
-                const StepInfo si = steps[st];
                 const bool w0 = (si.allow >> (0 + hf)) & 1u;  // warp-uniform
                 const bool w1 = (si.allow >> (2 + hf)) & 1u;
                 float s[4][32];
@@ -583,15 +835,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!((si.kmask[1] >> c) & 1ull)) s[2 + (c >> 5)][c & 31] = -CUDART_INF_F;
                     }
                 }
-                float mx = -CUDART_INF_F;
+                float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
                 if (u0) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(s[0][c], s[1][c]));
+                    for (int c = 0; c < 32; c += 2) {
+                        mx0 = fmaxf(mx0, fmaxf(s[0][c], s[0][c + 1]));
+                        mx1 = fmaxf(mx1, fmaxf(s[1][c], s[1][c + 1]));
+                    }
                 }
                 if (u1) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(s[2][c], s[3][c]));
+                    for (int c = 0; c < 32; c += 2) {
+                        mx2 = fmaxf(mx2, fmaxf(s[2][c], s[2][c + 1]));
+                        mx3 = fmaxf(mx3, fmaxf(s[3][c], s[3][c + 1]));
+                    }
                 }
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 const float m_new = fmaxf(m_ref, mx * sl2);
                 bool resc = false;
                 float alpha = 1.f;
@@ -603,160 +862,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
                 uint32_t pk[64];
-                float ls0 = 0.f, ls1 = 0.f;
+                float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const bool use = half == 0 ? u0 : u1;
+                    if (use) {
 #pragma unroll
-                    for (int c = 0; c < 64; c += 2) {
-                        float p0 = 0.f, p1 = 0.f;
-                        if (use) {
-                            p0 = ex2(fmaf(s[2 * half + (c >> 5)][c & 31], sl2, neg_m));
-                            p1 = ex2(fmaf(s[2 * half + (c >> 5)][(c & 31) + 1], sl2, neg_m));
+                        for (int c = 0; c < 64; c += 4) {
+                            const float *sp = &s[2 * half + (c >> 5)][c & 31];
+                            const float p0 = ex2(fmaf(sp[0], sl2, neg_m));
+                            const float p1 = ex2(fmaf(sp[1], sl2, neg_m));
+                            const float p2 = ex2(fmaf(sp[2], sl2, neg_m));
+                            const float p3 = ex2(fmaf(sp[3], sl2, neg_m));
+                            ls0 += p0;
+                            ls1 += p1;
+                            ls2 += p2;
+                            ls3 += p3;
+                            __nv_bfloat162 b01 = __floats2bfloat162_rn(p0, p1);
+                            __nv_bfloat162 b23 = __floats2bfloat162_rn(p2, p3);
+                            pk[half * 32 + (c >> 1)] = *reinterpret_cast<uint32_t *>(&b01);
+                            pk[half * 32 + (c >> 1) + 1] = *reinterpret_cast<uint32_t *>(&b23);
                         }
-                        ls0 += p0;
-                        ls1 += p1;
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                        pk[half * 32 + (c >> 1)] = *reinterpret_cast<uint32_t *>(&b2);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) pk[half * 32 + c] = 0u;
                     }
                 }
-                l += ls0 + ls1;
+                l += (ls0 + ls1) + (ls2 + ls3);
                 // P buffer pb is free once PV of step g-2 completed
-                if (g >= 2 && !(ok = wait_warp(bar(B_PVDONE + pb), ((g - 2) >> 1) & 1, ctl))) break;
-                uint8_t *pbuf = smem + C::P_OFF + pb * C::P_BYTES;
+                if (g >= 2 && !(ok = wait_warp(bar(C::B_PV + pb), ((g - 2) >> 1) & 1, ctl))) break;
+                {
+                    uint32_t q0[32], q1[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 v = make_uint4(pk[half * 32 + ch * 4 + 0], pk[half * 32 + ch * 4 + 1],
-                                             pk[half * 32 + ch * 4 + 2], pk[half * 32 + ch * 4 + 3]);
-                        *reinterpret_cast<uint4 *>(pbuf + half * kRegionBytes + tid * 128 +
-                                                   ((ch ^ (tid & 7)) << 4)) = v;
+                    for (int i = 0; i < 32; ++i) {
+                        q0[i] = pk[i];
+                        q1[i] = pk[32 + i];
                     }
+                    tmem_st32u(tmem + lane_base + sb * kBN, q0);
+                    tmem_st32u(tmem + lane_base + sb * kBN + 32, q1);
+                    tmem_wait_st();
                 }
-                fence_proxy_async_smem();
                 if (__any_sync(kFull, resc)) {
-                    if (!(ok = wait_warp(bar(B_PVDONE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, ctl))) break;
+                    if (!(ok = wait_warp(bar(C::B_PV + ((g - 1) & 1)), ((g - 1) >> 1) & 1, ctl))) break;
                     tc_fence_after();
                     const float a = resc ? alpha : 1.f;
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
                         float o[32];
-                        tmem_ld32(tmem + lane_base + C::O_COL + cc * 32, o);
+                        tmem_ld32(obase + cc * 32, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= a;
-                        tmem_st32(tmem + lane_base + C::O_COL + cc * 32, o);
+                        tmem_st32(obase + cc * 32, o);
                     }
                     tmem_wait_st();
                 }
                 tc_fence_before();
-                mbar_arrive(bar(B_PFULL + pb));
+                mbar_arrive(bar(C::B_PF + pb));
+                if (t == 0 && pe.kind != kUnitEnd) {  // previous unit's epilogue, now off the critical path
+                    if (!(ok = epilogue(pe))) break;
+                    pe.kind = kUnitEnd;
+                }
             }
             if (!ok) break;
-            // ---------------------------------------------------- epilogue
-            if (ui.n_steps > 0) {
-                const uint32_t gl = g - 1;
-                if (!wait_warp(bar(B_PVDONE + (gl & 1)), (gl >> 1) & 1, ctl)) break;
-                tc_fence_after();
-            }
-            const bool have = ui.n_steps > 0;
-            if (ui.kind == kUnitDirect) {
-                const float inv = (row_valid && l > 0.f) ? 1.f / l : 0.f;
-                __nv_bfloat16 *orow = p.O + ((size_t)ui.bh * G.n + (row < G.n ? row : 0)) * D;
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    float o[32];
-                    if (have) {
-                        tmem_ld32(tmem + lane_base + C::O_COL + cc * 32, o);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-                    }
-                    if (row < G.n) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t w4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                __nv_bfloat162 b2 =
-                                    __floats2bfloat162_rn(o[q * 8 + 2 * e] * inv, o[q * 8 + 2 * e + 1] * inv);
-                                w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                            }
-                            *reinterpret_cast<uint4 *>(orow + cc * 32 + q * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
-                    }
-                }
-            } else {
-                // split chunk: publish this row's partial, last arrival merges the row
-                const size_t prow = ((size_t)ui.tile_slot * G.splits + ui.chunk) * kBM + tid;
-                float *po = p.ws.part_o + prow * D;
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    float o[32];
-                    if (have) {
-                        tmem_ld32(tmem + lane_base + C::O_COL + cc * 32, o);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-                    }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        __stcg(reinterpret_cast<float4 *>(po + cc * 32 + q * 4),
-                               make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]));
-                }
-                __stcg(p.ws.part_ml + prow, make_float2(row_valid ? m_ref : -CUDART_INF_F, row_valid ? l : 0.f));
-                __threadfence();
-                unsigned *cnt = p.ws.row_cnt + (size_t)ui.tile_slot * kBM + tid;
-                const unsigned prev = atomicAdd(cnt, 1u);
-                if (prev == (unsigned)(ui.nchunks - 1)) {
-                    __threadfence();
-                    float M = -CUDART_INF_F;
-                    for (int c = 0; c < ui.nchunks; ++c) {
-                        const float2 ml = __ldcg(p.ws.part_ml + ((size_t)ui.tile_slot * G.splits + c) * kBM + tid);
-                        M = fmaxf(M, ml.x);
-                    }
-                    float acc[D];
-#pragma unroll
-                    for (int i = 0; i < D; ++i) acc[i] = 0.f;
-                    float L = 0.f;
-                    for (int c = 0; c < ui.nchunks; ++c) {
-                        const size_t pr = ((size_t)ui.tile_slot * G.splits + c) * kBM + tid;
-                        const float2 ml = __ldcg(p.ws.part_ml + pr);
-                        if (ml.y == 0.f || M == -CUDART_INF_F) continue;
-                        const float wgt = ex2(ml.x - M);
-                        L += wgt * ml.y;
-                        const float *src = p.ws.part_o + pr * D;
-#pragma unroll
-                        for (int i = 0; i < D; i += 4) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
-                            acc[i] = fmaf(wgt, v.x, acc[i]);
-                            acc[i + 1] = fmaf(wgt, v.y, acc[i + 1]);
-                            acc[i + 2] = fmaf(wgt, v.z, acc[i + 2]);
-                            acc[i + 3] = fmaf(wgt, v.w, acc[i + 3]);
-                        }
-                    }
-                    const float inv = (row_valid && L > 0.f) ? 1.f / L : 0.f;
-                    if (row < G.n) {
-                        __nv_bfloat16 *orow = p.O + ((size_t)ui.bh * G.n + row) * D;
-#pragma unroll
-                        for (int i = 0; i < D; i += 8) {
-                            uint32_t w4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i + 2 * e] * inv, acc[i + 2 * e + 1] * inv);
-                                w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                            }
-                            *reinterpret_cast<uint4 *>(orow + i) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                        }
-                    }
-                    atomicExch(cnt, 0u);  // ready for the next call
-                }
-            }
-            tc_fence_before();
+            cur.m = m_ref;
+            cur.l = l;
+            cur.g_last = g - 1;
+            pe = cur;
         }
+        if (ok && pe.kind != kUnitEnd) epilogue(pe);
+        tc_fence_before();
     }
 
     tc_fence_before();
@@ -828,7 +1003,7 @@ Geometry bigbird_geometry(const Problem &p, const TcConfig &cfg) {
     G.n_split_units = (int)(BH * G.gtiles * G.splits);
     G.total_units = G.n_split_units + (int)(BH * (G.tiles - G.gtiles));
     G.scale_log2 = 1.4426950408889634f / sqrtf((float)p.d);
-    G.wait_limit = cfg.wait_limit;
+    G.wait_ns = (unsigned long long)cfg.wait_limit * 1000ull;
     return G;
 }
 

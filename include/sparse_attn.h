@@ -98,7 +98,8 @@ sa_status build_bigbird_pattern(uint64_t seed, int H, int n, int b, int g, int w
  *   to the device), shared by all batch entries; -1 entries are ignored. May
  *   be NULL when r == 0. An entry outside [-1, n/b) is skipped and latches
  *   SA_ERR_BAD_INDEX.
- * key_mask: DEVICE uint8 [B][n], nonzero = valid token, or NULL (all valid).
+ * key_mask: DEVICE uint8 [B][n], nonzero = valid token, or NULL (all valid);
+ *   16-byte aligned.
  * dtype: SA_BF16 (tensor-core path) or SA_FP32 (exact fp32 SIMT path).
  * Scratch: global query blocks may be split across CTAs (split-KV) with a
  *   fixed-order merge; their partials live in the workspace (see
@@ -168,8 +169,8 @@ const char *sa_status_string(sa_status status);
  * Options (process-wide; set them before issuing calls):
  *  SA_OPT_FORCE_SIMT   value != 0: run bf16 calls on the exact SIMT kernels
  *                      instead of the tensor-core kernels (a cross-check path).
- *  SA_OPT_WAIT_LIMIT   iteration bound of every pipeline wait in the
- *                      tensor-core kernels (default 1<<22, about a second);
+ *  SA_OPT_WAIT_LIMIT   time bound, in microseconds, of every pipeline wait
+ *                      in the tensor-core kernels (default 2000000 = 2 s);
  *                      value <= 0 restores the default.
  *  SA_OPT_MAX_SPLITS   upper bound on split-KV chunks per global row tile
  *                      (default 16, 1 disables splitting).
