@@ -43,10 +43,8 @@ using namespace ptx;
 
 constexpr int kBM = 128;           // query rows per tile = TMEM lanes
 constexpr int kBN = 128;           // keys per step = S tile columns
-constexpr int kThreads = 256;
 constexpr int kNU = 4;             // unit-info ring depth
-constexpr int kSI = 8;             // step-info ring depth
-constexpr int kSoftmaxThread0 = 128;
+constexpr int kSI = 6;             // step-info ring depth
 constexpr int kTargetChunkSteps = 64;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (factor 256)
 constexpr unsigned kFull = 0xffffffffu;
@@ -58,7 +56,7 @@ enum UnitKind { kUnitEnd = 0, kUnitDirect = 1, kUnitSplit = 2 };
 struct UnitInfo {
     int kind, bh, q0, n_steps;
     int tile_slot, chunk, nchunks, step0;  // split bookkeeping; first sweep step (-1: block list)
-    int j0, j1, pad0, pad1;                // BigBird query blocks of the two halves (-1: none)
+    int j0, j1, pad0, pad1;                // BigBird query blocks of the halves (-1: none); pad0: list length
     int pad[4];
 };
 static_assert(sizeof(UnitInfo) == 64, "UnitInfo layout");
@@ -73,29 +71,38 @@ static_assert(sizeof(StepInfo) == 32, "StepInfo layout");
 
 template <int D>
 struct Cfg {
-    static constexpr int KST = (D == 64) ? 4 : 3;  // K stages
-    static constexpr int VST = (D == 64) ? 5 : 3;  // V stages (released later than K)
-    static constexpr int NQ = (D == 64) ? 2 : 1;
+    // Query tiles in flight per CTA: two independent pipelines for d = 64
+    // (one tile's softmax overlaps the other's waits and MMAs), one for d = 128.
+    static constexpr int NT = (D == 64) ? 2 : 1;
+    static constexpr int THREADS = 128 + 128 * NT;  // control warps + one softmax warpgroup per tile
+    static constexpr int NS = (NT == 2) ? 1 : 2;    // S buffers per tile; P is written over S
+    static constexpr int KST = 3, VST = 3, NQ = 1;  // K / V / Q stages per tile
     static constexpr int TILE_BYTES = 128 * D * 2;  // Q tile / K step / V step
+    // per-tile big buffers (1024-B aligned), then per-tile small areas
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + NQ * TILE_BYTES;
     static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
-    static constexpr int SMALL_OFF = V_OFF + VST * TILE_BYTES;
-    static constexpr int BAR_OFF = SMALL_OFF;          // 64 barriers max
-    static constexpr int MISC_OFF = SMALL_OFF + 512;   // TMEM address, abort flag
-    static constexpr int UNIT_OFF = MISC_OFF + 64;
+    static constexpr int BIG = V_OFF + VST * TILE_BYTES;
+    // barrier slots within a tile's small area
+    static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
+                         B_IF = B_VE + VST, B_IE = B_IF + kSI, B_SF = B_IE + kSI, B_PF = B_SF + NS, B_PV = B_PF + NS,
+                         B_UF = B_PV + NS, B_UE = B_UF + kNU, B_DRAIN = B_UE + kNU, B_COUNT = B_DRAIN + 1;
+    static constexpr int BAR_OFF = 0;
+    static constexpr int UNIT_OFF = (B_COUNT * 8 + 15) & ~15;
     static constexpr int STEP_OFF = UNIT_OFF + kNU * 64;
-    static constexpr int LIST_OFF = STEP_OFF + kSI * 32;  // producer's block list (32 entries)
-    static constexpr int SMEM_BYTES = LIST_OFF + 32 * 4;
+    static constexpr int LIST_OFF = STEP_OFF + kSI * 32;  // two lists: the next unit is decoded early
+    static constexpr int SMALL = LIST_OFF + 2 * 32 * 4;
+    static constexpr int SMALL_OFF = NT * BIG;
+    static constexpr int MISC_OFF = SMALL_OFF + NT * SMALL;  // TMEM address, abort flag
+    static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr int ALLOC_BYTES = SMEM_BYTES + 1024;  // slack for 1024-B alignment
+    // TMEM: each tile owns TILE_COLS columns: NS S buffers of 128, then two O buffers of D
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t O_COL = 256;  // O buffer ob at O_COL + ob * D
-    // barrier slots
-    static constexpr int B_QF = 0, B_QE = 2, B_KF = 4, B_KE = 8, B_VF = 12, B_VE = 17, B_IF = 22,
-                         B_IE = B_IF + kSI, B_SF = B_IE + kSI, B_PF = B_SF + 2, B_PV = B_PF + 2, B_UF = B_PV + 2,
-                         B_UE = B_UF + kNU, B_DRAIN = B_UE + kNU, B_COUNT = B_DRAIN + 1;
-    static_assert(KST <= 4 && VST <= 5 && NQ <= 2, "ring depths");
-    static_assert(B_COUNT * 8 <= 512, "barrier area");
+    static constexpr uint32_t TILE_COLS = TMEM_COLS / NT;
+    static constexpr uint32_t O_COL = NS * 128;
+
+    static_assert(O_COL + 2 * D <= TILE_COLS, "TMEM columns per tile");
+    static_assert(BIG % 1024 == 0, "tile buffers stay 1024-B aligned");
 };
 static_assert(Cfg<128>::ALLOC_BYTES <= 232448, "d=128 shared memory budget");
 static_assert(Cfg<64>::ALLOC_BYTES <= 232448, "d=64 shared memory budget");
@@ -228,6 +235,17 @@ __device__ __forceinline__ bool block_has_valid_lane(const uint8_t *km, int kb, 
     return any != 0;
 }
 
+// Any valid key in block kb (warp-uniform answer).
+__device__ __forceinline__ bool block_has_valid_warp(const uint8_t *km, int kb, int b) {
+    const int lane = threadIdx.x & 31;
+    bool any = false;
+    if (lane < b / 16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(km + (size_t)kb * b) + lane);
+        any = (v.x | v.y | v.z | v.w) != 0;
+    }
+    return __any_sync(kFull, any);
+}
+
 // 64-bit validity of keys [k0, k0 + 64) (warp-uniform).
 __device__ __forceinline__ uint64_t key_bits64(const uint8_t *km, int k0, int n) {
     const int lane = threadIdx.x & 31;
@@ -305,22 +323,38 @@ __device__ __forceinline__ int union_next_slow(const Params &p, const int32_t *r
     return cand < best ? cand : best;
 }
 
+struct UnitPtrs {
+    const uint8_t *km;
+    const int32_t *r0, *r1;
+    int wlo, whi;
+};
+// Key mask row, random lists of the tile's query blocks, and the merged window range.
+__device__ __forceinline__ UnitPtrs unit_ptrs(const Params &p, const UnitInfo &ui) {
+    const Geometry &G = p.geo;
+    UnitPtrs u;
+    const int beta = ui.bh / G.H, h = ui.bh - beta * G.H;
+    u.km = p.key_mask ? p.key_mask + (size_t)beta * G.n : nullptr;
+    u.r0 = (p.rand_idx && G.r > 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j0) * G.r : nullptr;
+    u.r1 = (p.rand_idx && G.r > 0 && ui.j1 >= 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j1) * G.r : nullptr;
+    const int jl = ui.j1 >= 0 ? ui.j1 : ui.j0;
+    u.wlo = max(0, ui.j0 - G.half);
+    u.whi = min(G.nb - 1, jl + G.half);
+    return u;
+}
+
 // ---------------------------------------------------------------- kernel
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// PADDED: a key mask is present. The unpadded instantiation carries no
+// per-key or per-row masking code at all (rows past n are never stored).
+template <int D, bool PADDED>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bigbird_tc_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bars = sbase + C::BAR_OFF;
-    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
-    UnitInfo *ring = reinterpret_cast<UnitInfo *>(smem + C::UNIT_OFF);
-    StepInfo *steps = reinterpret_cast<StepInfo *>(smem + C::STEP_OFF);
-    uint32_t *list = reinterpret_cast<uint32_t *>(smem + C::LIST_OFF);
 
     const Geometry &G = p.geo;
     const int warp = threadIdx.x >> 5;
@@ -329,32 +363,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        for (int i = 0; i < C::NQ; ++i) {
-            mbar_init(bar(C::B_QF + i), 1);
-            mbar_init(bar(C::B_QE + i), 1);
+        for (int x = 0; x < C::NT; ++x) {
+            const uint32_t bb = sbase + C::SMALL_OFF + x * C::SMALL + C::BAR_OFF;
+            auto bar = [&](int i) { return bb + 8u * (uint32_t)i; };
+            mbar_init(bar(C::B_QF), 1);
+            mbar_init(bar(C::B_QE), 1);
+            for (int i = 0; i < C::KST; ++i) {
+                mbar_init(bar(C::B_KF + i), 1);
+                mbar_init(bar(C::B_KE + i), 1);
+            }
+            for (int i = 0; i < C::VST; ++i) {
+                mbar_init(bar(C::B_VF + i), 1);
+                mbar_init(bar(C::B_VE + i), 1);
+            }
+            for (int i = 0; i < kSI; ++i) {
+                mbar_init(bar(C::B_IF + i), 1);
+                mbar_init(bar(C::B_IE + i), 4);  // one arrival per softmax warp
+            }
+            for (int i = 0; i < C::NS; ++i) {
+                mbar_init(bar(C::B_SF + i), 1);
+                mbar_init(bar(C::B_PF + i), 128);
+                mbar_init(bar(C::B_PV + i), 1);
+            }
+            for (int i = 0; i < kNU; ++i) {
+                mbar_init(bar(C::B_UF + i), 1);
+                mbar_init(bar(C::B_UE + i), 1 + 128);
+            }
+            mbar_init(bar(C::B_DRAIN), 1);
         }
-        for (int i = 0; i < C::KST; ++i) {
-            mbar_init(bar(C::B_KF + i), 1);
-            mbar_init(bar(C::B_KE + i), 1);
-        }
-        for (int i = 0; i < C::VST; ++i) {
-            mbar_init(bar(C::B_VF + i), 1);
-            mbar_init(bar(C::B_VE + i), 1);
-        }
-        for (int i = 0; i < kSI; ++i) {
-            mbar_init(bar(C::B_IF + i), 1);
-            mbar_init(bar(C::B_IE + i), 4);  // one arrival per softmax warp
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(C::B_SF + i), 1);
-            mbar_init(bar(C::B_PF + i), 128);
-            mbar_init(bar(C::B_PV + i), 1);
-        }
-        for (int i = 0; i < kNU; ++i) {
-            mbar_init(bar(C::B_UF + i), 1);
-            mbar_init(bar(C::B_UE + i), 1 + 128);
-        }
-        mbar_init(bar(C::B_DRAIN), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -369,30 +405,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ================================================================ producer
+    // Role and tile of this warp: warps 2x and 2x+1 are tile x's producer and
+    // MMA issuer; warps 4 + 4x .. 7 + 4x its softmax warpgroup.
+    int role = -1, x = 0;  // 0 producer, 1 MMA, 2 softmax
+    if (warp < 4) {
+        if ((warp >> 1) < C::NT) {
+            role = warp & 1;
+            x = warp >> 1;
+        }
+    } else {
+        role = 2;
+        x = (warp - 4) >> 2;
+    }
+    const uint32_t tbase = sbase + x * C::BIG;  // this tile's Q/K/V buffers
+    uint8_t *small = smem + C::SMALL_OFF + x * C::SMALL;
+    const uint32_t bars = sbase + C::SMALL_OFF + x * C::SMALL + C::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    UnitInfo *ring = reinterpret_cast<UnitInfo *>(small + C::UNIT_OFF);
+    StepInfo *steps = reinterpret_cast<StepInfo *>(small + C::STEP_OFF);
+    uint32_t *list = reinterpret_cast<uint32_t *>(small + C::LIST_OFF);
+    const uint32_t tmem = *tmem_holder + x * C::TILE_COLS;  // this tile's TMEM columns
+
+    if (role == 0) {
+        // ================================================================ producer (tile x)
+        // Units are decoded (and their key/value blocks prefetched into L2)
+        // one unit ahead of the TMA loads that consume them.
         uint32_t g = 0, qcnt = 0;
-        uint32_t k_arms[C::KST] = {}, v_arms[C::VST] = {}, q_arms[C::NQ] = {};
+        uint32_t k_arms[C::KST] = {}, v_arms[C::VST] = {}, q_arms = 0;
         bool ok = true;
         unsigned u_next = 0;
         if (lane == 0) u_next = atomicAdd(p.ws.counters, 1u);
-        for (uint32_t ui_idx = 0; ok; ++ui_idx) {
+        // decode the next unit from the work counter into ring slot `slot`
+        // and list buffer `lb`; returns its info (kind kUnitEnd when done)
+        auto decode_next = [&](uint32_t ui_idx, uint32_t *lbuf, bool &slow_out) -> UnitInfo {
+            UnitInfo ui = {};
+            slow_out = false;
             int u = (int)__shfl_sync(kFull, u_next, 0);
             if (lane == 0 && u < G.total_units) u_next = atomicAdd(p.ws.counters, 1u);  // prefetch the next
             const uint32_t slot = ui_idx % kNU;
-            if (ui_idx >= kNU && !(ok = wait_warp(bar(C::B_UE + slot), ((ui_idx / kNU) - 1) & 1, ctl))) break;
-            UnitInfo ui = {};
+            if (ui_idx >= kNU && !(ok = wait_warp(bar(C::B_UE + slot), ((ui_idx / kNU) - 1) & 1, ctl))) {
+                ui.kind = kUnitEnd;
+                return ui;
+            }
             if (u >= G.total_units) {
                 ui.kind = kUnitEnd;
                 if (lane == 0) {
                     ring[slot] = ui;
                     mbar_arrive(bar(C::B_UF + slot));
                 }
-                break;
+                return ui;
             }
-            // ---- decode the unit
             int tile;
             if (u < G.n_split_units) {
                 const int per = G.gtiles * G.splits;
@@ -421,167 +484,159 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ui.j0 = tile;
                 ui.j1 = -1;
             }
-            const int beta = ui.bh / G.H, h = ui.bh - beta * G.H;
-            const uint8_t *km = p.key_mask ? p.key_mask + (size_t)beta * G.n : nullptr;
-            const int32_t *r0 = (p.rand_idx && G.r > 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j0) * G.r : nullptr;
-            const int32_t *r1 =
-                (p.rand_idx && G.r > 0 && ui.j1 >= 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j1) * G.r : nullptr;
+            const UnitPtrs up = unit_ptrs(p, ui);
             const int bps = (G.b == 64) ? 2 : 1;  // key blocks per step
-            const int jl = ui.j1 >= 0 ? ui.j1 : ui.j0;
-            const int wlo = max(0, ui.j0 - G.half), whi = min(G.nb - 1, jl + G.half);
-            int nlist = 0;
-            bool slow = false;
             if (ui.step0 < 0) {
                 bool any_row = true;
-                if (km) {
+                if (up.km) {
                     bool a = false;
-                    for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && km[ui.q0 + t] != 0;
+                    for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && up.km[ui.q0 + t] != 0;
                     any_row = __any_sync(kFull, a);
                 }
+                int nlist = 0;
                 if (any_row) {
-                    nlist = build_local_list(p, ui.j0, ui.j1, r0, r1, km, list);
-                    if (nlist < 0) {  // wide pattern: generate the union block by block
-                        slow = true;
+                    nlist = build_local_list(p, ui.j0, ui.j1, up.r0, up.r1, up.km, lbuf);
+                    if (nlist < 0) {  // wide pattern: the union is generated block by block later
+                        slow_out = true;
                         nlist = 0;
-                        for (int x = union_next_slow(p, r0, r1, wlo, whi, -1); x < G.nb;
-                             x = union_next_slow(p, r0, r1, wlo, whi, x)) {
-                            bool has = true;
-                            if (km) has = __any_sync(kFull, lane < G.b / 16 &&
-                                                                 [&] {
-                                                                     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
-                                                                         km + (size_t)x * G.b) + lane);
-                                                                     return (v.x | v.y | v.z | v.w) != 0;
-                                                                 }());
-                            nlist += has ? 1 : 0;
-                        }
+                        for (int xb = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, -1); xb < G.nb;
+                             xb = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, xb))
+                            if (!up.km || block_has_valid_warp(up.km, xb, G.b)) ++nlist;
                     }
                 }
+                ui.pad0 = nlist;
                 ui.n_steps = (nlist + bps - 1) / bps;
             }
+
             if (lane == 0) {
                 ring[slot] = ui;
                 mbar_arrive(bar(C::B_UF + slot));
             }
-            if (ui.n_steps == 0) continue;
+            return ui;
+        };
 
-            // ---- Q tile
-            const uint32_t qb = qcnt % C::NQ;
-            if (qcnt >= C::NQ && !(ok = wait_warp(bar(C::B_QE + qb), ((qcnt / C::NQ) - 1) & 1, ctl))) break;
-            if (lane == 0) {
-                const uint32_t dst = sbase + C::Q_OFF + qb * C::TILE_BYTES;
-                mbar_arrive_expect_tx(bar(C::B_QF + qb), C::TILE_BYTES);
-                for (int dc = 0; dc < D / 64; ++dc)
-                    for (int rh = 0; rh < 2; ++rh)
-                        tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF + qb), dc * 64,
-                                    ui.q0 + rh * 64, ui.bh);
-            }
-            ++q_arms[qb];
-            ++qcnt;
-
-            // ---- key steps
-            int x = -1;  // slow path: last block emitted
-            for (int t = 0; t < ui.n_steps; ++t, ++g) {
-                StepInfo si;
-                si.masked = km ? 1u : 0u;
-                si.allow = 0;
-                si.kmask[0] = si.kmask[1] = ~0ull;
+        bool slow_cur = false, slow_nxt = false;
+        UnitInfo cur = decode_next(0, list, slow_cur);
+        for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
+            uint32_t *lcur = list + (ui_idx & 1) * 32;
+            const UnitInfo nxt = decode_next(ui_idx + 1, list + ((ui_idx + 1) & 1) * 32, slow_nxt);
+            if (!ok) break;
+            if (cur.n_steps > 0) {
+                const UnitPtrs up = unit_ptrs(p, cur);
+                const int nlist = cur.pad0;
+                // ---- Q tile
+                if (qcnt >= 1 && !(ok = wait_warp(bar(C::B_QE), (qcnt - 1) & 1, ctl))) break;
+                if (lane == 0) {
+                    const uint32_t dst = tbase + C::Q_OFF;
+                    mbar_arrive_expect_tx(bar(C::B_QF), C::TILE_BYTES);
+                    for (int dc = 0; dc < D / 64; ++dc)
+                        for (int rh = 0; rh < 2; ++rh)
+                            tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF), dc * 64,
+                                        cur.q0 + rh * 64, cur.bh);
+                }
+                ++q_arms;
+                ++qcnt;
+                // ---- key steps
+                int xs = -1;  // wide patterns: last block emitted
+                for (int t = 0; t < cur.n_steps; ++t, ++g) {
+                    StepInfo si;
+                    si.masked = up.km ? 1u : 0u;
+                    si.allow = 0;
+                    si.kmask[0] = si.kmask[1] = ~0ull;
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    int kb = -1, y = G.n;
-                    bool a0 = false, a1 = false;
-                    if (ui.step0 >= 0) {  // full sweep of a global tile
-                        if (G.b == 64) {
-                            kb = 2 * (ui.step0 + t) + s;
-                            if (kb >= G.nb) kb = -1;
-                            y = kb >= 0 ? kb * 64 : G.n;
+                    for (int s = 0; s < 2; ++s) {
+                        int kb = -1, y = G.n;
+                        bool a0 = false, a1 = false;
+                        if (cur.step0 >= 0) {  // full sweep of a global tile
+                            if (G.b == 64) {
+                                kb = 2 * (cur.step0 + t) + s;
+                                if (kb >= G.nb) kb = -1;
+                                y = kb >= 0 ? kb * 64 : G.n;
+                            } else {
+                                kb = cur.step0 + t;
+                                y = kb * 128 + s * 64;
+                            }
+                            if (kb >= 0) {
+                                a0 = block_allowed(p, up.r0, cur.j0, kb);
+                                a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
+                            }
+                        } else if (!slow_cur) {
+                            const int li = (G.b == 64) ? 2 * t + s : t;
+                            if (li < nlist) {
+                                const uint32_t e = lcur[li];
+                                kb = (int)(e & 0x3FFFFFFFu);
+                                a0 = (e >> 30) & 1u;
+                                a1 = (G.b == 64) ? ((e >> 31) & 1u) : a0;
+                                y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                            }
                         } else {
-                            kb = ui.step0 + t;
-                            y = kb * 128 + s * 64;
+                            if (G.b == 64 || s == 0) {
+                                do {
+                                    xs = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, xs);
+                                } while (xs < G.nb && up.km && !block_has_valid_warp(up.km, xs, G.b));
+                            }
+                            if (xs < G.nb) {
+                                kb = xs;
+                                a0 = block_allowed(p, up.r0, cur.j0, kb);
+                                a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
+                                y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                            }
                         }
-                        if (kb >= 0) {
-                            a0 = block_allowed(p, r0, ui.j0, kb);
-                            a1 = (G.b == 64) ? block_allowed(p, r1, ui.j1, kb) : a0;
+                        si.y[s] = y;
+                        if (kb < 0) continue;
+                        if (up.km) {
+                            const uint64_t bits = key_bits64(up.km, y, G.n);
+                            si.kmask[s] = bits;
+                            if (bits == 0) continue;
                         }
-                    } else if (!slow) {
-                        const int li = (G.b == 64) ? 2 * t + s : t;
-                        if (li < nlist) {
-                            const uint32_t e = list[li];
-                            kb = (int)(e & 0x3FFFFFFFu);
-                            a0 = (e >> 30) & 1u;
-                            a1 = (G.b == 64) ? ((e >> 31) & 1u) : a0;
-                            y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
-                        }
-                    } else {
-                        if (G.b == 64 || s == 0) {
-                            do {
-                                x = union_next_slow(p, r0, r1, wlo, whi, x);
-                            } while (x < G.nb && km &&
-                                     !__any_sync(kFull, lane < G.b / 16 && [&] {
-                                         const uint4 v =
-                                             __ldg(reinterpret_cast<const uint4 *>(km + (size_t)x * G.b) + lane);
-                                         return (v.x | v.y | v.z | v.w) != 0;
-                                     }()));
-                        }
-                        if (x < G.nb) {
-                            kb = x;
-                            a0 = block_allowed(p, r0, ui.j0, kb);
-                            a1 = (G.b == 64) ? block_allowed(p, r1, ui.j1, kb) : a0;
-                            y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
-                        }
+                        si.allow |= (a0 ? 1u : 0u) << (2 * s);
+                        si.allow |= (a1 ? 1u : 0u) << (2 * s + 1);
                     }
-                    si.y[s] = y;
-                    if (kb < 0) continue;
-                    if (km) {
-                        const uint64_t bits = key_bits64(km, y, G.n);
-                        si.kmask[s] = bits;
-                        if (bits == 0) continue;
+                    // step info -> softmax
+                    const uint32_t ii = g % kSI;
+                    if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
+                    if (lane == 0) {
+                        steps[ii] = si;
+                        mbar_arrive(bar(C::B_IF + ii));
                     }
-                    si.allow |= (a0 ? 1u : 0u) << (2 * s);
-                    si.allow |= (a1 ? 1u : 0u) << (2 * s + 1);
+                    // K
+                    const uint32_t sk = g % C::KST;
+                    if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
+                    if (lane == 0) {
+                        const uint32_t kdst = tbase + C::K_OFF + sk * C::TILE_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::TILE_BYTES);
+                        for (int s = 0; s < 2; ++s)
+                            for (int dc = 0; dc < D / 64; ++dc)
+                                tma_load_3d(kdst + dc * kRegionBytes + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
+                                            si.y[s], cur.bh);
+                    }
+                    ++k_arms[sk];
+                    // V
+                    const uint32_t sv = g % C::VST;
+                    if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
+                    if (lane == 0) {
+                        const uint32_t vdst = tbase + C::V_OFF + sv * C::TILE_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::TILE_BYTES);
+                        for (int s = 0; s < 2; ++s)
+                            for (int dc = 0; dc < D / 64; ++dc)
+                                tma_load_3d(vdst + dc * kRegionBytes + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
+                                            si.y[s], cur.bh);
+                    }
+                    ++v_arms[sv];
                 }
-                // step info -> softmax
-                const uint32_t ii = g % kSI;
-                if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
-                if (lane == 0) {
-                    steps[ii] = si;
-                    mbar_arrive(bar(C::B_IF + ii));
-                }
-                // K
-                const uint32_t sk = g % C::KST;
-                if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
-                if (lane == 0) {
-                    const uint32_t kdst = sbase + C::K_OFF + sk * C::TILE_BYTES;
-                    mbar_arrive_expect_tx(bar(C::B_KF + sk), C::TILE_BYTES);
-                    for (int s = 0; s < 2; ++s)
-                        for (int dc = 0; dc < D / 64; ++dc)
-                            tma_load_3d(kdst + dc * kRegionBytes + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
-                                        si.y[s], ui.bh);
-                }
-                ++k_arms[sk];
-                // V
-                const uint32_t sv = g % C::VST;
-                if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
-                if (lane == 0) {
-                    const uint32_t vdst = sbase + C::V_OFF + sv * C::TILE_BYTES;
-                    mbar_arrive_expect_tx(bar(C::B_VF + sv), C::TILE_BYTES);
-                    for (int s = 0; s < 2; ++s)
-                        for (int dc = 0; dc < D / 64; ++dc)
-                            tma_load_3d(vdst + dc * kRegionBytes + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
-                                        si.y[s], ui.bh);
-                }
-                ++v_arms[sv];
             }
+            cur = nxt;
+            slow_cur = slow_nxt;
         }
-        if (!ok && lane == 0) {  // abort: wait for the copies this CTA still has in flight
+        if (!ok && lane == 0) {  // abort: wait for the copies this tile still has in flight
             for (int i = 0; i < C::KST; ++i)
                 if (k_arms[i]) wait_drain(bar(C::B_KF + i), (k_arms[i] - 1) & 1, G.wait_ns);
             for (int i = 0; i < C::VST; ++i)
                 if (v_arms[i]) wait_drain(bar(C::B_VF + i), (v_arms[i] - 1) & 1, G.wait_ns);
-            for (int i = 0; i < C::NQ; ++i)
-                if (q_arms[i]) wait_drain(bar(C::B_QF + i), (q_arms[i] - 1) & 1, G.wait_ns);
+            if (q_arms) wait_drain(bar(C::B_QF), (q_arms - 1) & 1, G.wait_ns);
         }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
+    } else if (role == 1) {
+        // ================================================================ MMA issuer (tile x)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, kBN, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
@@ -590,20 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool pend_first = false;
             uint32_t pend_ob = 0;
             bool ok = true;
+            // O_ob (+)= P_h V_h; P_h is read from TMEM over S buffer h % NS
             auto issue_pv = [&](uint32_t h, bool first, uint32_t ob) -> bool {
-                const uint32_t sv = h % C::VST, pb = h & 1;
-                if (!wait_one(bar(C::B_PF + pb), (h >> 1) & 1, ctl)) return false;
+                const uint32_t sv = h % C::VST, sb = h % C::NS;
+                if (!wait_one(bar(C::B_PF + sb), (h / C::NS) & 1, ctl)) return false;
                 if (!wait_one(bar(C::B_VF + sv), (h / C::VST) & 1, ctl)) return false;
                 tc_fence_after();
-                const uint32_t pt = tmem + pb * kBN;  // P_h (bf16 pairs) over S buffer h & 1
-                const uint32_t va = sbase + C::V_OFF + sv * C::TILE_BYTES;
+                const uint32_t pt = tmem + sb * kBN;
+                const uint32_t va = tbase + C::V_OFF + sv * C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     const uint64_t b = desc_sw128(va + kk * 2048, kRegionBytes);
                     mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(bar(C::B_VE + sv));
-                mma_commit(bar(C::B_PV + pb));
+                mma_commit(bar(C::B_PV + sb));
                 return true;
             };
             for (uint32_t ui_idx = 0; ok; ++ui_idx) {
@@ -614,16 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(C::B_UE + slot));
                 if (kind == kUnitEnd) break;
                 if (n_steps == 0) continue;
-                const uint32_t qb = qcnt % C::NQ;
                 const uint32_t ob = qcnt & 1;
-                if (!(ok = wait_one(bar(C::B_QF + qb), (qcnt / C::NQ) & 1, ctl))) break;
+                if (!(ok = wait_one(bar(C::B_QF), qcnt & 1, ctl))) break;
                 tc_fence_after();
-                const uint32_t qa = sbase + C::Q_OFF + qb * C::TILE_BYTES;
+                const uint32_t qa = tbase + C::Q_OFF;
                 for (int t = 0; t < n_steps; ++t, ++g) {
-                    const uint32_t sk = g % C::KST, sb = g & 1;
+                    const uint32_t sk = g % C::KST, sb = g % C::NS;
                     if (!(ok = wait_one(bar(C::B_KF + sk), (g / C::KST) & 1, ctl))) break;
                     tc_fence_after();
-                    const uint32_t ka = sbase + C::K_OFF + sk * C::TILE_BYTES;
+                    const uint32_t ka = tbase + C::K_OFF + sk * C::TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kRegionBytes + (kk & 3) * 32;
@@ -632,11 +687,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(bar(C::B_KE + sk));
                     mma_commit(bar(C::B_SF + sb));
-                    if (t == n_steps - 1) mma_commit(bar(C::B_QE + qb));
-                    if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
-                    pend = (int)g;
-                    pend_first = (t == 0);
-                    pend_ob = ob;
+                    if (t == n_steps - 1) mma_commit(bar(C::B_QE));
+                    if (C::NS == 1) {
+                        // one S buffer: P_g overwrites S_g, so PV_g precedes S_{g+1}
+                        if (!(ok = issue_pv(g, t == 0, ob))) break;
+                    } else {
+                        // two S buffers: S_{g} overlaps the softmax of step g-1
+                        if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
+                        pend = (int)g;
+                        pend_first = (t == 0);
+                        pend_ob = ob;
+                    }
                 }
                 ++qcnt;
             }
@@ -645,10 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(C::B_DRAIN));
             wait_drain(bar(C::B_DRAIN), 0, G.wait_ns);
         }
-    } else if (warp >= 4) {
-        // ================================================================ softmax / epilogue
-        const int tid = threadIdx.x - kSoftmaxThread0;  // query row within the tile
-        const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    } else if (role == 2) {
+        // ================================================================ softmax / epilogue (tile x)
+        const int tid = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int hf = (G.b == 64) ? (tid >> 6) : 0;
         const float sl2 = G.scale_log2;
 
@@ -663,17 +724,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         Pend pe;
         pe.kind = kUnitEnd;
 
-        auto epilogue = [&](const Pend &e) -> bool {
+        // `wait_pv` false: the caller already saw PV of step g_last complete.
+        auto epilogue = [&](const Pend &e, bool wait_pv) -> bool {
             const int row = e.q0 + tid;
             const uint32_t oaddr = tmem + lane_base + C::O_COL + e.ob * D;
             if (e.have) {
-                if (!wait_warp(bar(C::B_PV + (e.g_last & 1)), (e.g_last >> 1) & 1, ctl)) return false;
+                if (wait_pv &&
+                    !wait_warp(bar(C::B_PV + (e.g_last % C::NS)), (e.g_last / C::NS) & 1, ctl))
+                    return false;
                 tc_fence_after();
             }
             if (e.kind == kUnitDirect) {
                 const float inv = (e.row_valid && e.l > 0.f) ? 1.f / e.l : 0.f;
                 __nv_bfloat16 *orow = p.O + ((size_t)e.bh * G.n + (row < G.n ? row : 0)) * D;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     float o[32];
                     if (e.have) {
@@ -702,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // split chunk: publish this row's partial; the last arrival merges the row
             const size_t prow = ((size_t)e.tile_slot * G.splits + e.chunk) * kBM + tid;
             float *po = p.ws.part_o + prow * D;
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 float o[32];
                 if (e.have) {
@@ -729,12 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 M = fmaxf(M, ml.x);
             }
             float L = 0.f;
-            float wgt[64];
-            const int nc = e.nchunks < 64 ? e.nchunks : 64;
-            for (int c = 0; c < nc; ++c) {
+            for (int c = 0; c < e.nchunks; ++c) {
                 const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
-                wgt[c] = (ml.y == 0.f || M == -CUDART_INF_F) ? 0.f : ex2(ml.x - M);
-                L += wgt[c] * ml.y;
+                if (ml.y > 0.f) L += ex2(ml.x - M) * ml.y;
             }
             const float inv = (e.row_valid && L > 0.f) ? 1.f / L : 0.f;
             // merge 32 columns at a time, chunks in fixed order
@@ -743,16 +804,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float acc[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-                for (int c = 0; c < nc; ++c) {
-                    if (wgt[c] == 0.f) continue;
+                for (int c = 0; c < e.nchunks; ++c) {
+                    const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
+                    if (!(ml.y > 0.f)) continue;
+                    const float wk = ex2(ml.x - M);
                     const float *src = p.ws.part_o + (((size_t)e.tile_slot * G.splits + c) * kBM + tid) * D + cc * 32;
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
-                        acc[i] = fmaf(wgt[c], v.x, acc[i]);
-                        acc[i + 1] = fmaf(wgt[c], v.y, acc[i + 1]);
-                        acc[i + 2] = fmaf(wgt[c], v.z, acc[i + 2]);
-                        acc[i + 3] = fmaf(wgt[c], v.w, acc[i + 3]);
+                        acc[i] = fmaf(wk, v.x, acc[i]);
+                        acc[i + 1] = fmaf(wk, v.y, acc[i + 1]);
+                        acc[i + 2] = fmaf(wk, v.z, acc[i + 2]);
+                        acc[i + 3] = fmaf(wk, v.w, acc[i + 3]);
                     }
                 }
                 if (row < G.n) {
@@ -783,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ui.kind == kUnitEnd) break;
             const int beta = ui.bh / G.H;
             const int row = ui.q0 + tid;
-            const bool row_valid = row < G.n && (!p.key_mask || p.key_mask[(size_t)beta * G.n + row] != 0);
+            const bool row_valid = row < G.n && (!PADDED || p.key_mask[(size_t)beta * G.n + row] != 0);
             Pend cur;
             cur.kind = ui.kind;
             cur.bh = ui.bh;
@@ -795,118 +858,128 @@ __global__ void __launch_bounds__(kThreads, 1)
             cur.row_valid = row_valid;
             cur.ob = qcnt & 1;
             if (ui.n_steps == 0) {
-                if (pe.kind != kUnitEnd && !(ok = epilogue(pe))) break;
+                if (pe.kind != kUnitEnd && !(ok = epilogue(pe, true))) break;
                 pe.kind = kUnitEnd;
                 cur.m = -CUDART_INF_F;
                 cur.l = 0.f;
                 cur.g_last = 0;
-                if (!(ok = epilogue(cur))) break;
+                if (!(ok = epilogue(cur, true))) break;
                 continue;
             }
             ++qcnt;
             float m_ref = -CUDART_INF_F, l = 0.f;
             const uint32_t obase = tmem + lane_base + C::O_COL + cur.ob * D;
             for (int t = 0; t < ui.n_steps; ++t, ++g) {
-                const uint32_t ii = g % kSI, sb = g & 1, pb = g & 1;
+                const uint32_t ii = g % kSI, sb = g % C::NS;
                 if (!(ok = wait_warp(bar(C::B_IF + ii), (g / kSI) & 1, ctl))) break;
-                const StepInfo si = steps[ii];
+                const uint32_t allow = steps[ii].allow;
+                uint64_t km0 = ~0ull, km1 = ~0ull;
+                if (PADDED) {
+                    km0 = steps[ii].kmask[0];
+                    km1 = steps[ii].kmask[1];
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_IE + ii));
-                if (!(ok = wait_warp(bar(C::B_SF + sb), (g >> 1) & 1, ctl))) break;
+                if (!(ok = wait_warp(bar(C::B_SF + sb), (g / C::NS) & 1, ctl))) break;
                 tc_fence_after();
-                const bool w0 = (si.allow >> (0 + hf)) & 1u;  // warp-uniform
-                const bool w1 = (si.allow >> (2 + hf)) & 1u;
-                float s[4][32];
+                // The buffer holding S_g receives P_g; PV of step g - NS must have
+                // read the previous P there (completes before S_g in issue order;
+                // the wait also establishes that PV_{g-1} completed when NS == 1).
+                if (g >= (uint32_t)C::NS &&
+                    !(ok = wait_warp(bar(C::B_PV + sb), ((g - C::NS) / C::NS) & 1, ctl)))
+                    break;
                 const uint32_t sa = tmem + lane_base + sb * kBN;
-                if (w0) {
-                    tmem_ld32(sa + 0, s[0]);
-                    tmem_ld32(sa + 32, s[1]);
-                }
-                if (w1) {
-                    tmem_ld32(sa + 64, s[2]);
-                    tmem_ld32(sa + 96, s[3]);
-                }
-                tmem_wait_ld();
-                const bool u0 = w0 && row_valid, u1 = w1 && row_valid;
-                if (si.masked) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        if (!((si.kmask[0] >> c) & 1ull)) s[c >> 5][c & 31] = -CUDART_INF_F;
-                        if (!((si.kmask[1] >> c) & 1ull)) s[2 + (c >> 5)][c & 31] = -CUDART_INF_F;
-                    }
-                }
-                float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
-                if (u0) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        mx0 = fmaxf(mx0, fmaxf(s[0][c], s[0][c + 1]));
-                        mx1 = fmaxf(mx1, fmaxf(s[1][c], s[1][c + 1]));
-                    }
-                }
-                if (u1) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        mx2 = fmaxf(mx2, fmaxf(s[2][c], s[2][c + 1]));
-                        mx3 = fmaxf(mx3, fmaxf(s[3][c], s[3][c + 1]));
-                    }
-                }
-                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-                const float m_new = fmaxf(m_ref, mx * sl2);
-                bool resc = false;
+                // Stream the two 64-key halves: each is loaded, reduced and
+                // exponentiated against the running reference m_ref, then
+                // written back as bf16 P over the first 64 columns of S_g.
                 float alpha = 1.f;
-                if (m_new > m_ref + kRescaleLog2) {
-                    alpha = ex2(m_ref - m_new);
-                    resc = (m_ref != -CUDART_INF_F) && t > 0;
-                    l *= alpha;
-                    m_ref = m_new;
-                }
-                const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
-                uint32_t pk[64];
-                float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
-#pragma unroll
+                bool resc = false;  // O needs a rescale by alpha
+                float lsum = 0.f;
+#pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
-                    const bool use = half == 0 ? u0 : u1;
-                    if (use) {
+                    const bool w_ok = (allow >> (2 * half + hf)) & 1u;  // warp-uniform
+                    uint32_t pk[32];
+                    if (w_ok) {
+                        float s0[32], s1[32];
+                        tmem_ld32(sa + half * 64, s0);
+                        tmem_ld32(sa + half * 64 + 32, s1);
+                        tmem_wait_ld();
+                        if (PADDED) {
+                            // padded row: nothing allowed; padded keys: -inf
+                            const uint64_t kmh = row_valid ? (half ? km1 : km0) : 0ull;
+                            const uint32_t lo = (uint32_t)kmh, hi = (uint32_t)(kmh >> 32);
 #pragma unroll
-                        for (int c = 0; c < 64; c += 4) {
-                            const float *sp = &s[2 * half + (c >> 5)][c & 31];
-                            const float p0 = ex2(fmaf(sp[0], sl2, neg_m));
-                            const float p1 = ex2(fmaf(sp[1], sl2, neg_m));
-                            const float p2 = ex2(fmaf(sp[2], sl2, neg_m));
-                            const float p3 = ex2(fmaf(sp[3], sl2, neg_m));
+                            for (int i = 0; i < 32; ++i) {
+                                s0[i] = ((lo >> i) & 1u) ? s0[i] : -CUDART_INF_F;
+                                s1[i] = ((hi >> i) & 1u) ? s1[i] : -CUDART_INF_F;
+                            }
+                        }
+                        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            mx0 = fmaxf(mx0, s0[i]);
+                            mx1 = fmaxf(mx1, s0[i + 1]);
+                            mx2 = fmaxf(mx2, s1[i]);
+                            mx3 = fmaxf(mx3, s1[i + 1]);
+                        }
+                        const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                        if (m_new > m_ref + kRescaleLog2) {
+                            const float a = ex2(m_ref - m_new);  // 0 when m_ref was -inf
+                            if (m_ref != -CUDART_INF_F) {
+                                if (t > 0) resc = true;
+                                alpha *= a;
+                                if (half == 1 && ((allow >> hf) & 1u)) {
+                                    // the first half's P already used the old reference
+                                    uint32_t q[32];
+                                    tmem_ld32u(sa, q);
+                                    tmem_wait_ld();
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) {
+                                        __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&q[i]);
+                                        float2 f = __bfloat1622float2(b2);
+                                        b2 = __floats2bfloat162_rn(f.x * a, f.y * a);
+                                        q[i] = *reinterpret_cast<uint32_t *>(&b2);
+                                    }
+                                    tmem_st32u(sa, q);
+                                }
+                            }
+                            l *= a;
+                            lsum *= a;
+                            m_ref = m_new;
+                        }
+                        const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
+                        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float p0 = ex2(fmaf(s0[i], sl2, neg_m));
+                            const float p1 = ex2(fmaf(s0[i + 1], sl2, neg_m));
+                            const float p2 = ex2(fmaf(s1[i], sl2, neg_m));
+                            const float p3 = ex2(fmaf(s1[i + 1], sl2, neg_m));
                             ls0 += p0;
                             ls1 += p1;
                             ls2 += p2;
                             ls3 += p3;
                             __nv_bfloat162 b01 = __floats2bfloat162_rn(p0, p1);
                             __nv_bfloat162 b23 = __floats2bfloat162_rn(p2, p3);
-                            pk[half * 32 + (c >> 1)] = *reinterpret_cast<uint32_t *>(&b01);
-                            pk[half * 32 + (c >> 1) + 1] = *reinterpret_cast<uint32_t *>(&b23);
+                            pk[i >> 1] = *reinterpret_cast<uint32_t *>(&b01);
+                            pk[16 + (i >> 1)] = *reinterpret_cast<uint32_t *>(&b23);
                         }
+                        lsum += (ls0 + ls1) + (ls2 + ls3);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) pk[half * 32 + c] = 0u;
+                        for (int i = 0; i < 32; ++i) pk[i] = 0u;
                     }
+                    tmem_st32u(sa + half * 32, pk);
                 }
-                l += (ls0 + ls1) + (ls2 + ls3);
-                // P buffer pb is free once PV of step g-2 completed
-                if (g >= 2 && !(ok = wait_warp(bar(C::B_PV + pb), ((g - 2) >> 1) & 1, ctl))) break;
-                {
-                    uint32_t q0[32], q1[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        q0[i] = pk[i];
-                        q1[i] = pk[32 + i];
-                    }
-                    tmem_st32u(tmem + lane_base + sb * kBN, q0);
-                    tmem_st32u(tmem + lane_base + sb * kBN + 32, q1);
-                    tmem_wait_st();
-                }
+                l += lsum;
+                tmem_wait_st();
                 if (__any_sync(kFull, resc)) {
-                    if (!(ok = wait_warp(bar(C::B_PV + ((g - 1) & 1)), ((g - 1) >> 1) & 1, ctl))) break;
+                    // O must hold PV of step g-1 before it is rescaled
+                    const uint32_t h = g - 1;
+                    if (!(ok = wait_warp(bar(C::B_PV + (h % C::NS)), (h / C::NS) & 1, ctl))) break;
                     tc_fence_after();
                     const float a = resc ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         float o[32];
                         tmem_ld32(obase + cc * 32, o);
@@ -918,9 +991,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 }
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PF + pb));
+                mbar_arrive(bar(C::B_PF + sb));
                 if (t == 0 && pe.kind != kUnitEnd) {  // previous unit's epilogue, now off the critical path
-                    if (!(ok = epilogue(pe))) break;
+                    // NS == 1: the P-buffer wait above already saw PV of step g-1 complete
+                    if (!(ok = epilogue(pe, C::NS != 1))) break;
                     pe.kind = kUnitEnd;
                 }
             }
@@ -930,14 +1004,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             cur.g_last = g - 1;
             pe = cur;
         }
-        if (ok && pe.kind != kUnitEnd) epilogue(pe);
-        tc_fence_before();
+        if (ok && pe.kind != kUnitEnd) epilogue(pe, true);
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == 1) tmem_dealloc(*tmem_holder, C::TMEM_COLS);
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned done = atomicAdd(p.ws.counters + 1, 1u);
@@ -1049,13 +1122,13 @@ cudaError_t launch_bigbird(const Problem &p, const TcConfig &cfg, void *ws, size
     if (!make_qkv_map(&mq, p.Q, BH, p.n, D) || !make_qkv_map(&mk, p.K, BH, p.n, D) ||
         !make_qkv_map(&mv, p.V, BH, p.n, D))
         return cudaErrorInvalidValue;
-    auto kern = bigbird_tc_fwd<D>;
+    auto kern = p.key_mask ? bigbird_tc_fwd<D, true> : bigbird_tc_fwd<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::ALLOC_BYTES);
     if (e != cudaSuccess) return e;
     int grid = cfg.grid_ctas;
     if (grid > prm.geo.total_units) grid = prm.geo.total_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, kThreads, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, prm);
+    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError();
 }
 
