@@ -49,5 +49,10 @@ size_t tc_workspace_bytes(const Problem &p, const TcConfig &cfg);
 size_t tc_workspace_counter_bytes(const Problem &p, const TcConfig &cfg);
 cudaError_t launch_tc(const Problem &p, const TcConfig &cfg, void *workspace, size_t ws_bytes,
                       cudaStream_t stream, int *launches);
+// Longformer parts of the above (tensor-core Longformer translation unit).
+size_t tc_longformer_workspace_bytes(const Problem &p, const TcConfig &cfg);
+size_t tc_longformer_counter_bytes(const Problem &p, const TcConfig &cfg);
+cudaError_t launch_tc_longformer(const Problem &p, const TcConfig &cfg, void *workspace, size_t ws_bytes,
+                                 cudaStream_t stream, int *launches);
 
 }  // namespace sa

@@ -1,0 +1,1255 @@
+// Tensor-core sparse-attention forward for sm_103a (GB300): TMA gathers of
+// key/value blocks into shared memory, tcgen05 MMAs with TMEM accumulators,
+// fp32 online softmax, persistent CTAs fed by a device-side work counter.
+// One kernel template serves both patterns; the BigBird and Longformer host
+// sides instantiate it in their own translation units.
+//
+// The BigBird method ("Big Bird", App. D; blog summary Sec. 4) packs each
+// query block's global, window and random key blocks into one dense product.
+// Here the same block lists drive a flash-style pipeline instead: no key
+// tensor is materialised and no score matrix leaves the SM.
+//
+// Work unit = one 128-row query tile of one (batch, head):
+//   * BigBird, b = 64: query blocks (2t, 2t+1); the unit walks the sorted
+//     union of their key-block lists, two 64-key blocks per 128-key step, and
+//     each 64-row half masks the blocks outside its own list.
+//   * BigBird, b = 128: query block t; one key block per step.
+//   * Tiles that contain a global query block (attends all n keys) are split
+//     into `splits` chunks of steps (split-KV); each chunk writes an fp32
+//     partial (m, l, O) and the last chunk to finish a row merges the
+//     partials of that row in chunk order (deterministic, no float atomics).
+//   * Longformer ("Longformer", Sec. 3.1), band unit: query rows
+//     [128t, 128t + 128); the unit walks the 64-key blocks that meet the
+//     band [128t - w/2, 128t + 127 + w/2], plus every other 64-key block that
+//     holds a global key. Each row masks keys outside its own window that are
+//     not global. Global rows of the tile are computed but not stored.
+//   * Longformer, global-row unit: up to 128 global query rows, gathered into
+//     the Q tile by the producer warp; they sweep all keys with split-KV as
+//     BigBird's global tiles do.
+// Roles (256 threads for one tile in flight, 384 for two): per tile, one warp
+// schedules units, builds the key-block lists and issues TMA loads (K and V
+// in separate rings: a K stage is free once its QK^T completed, a V stage
+// once its PV completed); one warp issues tcgen05 MMAs (lane 0); a warpgroup
+// runs the softmax (thread t owns query row t = TMEM lane t), the lazy O
+// rescale and the epilogue. The softmax writes P (bf16) over the first half
+// of its S buffer and the PV product reads A straight from TMEM. O is double
+// buffered in TMEM so a unit's epilogue runs while the next unit computes.
+// Every wait is bounded in time: on expiry the CTA records SA_ERR_TIMEOUT,
+// drains its in-flight copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <climits>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace sa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;           // query rows per tile = TMEM lanes
+constexpr int kBN = 128;           // keys per step = S tile columns
+constexpr int kNU = 4;             // unit-info ring depth
+constexpr int kSI = 6;             // step-info ring depth
+constexpr int kTargetChunkSteps = 64;
+constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (factor 256)
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzled region
+constexpr uint32_t kSuspendNs = 100000;  // try_wait suspend hint
+
+enum UnitKind { kUnitEnd = 0, kUnitDirect = 1, kUnitSplit = 2 };
+
+struct UnitInfo {
+    int kind, bh, q0, n_steps;
+    int tile_slot, chunk, nchunks, step0;  // split bookkeeping; first sweep step (-1: block list)
+    int j0, j1, pad0, pad1;                // BigBird query blocks of the halves (-1: none); pad0: list length
+    int pad[4];
+};
+static_assert(sizeof(UnitInfo) == 64, "UnitInfo layout");
+
+struct StepInfo {
+    int y[2];          // first key row of each 64-key sub-slot (n: empty, reads zeros)
+    uint32_t allow;    // bit (2*s + hf): sub-slot s is in query half hf's neighbourhood
+    uint32_t masked;   // nonzero: kmask holds per-key validity (key padding)
+    uint64_t kmask[2];
+};
+static_assert(sizeof(StepInfo) == 32, "StepInfo layout");
+
+template <int D>
+struct Cfg {
+    // Query tiles in flight per CTA: two independent pipelines for d = 64
+    // (one tile's softmax overlaps the other's waits and MMAs), one for d = 128.
+    static constexpr int NT = (D == 64) ? 2 : 1;
+    static constexpr int THREADS = 128 + 128 * NT;  // control warps + one softmax warpgroup per tile
+    static constexpr int NS = (NT == 2) ? 1 : 2;    // S buffers per tile; P is written over S
+    static constexpr int KST = 3, VST = 3, NQ = 1;  // K / V / Q stages per tile
+    static constexpr int TILE_BYTES = 128 * D * 2;  // Q tile / K step / V step
+    // per-tile big buffers (1024-B aligned), then per-tile small areas
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + NQ * TILE_BYTES;
+    static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
+    static constexpr int BIG = V_OFF + VST * TILE_BYTES;
+    // barrier slots within a tile's small area
+    static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
+                         B_IF = B_VE + VST, B_IE = B_IF + kSI, B_SF = B_IE + kSI, B_PF = B_SF + NS, B_PV = B_PF + NS,
+                         B_UF = B_PV + NS, B_UE = B_UF + kNU, B_DRAIN = B_UE + kNU, B_COUNT = B_DRAIN + 1;
+    static constexpr int BAR_OFF = 0;
+    static constexpr int UNIT_OFF = (B_COUNT * 8 + 15) & ~15;
+    static constexpr int STEP_OFF = UNIT_OFF + kNU * 64;
+    static constexpr int LIST_OFF = STEP_OFF + kSI * 32;  // two lists: the next unit is decoded early
+    static constexpr int SMALL = LIST_OFF + 2 * 32 * 4;
+    static constexpr int SMALL_OFF = NT * BIG;
+    static constexpr int MISC_OFF = SMALL_OFF + NT * SMALL;  // TMEM address, abort flag
+    static constexpr int SMEM_BYTES = MISC_OFF + 16;
+    static constexpr int ALLOC_BYTES = SMEM_BYTES + 1024;  // slack for 1024-B alignment
+    // TMEM: each tile owns TILE_COLS columns: NS S buffers of 128, then two O buffers of D
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TILE_COLS = TMEM_COLS / NT;
+    static constexpr uint32_t O_COL = NS * 128;
+
+    static_assert(O_COL + 2 * D <= TILE_COLS, "TMEM columns per tile");
+    static_assert(BIG % 1024 == 0, "tile buffers stay 1024-B aligned");
+};
+static_assert(Cfg<128>::ALLOC_BYTES <= 232448, "d=128 shared memory budget");
+static_assert(Cfg<64>::ALLOC_BYTES <= 232448, "d=64 shared memory budget");
+
+// Host-computed geometry of one call.
+struct Geometry {
+    int B, H, n, nb, b, g, w, r, half;
+    int tiles;            // query tiles per head
+    int gtiles;           // tiles holding a global query block
+    int splits;           // chunks per global tile
+    int steps_full;       // steps of a full key sweep
+    int steps_per_chunk;
+    int n_split_units;    // B*H*gtiles*splits
+    int total_units;
+    int ng;               // Longformer: entries of the global list
+    int nkb;              // Longformer: 64-key blocks, ceil(n / 64)
+    float scale_log2;
+    unsigned long long wait_ns;
+};
+
+struct Workspace {
+    unsigned *counters;   // [0] next unit, [1] finished CTAs
+    unsigned *row_cnt;    // [B*H*gtiles][128] arrivals per split row
+    float *part_o;        // [B*H*gtiles][splits][128][D]
+    float2 *part_ml;      // [B*H*gtiles][splits][128] (m, l)
+};
+
+struct Params {
+    Geometry geo;
+    Workspace ws;
+    const int32_t *rand_idx;
+    const uint8_t *key_mask;
+    // Longformer: the global list, and per 64-key block kb the bits of its
+    // global keys (gbits[kb]), the number of blocks before kb holding a
+    // global key (gpre[kb], gpre[nkb] = total) and those blocks in order
+    // (glist); all three written by longformer_prep before the main kernel.
+    const __nv_bfloat16 *Q;
+    const int32_t *gidx;
+    const unsigned long long *gbits;
+    const int *gpre;
+    const int *glist;
+    __nv_bfloat16 *O;
+    unsigned *status;
+};
+
+struct Ctl {
+    volatile int *abort;
+    unsigned *status;
+    unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Per-thread wait, bounded in time: returns false (and leaves) once the CTA
+// aborts. The first probe has no suspend hint (cheapest when the phase is
+// already complete); later probes sleep in the hardware until the phase
+// completes or the hint expires. No warp-collective operation inside, so
+// lanes of one warp may call it independently.
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Ctl &c) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = 0;
+    while (!try_wait_hint(bar, parity)) {
+        if (*c.abort) return false;
+        const unsigned long long now = global_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > c.limit_ns) {
+            *c.abort = 1;
+            atomicOr(c.status, kDevTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+// Warp-uniform wait: every lane probes the barrier itself (a divergent
+// single-lane wait costs hundreds of cycles to reconverge), then one vote
+// gives all lanes the same answer.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl &c) {
+    const bool ok = wait_one(bar, parity, c);
+    return __all_sync(kFull, ok);
+}
+// Drain wait used on the abort path (ignores the abort flag, still bounded).
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return;
+}
+
+// ---------------------------------------------------------------- producer helpers
+// Longformer global list entry t as a token position, or n when t is past the
+// list or the entry is out of [0, n) or not above its predecessor (such
+// entries are skipped everywhere and latch SA_ERR_BAD_INDEX in the prep pass).
+__device__ __forceinline__ int global_row(const int32_t *gidx, int ng, int n, int t) {
+    if (t >= ng) return n;
+    const int v = __ldg(gidx + t);
+    if (v < 0 || v >= n) return n;
+    if (t > 0 && __ldg(gidx + t - 1) >= v) return n;
+    return v;
+}
+
+// Bits [0, c) of a 64-bit word, c clamped to [0, 64].
+__device__ __forceinline__ uint64_t bits_below(int c) {
+    return c <= 0 ? 0ull : (c >= 64 ? ~0ull : ((1ull << c) - 1ull));
+}
+
+__device__ __forceinline__ int load_rand(const Params &p, const int32_t *row, int e, int nb) {
+    int v = row ? __ldg(row + e) : -1;
+    if (v == -1) return INT_MAX;
+    if (v < -1 || v >= nb) {
+        atomicOr(p.status, kDevBadIndex);
+        return INT_MAX;
+    }
+    return v;
+}
+
+// Is key block kb among the random blocks of `row` (warp-uniform answer)?
+__device__ __forceinline__ bool rand_has(const Params &p, const int32_t *row, int kb) {
+    bool hit = false;
+    if (row)
+        for (int e = threadIdx.x & 31; e < p.geo.r; e += 32) hit |= load_rand(p, row, e, p.geo.nb) == kb;
+    return __any_sync(kFull, hit);
+}
+
+// Does query block j (>= 0) see key block kb? `row`: j's random list.
+__device__ __forceinline__ bool block_allowed(const Params &p, const int32_t *row, int j, int kb) {
+    const Geometry &G = p.geo;
+    if (j < 0) return false;
+    if (j < G.g || kb < G.g) return true;
+    if (abs(kb - j) <= G.half) return true;
+    return rand_has(p, row, kb);
+}
+
+// Any valid key in block kb (per-lane check, 16-byte loads; key_mask is
+// 16-byte aligned and every block starts on a multiple of 64 bytes).
+__device__ __forceinline__ bool block_has_valid_lane(const uint8_t *km, int kb, int b) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(km + (size_t)kb * b);
+    uint32_t any = 0;
+    for (int i = 0; i < b / 16; ++i) {
+        const uint4 v = __ldg(src + i);
+        any |= v.x | v.y | v.z | v.w;
+    }
+    return any != 0;
+}
+
+// Any valid key in block kb (warp-uniform answer).
+__device__ __forceinline__ bool block_has_valid_warp(const uint8_t *km, int kb, int b) {
+    const int lane = threadIdx.x & 31;
+    bool any = false;
+    if (lane < b / 16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(km + (size_t)kb * b) + lane);
+        any = (v.x | v.y | v.z | v.w) != 0;
+    }
+    return __any_sync(kFull, any);
+}
+
+// 64-bit validity of keys [k0, k0 + 64) (warp-uniform).
+__device__ __forceinline__ uint64_t key_bits64(const uint8_t *km, int k0, int n) {
+    const int lane = threadIdx.x & 31;
+    const int a = k0 + lane, b = k0 + 32 + lane;
+    const unsigned lo = __ballot_sync(kFull, a < n && km[a] != 0);
+    const unsigned hi = __ballot_sync(kFull, b < n && km[b] != 0);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// Sorted, de-duplicated key-block list of a local tile, built by the whole
+// producer warp: each lane holds one candidate (global block, window block or
+// random block), duplicates and padded blocks drop out, and each survivor's
+// rank among the survivors is its position. list[pos] = block | allow bits
+// (bit 30: query block j0 sees it, bit 31: j1 sees it). Returns the number of
+// blocks, or -1 when the candidates do not fit in one warp.
+__device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1, const int32_t *r0,
+                                                const int32_t *r1, const uint8_t *km, uint32_t *list) {
+    const Geometry &G = p.geo;
+    const int lane = threadIdx.x & 31;
+    const int nglob = min(G.g, G.nb);
+    const int jl = j1 >= 0 ? j1 : j0;
+    const int wlo = max(max(0, j0 - G.half), nglob);
+    const int whi = min(G.nb - 1, jl + G.half);
+    const int wcount = max(0, whi - wlo + 1);
+    const int nr0 = r0 ? G.r : 0, nr1 = r1 ? G.r : 0;
+    const int total = nglob + wcount + nr0 + nr1;
+    if (total > 32) return -1;
+    int v = INT_MAX, src = 0;
+    if (lane < nglob) {
+        v = lane;
+        src = 1;
+    } else if (lane < nglob + wcount) {
+        v = wlo + (lane - nglob);
+        src = 2;
+    } else if (lane < nglob + wcount + nr0) {
+        v = load_rand(p, r0, lane - nglob - wcount, G.nb);
+        src = 3;
+    } else if (lane < total) {
+        v = load_rand(p, r1, lane - nglob - wcount - nr0, G.nb);
+        src = 4;
+    }
+    const unsigned same = __match_any_sync(kFull, v);
+    const bool in_r0 = (__ballot_sync(kFull, src == 3) & same) != 0;
+    const bool in_r1 = (__ballot_sync(kFull, src == 4) & same) != 0;
+    bool valid = v < G.nb && (same & ((1u << lane) - 1u)) == 0;  // first lane holding this block
+    if (valid && km) valid = block_has_valid_lane(km, v, G.b);
+    const bool a0 = valid && (j0 < G.g || v < G.g || abs(v - j0) <= G.half || in_r0);
+    const bool a1 = valid && j1 >= 0 && (j1 < G.g || v < G.g || abs(v - j1) <= G.half || in_r1);
+    const unsigned vm = __ballot_sync(kFull, valid);
+    int pos = 0;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) {
+        const int vj = __shfl_sync(kFull, v, j);
+        pos += ((vm >> j) & 1u) && vj < v;
+    }
+    if (valid) list[pos] = (uint32_t)v | (a0 ? (1u << 30) : 0u) | (a1 ? (1u << 31) : 0u);
+    __syncwarp();
+    return __popc(vm);
+}
+
+// Fallback for very wide patterns: smallest union block > x (warp-uniform).
+__device__ __forceinline__ int union_next_slow(const Params &p, const int32_t *r0, const int32_t *r1, int lo, int hi,
+                                               int x) {
+    const Geometry &G = p.geo;
+    int best = G.nb;
+    if (x + 1 < G.g) best = x + 1;
+    const int c = max(x + 1, lo);
+    if (c <= hi && c < best) best = c;
+    int cand = INT_MAX;
+    for (int e = threadIdx.x & 31; e < 2 * G.r; e += 32) {
+        const int v = e < G.r ? load_rand(p, r0, e, G.nb) : load_rand(p, r1, e - G.r, G.nb);
+        if (v > x && v < cand) cand = v;
+    }
+    cand = __reduce_min_sync(kFull, cand);
+    return cand < best ? cand : best;
+}
+
+struct UnitPtrs {
+    const uint8_t *km;
+    const int32_t *r0, *r1;
+    int wlo, whi;
+};
+// Key mask row, random lists of the tile's query blocks, and the merged window range.
+__device__ __forceinline__ UnitPtrs unit_ptrs(const Params &p, const UnitInfo &ui) {
+    const Geometry &G = p.geo;
+    UnitPtrs u;
+    const int beta = ui.bh / G.H, h = ui.bh - beta * G.H;
+    u.km = p.key_mask ? p.key_mask + (size_t)beta * G.n : nullptr;
+    u.r0 = (p.rand_idx && G.r > 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j0) * G.r : nullptr;
+    u.r1 = (p.rand_idx && G.r > 0 && ui.j1 >= 0) ? p.rand_idx + ((size_t)h * G.nb + ui.j1) * G.r : nullptr;
+    const int jl = ui.j1 >= 0 ? ui.j1 : ui.j0;
+    u.wlo = max(0, ui.j0 - G.half);
+    u.whi = min(G.nb - 1, jl + G.half);
+    return u;
+}
+
+// ---------------------------------------------------------------- kernel
+// PADDED: a key mask is present. The unpadded BigBird instantiation carries
+// no per-key or per-row masking code at all (rows past n are never stored).
+// LF: Longformer units (band and global-row) instead of BigBird units.
+template <int D, bool PADDED, bool LF>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+    sparse_tc_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using C = Cfg<D>;
+    static_assert(kSI * 2 * 8 <= 2 * 32 * 4, "Longformer global-key masks fit the list area");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
+
+    const Geometry &G = p.geo;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const Ctl ctl{abort_flag, p.status, G.wait_ns};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int x = 0; x < C::NT; ++x) {
+            const uint32_t bb = sbase + C::SMALL_OFF + x * C::SMALL + C::BAR_OFF;
+            auto bar = [&](int i) { return bb + 8u * (uint32_t)i; };
+            mbar_init(bar(C::B_QF), 1);
+            mbar_init(bar(C::B_QE), 1);
+            for (int i = 0; i < C::KST; ++i) {
+                mbar_init(bar(C::B_KF + i), 1);
+                mbar_init(bar(C::B_KE + i), 1);
+            }
+            for (int i = 0; i < C::VST; ++i) {
+                mbar_init(bar(C::B_VF + i), 1);
+                mbar_init(bar(C::B_VE + i), 1);
+            }
+            for (int i = 0; i < kSI; ++i) {
+                mbar_init(bar(C::B_IF + i), 1);
+                mbar_init(bar(C::B_IE + i), 4);  // one arrival per softmax warp
+            }
+            for (int i = 0; i < C::NS; ++i) {
+                mbar_init(bar(C::B_SF + i), 1);
+                mbar_init(bar(C::B_PF + i), 128);
+                mbar_init(bar(C::B_PV + i), 1);
+            }
+            for (int i = 0; i < kNU; ++i) {
+                mbar_init(bar(C::B_UF + i), 1);
+                mbar_init(bar(C::B_UE + i), 1 + 128);
+            }
+            mbar_init(bar(C::B_DRAIN), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // Role and tile of this warp: warps 2x and 2x+1 are tile x's producer and
+    // MMA issuer; warps 4 + 4x .. 7 + 4x its softmax warpgroup.
+    int role = -1, x = 0;  // 0 producer, 1 MMA, 2 softmax
+    if (warp < 4) {
+        if ((warp >> 1) < C::NT) {
+            role = warp & 1;
+            x = warp >> 1;
+        }
+    } else {
+        role = 2;
+        x = (warp - 4) >> 2;
+    }
+    const uint32_t tbase = sbase + x * C::BIG;  // this tile's Q/K/V buffers
+    uint8_t *small = smem + C::SMALL_OFF + x * C::SMALL;
+    const uint32_t bars = sbase + C::SMALL_OFF + x * C::SMALL + C::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    UnitInfo *ring = reinterpret_cast<UnitInfo *>(small + C::UNIT_OFF);
+    StepInfo *steps = reinterpret_cast<StepInfo *>(small + C::STEP_OFF);
+    uint32_t *list = reinterpret_cast<uint32_t *>(small + C::LIST_OFF);
+    const uint32_t tmem = *tmem_holder + x * C::TILE_COLS;  // this tile's TMEM columns
+
+    if (role == 0) {
+        // ================================================================ producer (tile x)
+        // Units are decoded (and their key/value blocks prefetched into L2)
+        // one unit ahead of the TMA loads that consume them.
+        uint32_t g = 0, qcnt = 0;
+        uint32_t k_arms[C::KST] = {}, v_arms[C::VST] = {};
+        bool q_tma_last = false;  // the latest Q fill was a TMA copy (drained on abort)
+        uint64_t *gmk = reinterpret_cast<uint64_t *>(list);  // Longformer: global-key bits per step
+        bool ok = true;
+        unsigned u_next = 0;
+        if (lane == 0) u_next = atomicAdd(p.ws.counters, 1u);
+        // decode the next unit from the work counter into ring slot `slot`
+        // and list buffer `lb`; returns its info (kind kUnitEnd when done)
+        auto decode_next = [&](uint32_t ui_idx, uint32_t *lbuf, bool &slow_out) -> UnitInfo {
+            UnitInfo ui = {};
+            slow_out = false;
+            int u = (int)__shfl_sync(kFull, u_next, 0);
+            if (lane == 0 && u < G.total_units) u_next = atomicAdd(p.ws.counters, 1u);  // prefetch the next
+            const uint32_t slot = ui_idx % kNU;
+            if (ui_idx >= kNU && !(ok = wait_warp(bar(C::B_UE + slot), ((ui_idx / kNU) - 1) & 1, ctl))) {
+                ui.kind = kUnitEnd;
+                return ui;
+            }
+            if (u >= G.total_units) {
+                ui.kind = kUnitEnd;
+                if (lane == 0) {
+                    ring[slot] = ui;
+                    mbar_arrive(bar(C::B_UF + slot));
+                }
+                return ui;
+            }
+            int tile;
+            if (u < G.n_split_units) {
+                const int per = G.gtiles * G.splits;
+                ui.bh = u / per;
+                const int rem = u - ui.bh * per;
+                tile = rem / G.splits;
+                ui.chunk = rem - tile * G.splits;
+                ui.nchunks = G.splits;
+                ui.tile_slot = ui.bh * G.gtiles + tile;
+                ui.kind = G.splits > 1 ? kUnitSplit : kUnitDirect;
+                ui.step0 = ui.chunk * G.steps_per_chunk;
+                ui.n_steps = max(0, min(G.steps_per_chunk, G.steps_full - ui.step0));
+            } else {
+                const int t0 = LF ? 0 : G.gtiles;  // Longformer: every tile has a band unit
+                const int per = G.tiles - t0;
+                const int v = u - G.n_split_units;
+                ui.bh = v / per;
+                tile = t0 + (v - ui.bh * per);
+                ui.kind = kUnitDirect;
+                ui.step0 = -1;
+            }
+            ui.q0 = tile * kBM;  // Longformer global-row unit: first entry of the global list
+            if constexpr (LF) {
+                ui.j0 = ui.j1 = -1;
+                if (ui.step0 < 0) {
+                    // band unit: 64-key blocks [blo, bhi] meet the band of rows
+                    // [q0, q0 + 128); global-key blocks outside it come from
+                    // glist[0, pad0) (before) and glist[pad1, ...) (after)
+                    bool any_row = true;
+                    if (PADDED) {
+                        const uint8_t *km = p.key_mask + (size_t)(ui.bh / G.H) * G.n;
+                        bool a = false;
+                        for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && km[ui.q0 + t] != 0;
+                        any_row = __any_sync(kFull, a);
+                    }
+                    const int blo = max(0, ui.q0 - G.half) >> 6;
+                    const int bhi = min(G.n - 1, ui.q0 + kBM - 1 + G.half) >> 6;
+                    int before = 0, after0 = 0, after = 0;
+                    if (G.ng > 0) {
+                        before = __ldg(p.gpre + blo);
+                        after0 = __ldg(p.gpre + bhi + 1);
+                        after = __ldg(p.gpre + G.nkb) - after0;
+                    }
+                    ui.j0 = blo;
+                    ui.j1 = bhi;
+                    ui.pad0 = before;
+                    ui.pad1 = after0;
+                    ui.pad[0] = before + (bhi - blo + 1) + after;
+                    if (before < 0 || after < 0 || ui.pad[0] > G.nkb) {  // prep tables out of step
+                        if (lane == 0) atomicOr(p.status, kDevBadIndex);
+                        ui.pad0 = ui.pad1 = 0;
+                        ui.pad[0] = bhi - blo + 1;
+                    }
+                    ui.n_steps = any_row ? (ui.pad[0] + 1) / 2 : 0;
+                }
+                if (lane == 0) {
+                    ring[slot] = ui;
+                    mbar_arrive(bar(C::B_UF + slot));
+                }
+                return ui;
+            }
+            if (G.b == 64) {
+                ui.j0 = 2 * tile;
+                ui.j1 = (2 * tile + 1 < G.nb) ? 2 * tile + 1 : -1;
+            } else {
+                ui.j0 = tile;
+                ui.j1 = -1;
+            }
+            const UnitPtrs up = unit_ptrs(p, ui);
+            const int bps = (G.b == 64) ? 2 : 1;  // key blocks per step
+            if (ui.step0 < 0) {
+                bool any_row = true;
+                if (up.km) {
+                    bool a = false;
+                    for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && up.km[ui.q0 + t] != 0;
+                    any_row = __any_sync(kFull, a);
+                }
+                int nlist = 0;
+                if (any_row) {
+                    nlist = build_local_list(p, ui.j0, ui.j1, up.r0, up.r1, up.km, lbuf);
+                    if (nlist < 0) {  // wide pattern: the union is generated block by block later
+                        slow_out = true;
+                        nlist = 0;
+                        for (int xb = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, -1); xb < G.nb;
+                             xb = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, xb))
+                            if (!up.km || block_has_valid_warp(up.km, xb, G.b)) ++nlist;
+                    }
+                }
+                ui.pad0 = nlist;
+                ui.n_steps = (nlist + bps - 1) / bps;
+            }
+
+            if (lane == 0) {
+                ring[slot] = ui;
+                mbar_arrive(bar(C::B_UF + slot));
+            }
+            return ui;
+        };
+
+        bool slow_cur = false, slow_nxt = false;
+        UnitInfo cur = decode_next(0, list, slow_cur);
+        for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
+            uint32_t *lcur = list + (ui_idx & 1) * 32;
+            const UnitInfo nxt = decode_next(ui_idx + 1, list + ((ui_idx + 1) & 1) * 32, slow_nxt);
+            if (!ok) break;
+            if (cur.n_steps > 0) {
+                const UnitPtrs up = unit_ptrs(p, cur);
+                const int nlist = cur.pad0;
+                // ---- Q tile
+                if (qcnt >= 1 && !(ok = wait_warp(bar(C::B_QE), (qcnt - 1) & 1, ctl))) break;
+                if (LF && cur.step0 >= 0) {
+                    // Longformer global rows: gather them with plain loads into
+                    // the 128-B swizzled K-major layout the TMA would produce
+                    // (16-B chunk c of row r lands at chunk c ^ (r & 7)).
+                    constexpr int CPR = D / 8;  // 16-B chunks per row
+                    int pr[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) pr[k] = global_row(p.gidx, G.ng, G.n, cur.q0 + lane + 32 * k);
+                    const uint4 *qh = reinterpret_cast<const uint4 *>(p.Q + (size_t)cur.bh * G.n * D);
+                    uint8_t *qs = smem + x * C::BIG + C::Q_OFF;
+#pragma unroll 8
+                    for (int it = 0; it < kBM * CPR / 32; ++it) {
+                        const int idx = it * 32 + lane;
+                        const int r = idx / CPR, cq = idx % CPR;
+                        const int grp = r >> 5;  // warp-uniform
+                        const int src = grp == 0 ? pr[0] : grp == 1 ? pr[1] : grp == 2 ? pr[2] : pr[3];
+                        const int pos = __shfl_sync(kFull, src, r & 31);
+                        const uint4 v = pos < G.n ? __ldg(qh + (size_t)pos * CPR + cq) : make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(qs + (cq >> 3) * kRegionBytes + r * 128 +
+                                                   (((cq & 7) ^ (r & 7)) << 4)) = v;
+                    }
+                    fence_proxy_async_smem();  // generic-proxy writes -> tcgen05 operand reads
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_QF));
+                    q_tma_last = false;
+                } else {
+                    if (lane == 0) {
+                        const uint32_t dst = tbase + C::Q_OFF;
+                        mbar_arrive_expect_tx(bar(C::B_QF), C::TILE_BYTES);
+                        for (int dc = 0; dc < D / 64; ++dc)
+                            for (int rh = 0; rh < 2; ++rh)
+                                tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF), dc * 64,
+                                            cur.q0 + rh * 64, cur.bh);
+                    }
+                    q_tma_last = true;
+                }
+                ++qcnt;
+                // ---- key steps
+                int xs = -1;  // wide patterns: last block emitted
+                for (int t = 0; t < cur.n_steps; ++t, ++g) {
+                    StepInfo si;
+                    si.masked = up.km ? 1u : 0u;
+                    si.allow = 0;
+                    si.kmask[0] = si.kmask[1] = ~0ull;
+                    uint64_t gm2[2] = {~0ull, ~0ull};
+                    if constexpr (LF) {
+                        // sub-slot s of step t is entry 2t + s of: global-key blocks
+                        // before the band, the band blocks, global-key blocks after;
+                        // a global-row unit sweeps every block.
+                        // kmask: valid keys; gm2: global keys; masked bit s: band block
+                        si.masked = 0;
+                        const int nband = cur.j1 - cur.j0 + 1;
+#pragma unroll
+                        for (int s = 0; s < 2; ++s) {
+                            const int li = 2 * t + s;
+                            int kb = -1;
+                            bool band = false;
+                            if (cur.step0 >= 0) {
+                                kb = 2 * (cur.step0 + t) + s;
+                                if (kb >= G.nkb) kb = -1;
+                            } else if (li < cur.pad0) {
+                                kb = __ldg(p.glist + li);
+                            } else if (li < cur.pad0 + nband) {
+                                kb = cur.j0 + (li - cur.pad0);
+                                band = true;
+                            } else if (li < cur.pad[0]) {
+                                kb = __ldg(p.glist + cur.pad1 + (li - cur.pad0 - nband));
+                            }
+                            if (kb >= G.nkb) {  // prep tables out of step with this call
+                                if (lane == 0) atomicOr(p.status, kDevBadIndex);
+                                kb = -1;
+                            }
+                            const int y = kb >= 0 ? kb * 64 : G.n;
+                            uint64_t kv = 0ull, gm = 0ull;
+                            if (kb >= 0) {
+                                kv = PADDED ? key_bits64(up.km, y, G.n) : bits_below(G.n - y);
+                                gm = cur.step0 >= 0 ? ~0ull : (G.ng > 0 ? __ldg(p.gbits + kb) : 0ull);
+                            }
+                            si.y[s] = y;
+                            si.kmask[s] = kv;
+                            gm2[s] = gm;
+                            if (kv & (band ? ~0ull : gm)) si.allow |= 3u << (2 * s);
+                            if (band) si.masked |= 1u << s;
+                        }
+                    } else {
+#pragma unroll
+                    for (int s = 0; s < 2; ++s) {
+                        int kb = -1, y = G.n;
+                        bool a0 = false, a1 = false;
+                        if (cur.step0 >= 0) {  // full sweep of a global tile
+                            if (G.b == 64) {
+                                kb = 2 * (cur.step0 + t) + s;
+                                if (kb >= G.nb) kb = -1;
+                                y = kb >= 0 ? kb * 64 : G.n;
+                            } else {
+                                kb = cur.step0 + t;
+                                y = kb * 128 + s * 64;
+                            }
+                            if (kb >= 0) {
+                                a0 = block_allowed(p, up.r0, cur.j0, kb);
+                                a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
+                            }
+                        } else if (!slow_cur) {
+                            const int li = (G.b == 64) ? 2 * t + s : t;
+                            if (li < nlist) {
+                                const uint32_t e = lcur[li];
+                                kb = (int)(e & 0x3FFFFFFFu);
+                                a0 = (e >> 30) & 1u;
+                                a1 = (G.b == 64) ? ((e >> 31) & 1u) : a0;
+                                y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                            }
+                        } else {
+                            if (G.b == 64 || s == 0) {
+                                do {
+                                    xs = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, xs);
+                                } while (xs < G.nb && up.km && !block_has_valid_warp(up.km, xs, G.b));
+                            }
+                            if (xs < G.nb) {
+                                kb = xs;
+                                a0 = block_allowed(p, up.r0, cur.j0, kb);
+                                a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
+                                y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                            }
+                        }
+                        si.y[s] = y;
+                        if (kb < 0) continue;
+                        if (up.km) {
+                            const uint64_t bits = key_bits64(up.km, y, G.n);
+                            si.kmask[s] = bits;
+                            if (bits == 0) continue;
+                        }
+                        si.allow |= (a0 ? 1u : 0u) << (2 * s);
+                        si.allow |= (a1 ? 1u : 0u) << (2 * s + 1);
+                    }
+                    }
+                    // step info -> softmax
+                    const uint32_t ii = g % kSI;
+                    if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
+                    if (lane == 0) {
+                        steps[ii] = si;
+                        if (LF) {
+                            gmk[2 * ii] = gm2[0];
+                            gmk[2 * ii + 1] = gm2[1];
+                        }
+                        mbar_arrive(bar(C::B_IF + ii));
+                    }
+                    // K
+                    const uint32_t sk = g % C::KST;
+                    if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
+                    if (lane == 0) {
+                        const uint32_t kdst = tbase + C::K_OFF + sk * C::TILE_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::TILE_BYTES);
+                        for (int s = 0; s < 2; ++s)
+                            for (int dc = 0; dc < D / 64; ++dc)
+                                tma_load_3d(kdst + dc * kRegionBytes + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
+                                            si.y[s], cur.bh);
+                    }
+                    ++k_arms[sk];
+                    // V
+                    const uint32_t sv = g % C::VST;
+                    if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
+                    if (lane == 0) {
+                        const uint32_t vdst = tbase + C::V_OFF + sv * C::TILE_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::TILE_BYTES);
+                        for (int s = 0; s < 2; ++s)
+                            for (int dc = 0; dc < D / 64; ++dc)
+                                tma_load_3d(vdst + dc * kRegionBytes + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
+                                            si.y[s], cur.bh);
+                    }
+                    ++v_arms[sv];
+                }
+            }
+            cur = nxt;
+            slow_cur = slow_nxt;
+        }
+        if (!ok && lane == 0) {  // abort: wait for the copies this tile still has in flight
+            for (int i = 0; i < C::KST; ++i)
+                if (k_arms[i]) wait_drain(bar(C::B_KF + i), (k_arms[i] - 1) & 1, G.wait_ns);
+            for (int i = 0; i < C::VST; ++i)
+                if (v_arms[i]) wait_drain(bar(C::B_VF + i), (v_arms[i] - 1) & 1, G.wait_ns);
+            if (qcnt && q_tma_last) wait_drain(bar(C::B_QF), (qcnt - 1) & 1, G.wait_ns);
+        }
+    } else if (role == 1) {
+        // ================================================================ MMA issuer (tile x)
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(128, kBN, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
+            uint32_t g = 0, qcnt = 0;
+            int pend = -1;
+            bool pend_first = false;
+            uint32_t pend_ob = 0;
+            bool ok = true;
+            // O_ob (+)= P_h V_h; P_h is read from TMEM over S buffer h % NS
+            auto issue_pv = [&](uint32_t h, bool first, uint32_t ob) -> bool {
+                const uint32_t sv = h % C::VST, sb = h % C::NS;
+                if (!wait_one(bar(C::B_PF + sb), (h / C::NS) & 1, ctl)) return false;
+                if (!wait_one(bar(C::B_VF + sv), (h / C::VST) & 1, ctl)) return false;
+                tc_fence_after();
+                const uint32_t pt = tmem + sb * kBN;
+                const uint32_t va = tbase + C::V_OFF + sv * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t b = desc_sw128(va + kk * 2048, kRegionBytes);
+                    mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(bar(C::B_VE + sv));
+                mma_commit(bar(C::B_PV + sb));
+                return true;
+            };
+            for (uint32_t ui_idx = 0; ok; ++ui_idx) {
+                const uint32_t slot = ui_idx % kNU;
+                if (!(ok = wait_one(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
+                const int kind = ring[slot].kind;
+                const int n_steps = ring[slot].n_steps;
+                mbar_arrive(bar(C::B_UE + slot));
+                if (kind == kUnitEnd) break;
+                if (n_steps == 0) continue;
+                const uint32_t ob = qcnt & 1;
+                if (!(ok = wait_one(bar(C::B_QF), qcnt & 1, ctl))) break;
+                tc_fence_after();
+                const uint32_t qa = tbase + C::Q_OFF;
+                for (int t = 0; t < n_steps; ++t, ++g) {
+                    const uint32_t sk = g % C::KST, sb = g % C::NS;
+                    if (!(ok = wait_one(bar(C::B_KF + sk), (g / C::KST) & 1, ctl))) break;
+                    tc_fence_after();
+                    const uint32_t ka = tbase + C::K_OFF + sk * C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kRegionBytes + (kk & 3) * 32;
+                        mma_bf16_ss(tmem + sb * kBN, desc_sw128(qa + off, 16), desc_sw128(ka + off, 16), idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(C::B_KE + sk));
+                    mma_commit(bar(C::B_SF + sb));
+                    if (t == n_steps - 1) mma_commit(bar(C::B_QE));
+                    if (C::NS == 1) {
+                        // one S buffer: P_g overwrites S_g, so PV_g precedes S_{g+1}
+                        if (!(ok = issue_pv(g, t == 0, ob))) break;
+                    } else {
+                        // two S buffers: S_{g} overlaps the softmax of step g-1
+                        if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
+                        pend = (int)g;
+                        pend_first = (t == 0);
+                        pend_ob = ob;
+                    }
+                }
+                ++qcnt;
+            }
+            if (ok && pend >= 0) issue_pv((uint32_t)pend, pend_first, pend_ob);
+            // drain: every MMA issued by this thread has completed once this arrives
+            mma_commit(bar(C::B_DRAIN));
+            wait_drain(bar(C::B_DRAIN), 0, G.wait_ns);
+        }
+    } else if (role == 2) {
+        // ================================================================ softmax / epilogue (tile x)
+        const int tid = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int hf = (!LF && G.b == 64) ? (tid >> 6) : 0;
+        const uint64_t *gmk = reinterpret_cast<const uint64_t *>(list);  // Longformer: global-key bits per step
+        const float sl2 = G.scale_log2;
+
+        // State of the unit whose epilogue is deferred until the next unit's
+        // first step has been handed to the MMA warp.
+        struct Pend {
+            int kind, bh, row, tile_slot, chunk, nchunks, have;  // row: output row of this thread (n: none)
+            bool row_valid;
+            float m, l;
+            uint32_t ob, g_last;
+        };
+        Pend pe;
+        pe.kind = kUnitEnd;
+
+        // `wait_pv` false: the caller already saw PV of step g_last complete.
+        auto epilogue = [&](const Pend &e, bool wait_pv) -> bool {
+            const int row = e.row;
+            const uint32_t oaddr = tmem + lane_base + C::O_COL + e.ob * D;
+            if (e.have) {
+                if (wait_pv &&
+                    !wait_warp(bar(C::B_PV + (e.g_last % C::NS)), (e.g_last / C::NS) & 1, ctl))
+                    return false;
+                tc_fence_after();
+            }
+            if (e.kind == kUnitDirect) {
+                const float inv = (e.row_valid && e.l > 0.f) ? 1.f / e.l : 0.f;
+                __nv_bfloat16 *orow = p.O + ((size_t)e.bh * G.n + (row < G.n ? row : 0)) * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float o[32];
+                    if (e.have) {
+                        tmem_ld32(oaddr + cc * 32, o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                    }
+                    if (row < G.n) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                __nv_bfloat162 b2 =
+                                    __floats2bfloat162_rn(o[q * 8 + 2 * k] * inv, o[q * 8 + 2 * k + 1] * inv);
+                                w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                            *reinterpret_cast<uint4 *>(orow + cc * 32 + q * 8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                }
+                return true;
+            }
+            // split chunk: publish this row's partial; the last arrival merges the row
+            const size_t prow = ((size_t)e.tile_slot * G.splits + e.chunk) * kBM + tid;
+            float *po = p.ws.part_o + prow * D;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float o[32];
+                if (e.have) {
+                    tmem_ld32(oaddr + cc * 32, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    __stcg(reinterpret_cast<float4 *>(po + cc * 32 + q * 4),
+                           make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]));
+            }
+            __stcg(p.ws.part_ml + prow, make_float2(e.row_valid ? e.m : -CUDART_INF_F, e.row_valid ? e.l : 0.f));
+            __threadfence();
+            unsigned *cnt = p.ws.row_cnt + (size_t)e.tile_slot * kBM + tid;
+            const unsigned prev = atomicAdd(cnt, 1u);
+            if (prev != (unsigned)(e.nchunks - 1)) return true;
+            __threadfence();
+            float M = -CUDART_INF_F;
+            for (int c = 0; c < e.nchunks; ++c) {
+                const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
+                M = fmaxf(M, ml.x);
+            }
+            float L = 0.f;
+            for (int c = 0; c < e.nchunks; ++c) {
+                const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
+                if (ml.y > 0.f) L += ex2(ml.x - M) * ml.y;
+            }
+            const float inv = (e.row_valid && L > 0.f) ? 1.f / L : 0.f;
+            // merge 32 columns at a time, chunks in fixed order
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float acc[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                for (int c = 0; c < e.nchunks; ++c) {
+                    const float2 ml = __ldcg(p.ws.part_ml + ((size_t)e.tile_slot * G.splits + c) * kBM + tid);
+                    if (!(ml.y > 0.f)) continue;
+                    const float wk = ex2(ml.x - M);
+                    const float *src = p.ws.part_o + (((size_t)e.tile_slot * G.splits + c) * kBM + tid) * D + cc * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
+                        acc[i] = fmaf(wk, v.x, acc[i]);
+                        acc[i + 1] = fmaf(wk, v.y, acc[i + 1]);
+                        acc[i + 2] = fmaf(wk, v.z, acc[i + 2]);
+                        acc[i + 3] = fmaf(wk, v.w, acc[i + 3]);
+                    }
+                }
+                if (row < G.n) {
+                    __nv_bfloat16 *orow = p.O + ((size_t)e.bh * G.n + row) * D + cc * 32;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[i + 2 * k] * inv, acc[i + 2 * k + 1] * inv);
+                            w4[k] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(orow + i) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+            }
+            atomicExch(cnt, 0u);  // ready for the next call
+            return true;
+        };
+
+        uint32_t g = 0, qcnt = 0;
+        bool ok = true;
+        for (uint32_t ui_idx = 0; ok; ++ui_idx) {
+            const uint32_t slot = ui_idx % kNU;
+            if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
+            const UnitInfo ui = ring[slot];
+            mbar_arrive(bar(C::B_UE + slot));
+            if (ui.kind == kUnitEnd) break;
+            const int beta = ui.bh / G.H;
+            // qpos: the query token of this thread's row; srow: where it is stored
+            int qpos = ui.q0 + tid, srow = qpos;
+            if constexpr (LF) {
+                if (ui.step0 >= 0) {
+                    qpos = srow = global_row(p.gidx, G.ng, G.n, ui.q0 + tid);
+                } else if (qpos < G.n && G.ng > 0 && ((__ldg(p.gbits + (qpos >> 6)) >> (qpos & 63)) & 1ull)) {
+                    srow = G.n;  // a global row: its global-row unit stores it
+                }
+            }
+            const bool row_valid = qpos < G.n && (!PADDED || p.key_mask[(size_t)beta * G.n + qpos] != 0);
+            Pend cur;
+            cur.kind = ui.kind;
+            cur.bh = ui.bh;
+            cur.row = srow;
+            cur.tile_slot = ui.tile_slot;
+            cur.chunk = ui.chunk;
+            cur.nchunks = ui.nchunks;
+            cur.have = ui.n_steps > 0;
+            cur.row_valid = row_valid;
+            cur.ob = qcnt & 1;
+            if (ui.n_steps == 0) {
+                if (pe.kind != kUnitEnd && !(ok = epilogue(pe, true))) break;
+                pe.kind = kUnitEnd;
+                cur.m = -CUDART_INF_F;
+                cur.l = 0.f;
+                cur.g_last = 0;
+                if (!(ok = epilogue(cur, true))) break;
+                continue;
+            }
+            ++qcnt;
+            float m_ref = -CUDART_INF_F, l = 0.f;
+            const uint32_t obase = tmem + lane_base + C::O_COL + cur.ob * D;
+            for (int t = 0; t < ui.n_steps; ++t, ++g) {
+                const uint32_t ii = g % kSI, sb = g % C::NS;
+                if (!(ok = wait_warp(bar(C::B_IF + ii), (g / kSI) & 1, ctl))) break;
+                const uint32_t allow = steps[ii].allow;
+                uint64_t km0 = ~0ull, km1 = ~0ull, gm0 = 0ull, gm1 = 0ull;
+                int y0 = 0, y1 = 0;
+                uint32_t bandb = 0;
+                if (PADDED || LF) {
+                    km0 = steps[ii].kmask[0];
+                    km1 = steps[ii].kmask[1];
+                }
+                if (LF) {
+                    gm0 = gmk[2 * ii];
+                    gm1 = gmk[2 * ii + 1];
+                    y0 = steps[ii].y[0];
+                    y1 = steps[ii].y[1];
+                    bandb = steps[ii].masked;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_IE + ii));
+                if (!(ok = wait_warp(bar(C::B_SF + sb), (g / C::NS) & 1, ctl))) break;
+                tc_fence_after();
+                // The buffer holding S_g receives P_g; PV of step g - NS must have
+                // read the previous P there (completes before S_g in issue order;
+                // the wait also establishes that PV_{g-1} completed when NS == 1).
+                if (g >= (uint32_t)C::NS &&
+                    !(ok = wait_warp(bar(C::B_PV + sb), ((g - C::NS) / C::NS) & 1, ctl)))
+                    break;
+                const uint32_t sa = tmem + lane_base + sb * kBN;
+                // Stream the two 64-key halves: each is loaded, reduced and
+                // exponentiated against the running reference m_ref, then
+                // written back as bf16 P over the first 64 columns of S_g.
+                float alpha = 1.f;
+                bool resc = false;  // O needs a rescale by alpha
+                float lsum = 0.f;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    const bool w_ok = (allow >> (2 * half + hf)) & 1u;  // warp-uniform
+                    uint32_t pk[32];
+                    if (w_ok) {
+                        float s0[32], s1[32];
+                        tmem_ld32(sa + half * 64, s0);
+                        tmem_ld32(sa + half * 64 + 32, s1);
+                        tmem_wait_ld();
+                        if constexpr (LF) {
+                            // valid key and (global key, or inside this row's window
+                            // [qpos - w/2, qpos + w/2] on a band block); else -inf
+                            uint64_t kmh = 0ull;
+                            if (row_valid) {
+                                const int yh = half ? y1 : y0;
+                                const uint64_t bandm = ((bandb >> half) & 1u)
+                                                           ? bits_below(qpos + G.half - yh + 1) &
+                                                                 ~bits_below(qpos - G.half - yh)
+                                                           : 0ull;
+                                kmh = (half ? km1 : km0) & ((half ? gm1 : gm0) | bandm);
+                            }
+                            if (!__all_sync(kFull, kmh == ~0ull)) {
+                                const uint32_t lo = (uint32_t)kmh, hi = (uint32_t)(kmh >> 32);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    s0[i] = ((lo >> i) & 1u) ? s0[i] : -CUDART_INF_F;
+                                    s1[i] = ((hi >> i) & 1u) ? s1[i] : -CUDART_INF_F;
+                                }
+                            }
+                        } else if (PADDED) {
+                            // padded row: nothing allowed; padded keys: -inf
+                            const uint64_t kmh = row_valid ? (half ? km1 : km0) : 0ull;
+                            const uint32_t lo = (uint32_t)kmh, hi = (uint32_t)(kmh >> 32);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                s0[i] = ((lo >> i) & 1u) ? s0[i] : -CUDART_INF_F;
+                                s1[i] = ((hi >> i) & 1u) ? s1[i] : -CUDART_INF_F;
+                            }
+                        }
+                        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            mx0 = fmaxf(mx0, s0[i]);
+                            mx1 = fmaxf(mx1, s0[i + 1]);
+                            mx2 = fmaxf(mx2, s1[i]);
+                            mx3 = fmaxf(mx3, s1[i + 1]);
+                        }
+                        const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                        float fix = 1.f;  // factor for this row's first-half P (second half only)
+                        if (m_new > m_ref + kRescaleLog2) {
+                            const float a = ex2(m_ref - m_new);  // 0 when m_ref was -inf
+                            if (m_ref != -CUDART_INF_F) {
+                                if (t > 0) resc = true;
+                                alpha *= a;
+                                fix = a;
+                            }
+                            l *= a;
+                            lsum *= a;
+                            m_ref = m_new;
+                        }
+                        // The first half's P already used the old reference. tcgen05.ld/st
+                        // are warp-collective (.sync.aligned): the whole warp takes the
+                        // round trip when any row needs it, each row scaling by its own
+                        // factor (1 leaves a bf16 value unchanged).
+                        if (half == 1 && ((allow >> hf) & 1u) && __any_sync(kFull, fix != 1.f)) {
+                            uint32_t q[32];
+                            tmem_ld32u(sa, q);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&q[i]);
+                                float2 f = __bfloat1622float2(b2);
+                                b2 = __floats2bfloat162_rn(f.x * fix, f.y * fix);
+                                q[i] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                            tmem_st32u(sa, q);
+                        }
+                        const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
+                        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const float p0 = ex2(fmaf(s0[i], sl2, neg_m));
+                            const float p1 = ex2(fmaf(s0[i + 1], sl2, neg_m));
+                            const float p2 = ex2(fmaf(s1[i], sl2, neg_m));
+                            const float p3 = ex2(fmaf(s1[i + 1], sl2, neg_m));
+                            ls0 += p0;
+                            ls1 += p1;
+                            ls2 += p2;
+                            ls3 += p3;
+                            __nv_bfloat162 b01 = __floats2bfloat162_rn(p0, p1);
+                            __nv_bfloat162 b23 = __floats2bfloat162_rn(p2, p3);
+                            pk[i >> 1] = *reinterpret_cast<uint32_t *>(&b01);
+                            pk[16 + (i >> 1)] = *reinterpret_cast<uint32_t *>(&b23);
+                        }
+                        lsum += (ls0 + ls1) + (ls2 + ls3);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+                    }
+                    tmem_st32u(sa + half * 32, pk);
+                }
+                l += lsum;
+                tmem_wait_st();
+                if (__any_sync(kFull, resc)) {
+                    // O must hold PV of step g-1 before it is rescaled
+                    const uint32_t h = g - 1;
+                    if (!(ok = wait_warp(bar(C::B_PV + (h % C::NS)), (h / C::NS) & 1, ctl))) break;
+                    tc_fence_after();
+                    const float a = resc ? alpha : 1.f;
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        float o[32];
+                        tmem_ld32(obase + cc * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= a;
+                        tmem_st32(obase + cc * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(bar(C::B_PF + sb));
+                if (t == 0 && pe.kind != kUnitEnd) {  // previous unit's epilogue, now off the critical path
+                    // NS == 1: the P-buffer wait above already saw PV of step g-1 complete
+                    if (!(ok = epilogue(pe, C::NS != 1))) break;
+                    pe.kind = kUnitEnd;
+                }
+            }
+            if (!ok) break;
+            cur.m = m_ref;
+            cur.l = l;
+            cur.g_last = g - 1;
+            pe = cur;
+        }
+        if (ok && pe.kind != kUnitEnd) epilogue(pe, true);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(*tmem_holder, C::TMEM_COLS);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(p.ws.counters + 1, 1u);
+        if (done == gridDim.x - 1) {  // last CTA: reset the scheduler for the next call
+            atomicExch(p.ws.counters, 0u);
+            atomicExch(p.ws.counters + 1, 0u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [B*H][n][d] bf16 viewed as a 3-D tensor {d, n, B*H}; 64 x 64 boxes, 128-B swizzle.
+bool make_qkv_map(CUtensorMap *m, const void *base, int BH, int n, int d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace sa

@@ -1,0 +1,188 @@
+// Longformer host side of the tensor-core forward ("Longformer", Sec. 3.1:
+// sliding window of w/2 tokens per side plus symmetric global attention).
+// A one-CTA preparation kernel turns the global list into per-block bit masks
+// and a compact list of the 64-key blocks holding global keys; the persistent
+// kernel then runs the global-row units (split-KV sweeps over all keys) and
+// one band unit per 128-row tile.
+#include "tc_kernel.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kPrepThreads = 1024;
+
+// For every 64-key block kb: gbits[kb] = bits of its global keys, gpre[kb] =
+// number of blocks before kb holding a global key (gpre[nkb] = their total),
+// glist = those blocks in increasing order. Entries of gidx out of [0, n) or
+// not above their predecessor are skipped and latch SA_ERR_BAD_INDEX. Every
+// output word is rewritten, so the scratch needs no clearing between calls.
+__global__ void __launch_bounds__(kPrepThreads) longformer_prep(const int32_t *gidx, int ng, int n, int nkb,
+                                                                unsigned long long *gbits, int *gpre, int *glist,
+                                                                unsigned *status) {
+    __shared__ int warp_off[kPrepThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    for (int i = tid; i < nkb; i += kPrepThreads) gbits[i] = 0ull;
+    __syncthreads();
+    bool bad = false;
+    for (int t = tid; t < ng; t += kPrepThreads) {
+        const int v = global_row(gidx, ng, n, t);
+        if (v >= n) {
+            bad = true;
+            continue;
+        }
+        atomicOr(gbits + (v >> 6), 1ull << (v & 63));
+    }
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(status, kDevBadIndex);
+    // exclusive prefix count of non-empty blocks; thread tid owns blocks [lo, hi)
+    const int seg = (nkb + kPrepThreads - 1) / kPrepThreads;
+    const int lo = min(nkb, tid * seg), hi = min(nkb, lo + seg);
+    int cnt = 0;
+    for (int i = lo; i < hi; ++i) cnt += __ldcg(gbits + i) != 0ull;
+    int inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += v;
+    }
+    if (lane == 31) warp_off[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        const int w = warp_off[lane];
+        int winc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, winc, o);
+            if (lane >= o) winc += v;
+        }
+        warp_off[lane] = winc - w;
+    }
+    __syncthreads();
+    int base = warp_off[wid] + inc - cnt;
+    for (int i = lo; i < hi; ++i) {
+        gpre[i] = base;
+        if (__ldcg(gbits + i) != 0ull) glist[base++] = i;
+    }
+    if (tid == kPrepThreads - 1) gpre[nkb] = base;
+}
+
+Geometry longformer_geometry(const Problem &p, const TcConfig &cfg) {
+    Geometry G = {};
+    G.B = p.B;
+    G.H = p.H;
+    G.n = p.n;
+    G.b = kBM;
+    G.half = p.window / 2 < p.n ? p.window / 2 : p.n;  // |i - k| < n always: a wider window changes nothing
+    G.tiles = (p.n + kBM - 1) / kBM;
+    G.ng = p.n_global;
+    G.gtiles = (p.n_global + kBM - 1) / kBM;
+    G.nkb = (p.n + 63) / 64;
+    G.steps_full = (p.n + kBN - 1) / kBN;
+    int s0 = (G.steps_full + kTargetChunkSteps - 1) / kTargetChunkSteps;
+    if (s0 > cfg.max_splits) s0 = cfg.max_splits;
+    if (s0 < 1) s0 = 1;
+    G.steps_per_chunk = (G.steps_full + s0 - 1) / s0;
+    G.splits = (G.steps_full + G.steps_per_chunk - 1) / G.steps_per_chunk;
+    const long long BH = (long long)p.B * p.H;
+    G.n_split_units = (int)(BH * G.gtiles * G.splits);
+    G.total_units = G.n_split_units + (int)(BH * G.tiles);
+    G.scale_log2 = 1.4426950408889634f / sqrtf((float)p.d);
+    G.wait_ns = (unsigned long long)cfg.wait_limit * 1000ull;
+    return G;
+}
+
+// Scratch: counters and per-row merge counters (zero at entry, left zero),
+// then split partials and the prep outputs (rewritten by every call).
+struct LfLayout {
+    size_t row_cnt, part_o, part_ml, gbits, gpre, glist, total;
+};
+
+LfLayout lf_layout(const Geometry &G, int d) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    LfLayout L;
+    const size_t tiles = (size_t)G.B * G.H * G.gtiles;
+    size_t off = 256;
+    L.row_cnt = off;
+    off += up(tiles * kBM * sizeof(unsigned));
+    if (G.splits > 1 && tiles > 0) {
+        L.part_o = off;
+        off += up(tiles * G.splits * kBM * d * sizeof(float));
+        L.part_ml = off;
+        off += up(tiles * G.splits * kBM * sizeof(float2));
+    } else {
+        L.part_o = L.part_ml = 0;
+    }
+    L.gbits = off;
+    off += up((size_t)G.nkb * sizeof(unsigned long long));
+    L.gpre = off;
+    off += up(((size_t)G.nkb + 1) * sizeof(int));
+    L.glist = off;
+    off += up((size_t)G.nkb * sizeof(int));
+    L.total = off;
+    return L;
+}
+
+template <int D>
+cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, size_t ws_bytes, cudaStream_t stream,
+                              int *launches) {
+    Params prm = {};
+    prm.geo = longformer_geometry(p, cfg);
+    const LfLayout L = lf_layout(prm.geo, D);
+    if (!ws || ws_bytes < L.total) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    prm.ws.counters = reinterpret_cast<unsigned *>(base);
+    prm.ws.row_cnt = reinterpret_cast<unsigned *>(base + L.row_cnt);
+    prm.ws.part_o = L.part_o ? reinterpret_cast<float *>(base + L.part_o) : nullptr;
+    prm.ws.part_ml = L.part_ml ? reinterpret_cast<float2 *>(base + L.part_ml) : nullptr;
+    prm.key_mask = p.key_mask;
+    prm.O = static_cast<__nv_bfloat16 *>(p.O);
+    prm.status = p.status;
+    prm.Q = static_cast<const __nv_bfloat16 *>(p.Q);
+    prm.gidx = p.global_idx;
+    unsigned long long *gbits = reinterpret_cast<unsigned long long *>(base + L.gbits);
+    int *gpre = reinterpret_cast<int *>(base + L.gpre);
+    int *glist = reinterpret_cast<int *>(base + L.glist);
+    prm.gbits = gbits;
+    prm.gpre = gpre;
+    prm.glist = glist;
+    const int BH = p.B * p.H;
+    CUtensorMap mq, mk, mv;
+    if (!make_qkv_map(&mq, p.Q, BH, p.n, D) || !make_qkv_map(&mk, p.K, BH, p.n, D) ||
+        !make_qkv_map(&mv, p.V, BH, p.n, D))
+        return cudaErrorInvalidValue;
+    auto kern = p.key_mask ? sparse_tc_fwd<D, true, true> : sparse_tc_fwd<D, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::ALLOC_BYTES);
+    if (e != cudaSuccess) return e;
+    if (prm.geo.ng > 0) {
+        longformer_prep<<<1, kPrepThreads, 0, stream>>>(p.global_idx, prm.geo.ng, p.n, prm.geo.nkb, gbits, gpre,
+                                                        glist, p.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        ++*launches;
+    }
+    int grid = cfg.grid_ctas;
+    if (grid > prm.geo.total_units) grid = prm.geo.total_units;
+    if (grid < 1) grid = 1;
+    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, prm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ++*launches;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t tc_longformer_workspace_bytes(const Problem &p, const TcConfig &cfg) {
+    return lf_layout(longformer_geometry(p, cfg), p.d).total;
+}
+
+size_t tc_longformer_counter_bytes(const Problem &p, const TcConfig &cfg) {
+    const LfLayout L = lf_layout(longformer_geometry(p, cfg), p.d);
+    return L.part_o ? L.part_o : L.gbits;
+}
+
+cudaError_t launch_tc_longformer(const Problem &p, const TcConfig &cfg, void *ws, size_t ws_bytes,
+                                 cudaStream_t stream, int *launches) {
+    *launches = 0;
+    return (p.d == 64) ? launch_longformer<64>(p, cfg, ws, ws_bytes, stream, launches)
+                       : launch_longformer<128>(p, cfg, ws, ws_bytes, stream, launches);
+}
+
+}  // namespace sa

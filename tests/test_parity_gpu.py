@@ -120,6 +120,38 @@ def test_longformer_fp32(path):
     longformer_case(1, 1, 640, 64, 64, gidx, dtype="fp32", path=path, tol=FP32_TOL)
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_d128_padded(path):
+    from block_sparse_long_bigbird_gb300.inputs import make_global_positions
+
+    B, n = 2, 1100
+    gidx = make_global_positions(n, 40, seed=11)
+    km = make_key_mask(B, n, seed=12)
+    longformer_case(B, 1, n, 128, 200, gidx, key_mask=km, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_every_token_global(path):
+    # every row is a global row: the band units store nothing, three global tiles
+    n = 300
+    gidx = torch.arange(n, dtype=torch.int32)
+    longformer_case(1, 2, n, 64, 32, gidx, path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_split_global_rows(path):
+    # 12288 keys = 96 steps of 128: the global rows sweep in two split-KV chunks;
+    # 131 global rows span two global tiles
+    from block_sparse_long_bigbird_gb300.inputs import make_global_positions
+
+    n = 12288
+    gidx = make_global_positions(n, 131, seed=13)
+    rng = np.random.default_rng(14)
+    rows = np.unique(np.concatenate([gidx.numpy(), np.arange(0, 200), np.arange(n - 200, n),
+                                     rng.choice(n, 300, replace=False)]))
+    longformer_case(1, 2, n, 64, 256, gidx, path=path, rows=rows)
+
+
 # ------------------------------------------------------------- full-size workloads (sampled rows)
 
 @pytest.mark.parametrize("path", PATHS)
