@@ -35,7 +35,7 @@ from block_sparse_long_bigbird_gb300.workloads import HEADLINE, WORKLOADS  # noq
 METRIC = "useful TFLOP/s and tokens/s of sparse attn fwd at n=4096, % of bf16 tensor peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
-TC_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_attn.cu")
+TC_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_kernel.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -352,7 +352,8 @@ def main(argv=None):
 
     peaks, peak_src = read_peaks()
     kernel_tflops = prob["flops"] / (my_ms * 1e-3) / 1e12
-    kernel_name = "bigbird_tc_fwd" if wl.kind == "bigbird" else "longformer_tc_fwd"
+    kernel_name = "sparse_tc_fwd<{},{},{}>".format(wl.d, "padded" if wl.padded else "dense",
+                                                   "longformer" if wl.kind == "longformer" else "bigbird")
     traffic = read_traffic(kernel_name, wl.name)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": traffic,

@@ -76,8 +76,8 @@ def bigbird_case(B, H, n, d, b, g, w, r, dtype="bf16", sigma=1.0, cfg_id=50, key
 
 
 def longformer_case(B, H, n, d, window, gidx, dtype="bf16", cfg_id=60, key_mask=None, path="tc",
-                    rows=None, heads=None, tol=(2e-2, 2e-3)):
-    Q, K, V = make_qkv(B, H, n, d, dtype, cfg_id=cfg_id)
+                    rows=None, heads=None, tol=(2e-2, 2e-3), sigma=1.0):
+    Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
     O = gpu_longformer(Q, K, V, window, gidx, key_mask, path).float().cpu()
     heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
     g_np = np.zeros(0, dtype=np.int64) if gidx is None else gidx.numpy()

@@ -152,6 +152,35 @@ def test_longformer_split_global_rows(path):
     longformer_case(1, 2, n, 64, 256, gidx, path=path, rows=rows)
 
 
+# σ = 4 spreads the scaled scores over ~±50: within one 128-key step a row's
+# running maximum often rises by more than the lazy-rescale threshold between
+# the two 64-key halves, so the rescale of the first half's P runs for some
+# rows of a warp and not others. Outputs reach |O| ~ 16 (bf16 half-ulp 1/16
+# there), so the tolerance is 8x the σ = 1 one; a first-half P left unscaled
+# would be off by a factor of at least 2^8.
+WIDE_TOL = (1.6e-1, 1.6e-2)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_bigbird_wide_score_range(path, d):
+    bigbird_case(1, 2, 1024, d, 64, 2, 3, 3, sigma=4.0, cfg_id=81, path=path, tol=WIDE_TOL)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_wide_score_range_padded(path):
+    B, n = 2, 1024
+    km = make_key_mask(B, n, seed=21, low=200)
+    bigbird_case(B, 1, n, 64, 64, 2, 3, 3, sigma=4.0, cfg_id=82, key_mask=km, path=path, tol=WIDE_TOL)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_longformer_wide_score_range(path, d):
+    gidx = torch.tensor([0, 5, 500, 999], dtype=torch.int32)
+    longformer_case(1, 2, 1000, d, 64, gidx, sigma=4.0, cfg_id=83, path=path, tol=WIDE_TOL)
+
+
 # ------------------------------------------------------------- full-size workloads (sampled rows)
 
 @pytest.mark.parametrize("path", PATHS)
