@@ -54,10 +54,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kBM = 128;           // query rows per tile = TMEM lanes
-constexpr int kBN = 128;           // keys per step = S tile columns
 constexpr int kNU = 4;             // unit-info ring depth
-constexpr int kSI = 6;             // step-info ring depth
-constexpr int kTargetChunkSteps = 64;
+constexpr int kTargetChunkKeys = 8192;  // keys per split-KV chunk (at most)
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (factor 256)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzled region
@@ -81,37 +79,49 @@ struct StepInfo {
 };
 static_assert(sizeof(StepInfo) == 32, "StepInfo layout");
 
+// Keys per pipeline step (= S columns of one step): 64 for d = 64, where
+// two query tiles share the SM and each tile's TMEM share (256 columns) holds
+// two 64-column S slots and two O buffers; 128 for d = 128 (one tile, two
+// 128-column S slots, two O buffers). Host and device both use this.
+__host__ __device__ constexpr int keys_per_step(int d) { return d == 64 ? 64 : 128; }
+
 template <int D>
 struct Cfg {
     // Query tiles in flight per CTA: two independent pipelines for d = 64
     // (one tile's softmax overlaps the other's waits and MMAs), one for d = 128.
     static constexpr int NT = (D == 64) ? 2 : 1;
     static constexpr int THREADS = 128 + 128 * NT;  // control warps + one softmax warpgroup per tile
-    static constexpr int NS = (NT == 2) ? 1 : 2;    // S buffers per tile; P is written over S
-    static constexpr int KST = 3, VST = 3, NQ = 1;  // K / V / Q stages per tile
-    static constexpr int TILE_BYTES = 128 * D * 2;  // Q tile / K step / V step
+    static constexpr int KB = keys_per_step(D);     // keys per step
+    static constexpr int SUB = KB / 64;             // 64-key sub-blocks per step
+    static constexpr int NS = 2;                    // S slots per tile (QK^T of step g+1 overlaps softmax g)
+    static constexpr int KST = (KB == 64) ? 5 : 3;  // K / V stages per tile
+    static constexpr int VST = KST, NQ = 1;
+    static constexpr int SI = (KB == 64) ? 8 : 6;   // step-info ring depth
+    static constexpr int Q_BYTES = kBM * D * 2;     // Q tile
+    static constexpr int KV_BYTES = KB * D * 2;     // K or V stage
+    static constexpr int KV_REGION = KB * 128;      // one 64-column swizzled region of a K/V stage
     // per-tile big buffers (1024-B aligned), then per-tile small areas
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + NQ * TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
-    static constexpr int BIG = V_OFF + VST * TILE_BYTES;
+    static constexpr int K_OFF = Q_OFF + NQ * Q_BYTES;
+    static constexpr int V_OFF = K_OFF + KST * KV_BYTES;
+    static constexpr int BIG = V_OFF + VST * KV_BYTES;
     // barrier slots within a tile's small area
     static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
-                         B_IF = B_VE + VST, B_IE = B_IF + kSI, B_SF = B_IE + kSI, B_PF = B_SF + NS, B_PV = B_PF + NS,
+                         B_IF = B_VE + VST, B_IE = B_IF + SI, B_SF = B_IE + SI, B_PF = B_SF + NS, B_PV = B_PF + NS,
                          B_UF = B_PV + NS, B_UE = B_UF + kNU, B_DRAIN = B_UE + kNU, B_COUNT = B_DRAIN + 1;
     static constexpr int BAR_OFF = 0;
     static constexpr int UNIT_OFF = (B_COUNT * 8 + 15) & ~15;
     static constexpr int STEP_OFF = UNIT_OFF + kNU * 64;
-    static constexpr int LIST_OFF = STEP_OFF + kSI * 32;  // two lists: the next unit is decoded early
+    static constexpr int LIST_OFF = STEP_OFF + SI * 32;  // two lists: the next unit is decoded early
     static constexpr int SMALL = LIST_OFF + 2 * 32 * 4;
     static constexpr int SMALL_OFF = NT * BIG;
     static constexpr int MISC_OFF = SMALL_OFF + NT * SMALL;  // TMEM address, abort flag
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr int ALLOC_BYTES = SMEM_BYTES + 1024;  // slack for 1024-B alignment
-    // TMEM: each tile owns TILE_COLS columns: NS S buffers of 128, then two O buffers of D
+    // TMEM: each tile owns TILE_COLS columns: NS S slots of KB, then two O buffers of D
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TILE_COLS = TMEM_COLS / NT;
-    static constexpr uint32_t O_COL = NS * 128;
+    static constexpr uint32_t O_COL = NS * KB;
 
     static_assert(O_COL + 2 * D <= TILE_COLS, "TMEM columns per tile");
     static_assert(BIG % 1024 == 0, "tile buffers stay 1024-B aligned");
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     sparse_tc_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
     using C = Cfg<D>;
-    static_assert(kSI * 2 * 8 <= 2 * 32 * 4, "Longformer global-key masks fit the list area");
+    static_assert(C::SI * 2 * 8 <= 2 * 32 * 4, "Longformer global-key masks fit the list area");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -417,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 mbar_init(bar(C::B_VF + i), 1);
                 mbar_init(bar(C::B_VE + i), 1);
             }
-            for (int i = 0; i < kSI; ++i) {
+            for (int i = 0; i < C::SI; ++i) {
                 mbar_init(bar(C::B_IF + i), 1);
                 mbar_init(bar(C::B_IE + i), 4);  // one arrival per softmax warp
             }
@@ -552,7 +562,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         ui.pad0 = ui.pad1 = 0;
                         ui.pad[0] = bhi - blo + 1;
                     }
-                    ui.n_steps = any_row ? (ui.pad[0] + 1) / 2 : 0;
+                    ui.n_steps = any_row ? (ui.pad[0] + C::SUB - 1) / C::SUB : 0;
                 }
                 if (lane == 0) {
                     ring[slot] = ui;
@@ -568,7 +578,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 ui.j1 = -1;
             }
             const UnitPtrs up = unit_ptrs(p, ui);
-            const int bps = (G.b == 64) ? 2 : 1;  // key blocks per step
+            // steps covering `nlist` key blocks of b keys, KB keys per step
+            auto list_steps = [&](int nlist) {
+                return G.b == 64 ? (nlist + C::SUB - 1) / C::SUB : nlist * (2 / C::SUB);
+            };
             if (ui.step0 < 0) {
                 bool any_row = true;
                 if (up.km) {
@@ -588,7 +601,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     }
                 }
                 ui.pad0 = nlist;
-                ui.n_steps = (nlist + bps - 1) / bps;
+                ui.n_steps = list_steps(nlist);
             }
 
             if (lane == 0) {
@@ -637,7 +650,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 } else {
                     if (lane == 0) {
                         const uint32_t dst = tbase + C::Q_OFF;
-                        mbar_arrive_expect_tx(bar(C::B_QF), C::TILE_BYTES);
+                        mbar_arrive_expect_tx(bar(C::B_QF), C::Q_BYTES);
                         for (int dc = 0; dc < D / 64; ++dc)
                             for (int rh = 0; rh < 2; ++rh)
                                 tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF), dc * 64,
@@ -662,12 +675,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         si.masked = 0;
                         const int nband = cur.j1 - cur.j0 + 1;
 #pragma unroll
-                        for (int s = 0; s < 2; ++s) {
-                            const int li = 2 * t + s;
+                        for (int s = 0; s < C::SUB; ++s) {
+                            const int li = C::SUB * t + s;
                             int kb = -1;
                             bool band = false;
                             if (cur.step0 >= 0) {
-                                kb = 2 * (cur.step0 + t) + s;
+                                kb = C::SUB * (cur.step0 + t) + s;
                                 if (kb >= G.nkb) kb = -1;
                             } else if (li < cur.pad0) {
                                 kb = __ldg(p.glist + li);
@@ -695,33 +708,31 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         }
                     } else {
 #pragma unroll
-                    for (int s = 0; s < 2; ++s) {
+                    for (int s = 0; s < C::SUB; ++s) {
+                        // sub-slot u (64 keys) of the unit; a b = 128 block spans two
+                        const int u = C::SUB * t + s;
+                        const int part = (G.b == 64) ? 0 : (u & 1);
                         int kb = -1, y = G.n;
                         bool a0 = false, a1 = false;
                         if (cur.step0 >= 0) {  // full sweep of a global tile
-                            if (G.b == 64) {
-                                kb = 2 * (cur.step0 + t) + s;
-                                if (kb >= G.nb) kb = -1;
-                                y = kb >= 0 ? kb * 64 : G.n;
-                            } else {
-                                kb = cur.step0 + t;
-                                y = kb * 128 + s * 64;
-                            }
-                            if (kb >= 0) {
+                            const int yy = (C::SUB * cur.step0) * 64 + u * 64;
+                            if (yy < G.n) {
+                                y = yy;
+                                kb = (G.b == 64) ? (yy >> 6) : (yy >> 7);
                                 a0 = block_allowed(p, up.r0, cur.j0, kb);
                                 a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
                             }
                         } else if (!slow_cur) {
-                            const int li = (G.b == 64) ? 2 * t + s : t;
+                            const int li = (G.b == 64) ? u : (u >> 1);
                             if (li < nlist) {
                                 const uint32_t e = lcur[li];
                                 kb = (int)(e & 0x3FFFFFFFu);
                                 a0 = (e >> 30) & 1u;
                                 a1 = (G.b == 64) ? ((e >> 31) & 1u) : a0;
-                                y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                                y = kb * G.b + part * 64;
                             }
                         } else {
-                            if (G.b == 64 || s == 0) {
+                            if (part == 0) {
                                 do {
                                     xs = union_next_slow(p, up.r0, up.r1, up.wlo, up.whi, xs);
                                 } while (xs < G.nb && up.km && !block_has_valid_warp(up.km, xs, G.b));
@@ -730,7 +741,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                 kb = xs;
                                 a0 = block_allowed(p, up.r0, cur.j0, kb);
                                 a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
-                                y = (G.b == 64) ? kb * 64 : kb * 128 + s * 64;
+                                y = kb * G.b + part * 64;
                             }
                         }
                         si.y[s] = y;
@@ -745,8 +756,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     }
                     }
                     // step info -> softmax
-                    const uint32_t ii = g % kSI;
-                    if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
+                    const uint32_t ii = g % C::SI;
+                    if (g >= C::SI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / C::SI) - 1) & 1, ctl))) break;
                     if (lane == 0) {
                         steps[ii] = si;
                         if (LF) {
@@ -759,11 +770,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     const uint32_t sk = g % C::KST;
                     if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
                     if (lane == 0) {
-                        const uint32_t kdst = tbase + C::K_OFF + sk * C::TILE_BYTES;
-                        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::TILE_BYTES);
-                        for (int s = 0; s < 2; ++s)
+                        const uint32_t kdst = tbase + C::K_OFF + sk * C::KV_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::KV_BYTES);
+                        for (int s = 0; s < C::SUB; ++s)
                             for (int dc = 0; dc < D / 64; ++dc)
-                                tma_load_3d(kdst + dc * kRegionBytes + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
+                                tma_load_3d(kdst + dc * C::KV_REGION + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
                                             si.y[s], cur.bh);
                     }
                     ++k_arms[sk];
@@ -771,11 +782,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     const uint32_t sv = g % C::VST;
                     if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
                     if (lane == 0) {
-                        const uint32_t vdst = tbase + C::V_OFF + sv * C::TILE_BYTES;
-                        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::TILE_BYTES);
-                        for (int s = 0; s < 2; ++s)
+                        const uint32_t vdst = tbase + C::V_OFF + sv * C::KV_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::KV_BYTES);
+                        for (int s = 0; s < C::SUB; ++s)
                             for (int dc = 0; dc < D / 64; ++dc)
-                                tma_load_3d(vdst + dc * kRegionBytes + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
+                                tma_load_3d(vdst + dc * C::KV_REGION + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
                                             si.y[s], cur.bh);
                     }
                     ++v_arms[sv];
@@ -794,7 +805,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     } else if (role == 1) {
         // ================================================================ MMA issuer (tile x)
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16(128, kBN, false);
+            constexpr uint32_t idesc_qk = idesc_bf16(128, C::KB, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
             uint32_t g = 0, qcnt = 0;
             int pend = -1;
@@ -807,11 +818,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 if (!wait_one(bar(C::B_PF + sb), (h / C::NS) & 1, ctl)) return false;
                 if (!wait_one(bar(C::B_VF + sv), (h / C::VST) & 1, ctl)) return false;
                 tc_fence_after();
-                const uint32_t pt = tmem + sb * kBN;
-                const uint32_t va = tbase + C::V_OFF + sv * C::TILE_BYTES;
+                const uint32_t pt = tmem + sb * C::KB;
+                const uint32_t va = tbase + C::V_OFF + sv * C::KV_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t b = desc_sw128(va + kk * 2048, kRegionBytes);
+                for (int kk = 0; kk < C::KB / 16; ++kk) {
+                    const uint64_t b = desc_sw128(va + kk * 2048, C::KV_REGION);
                     mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(bar(C::B_VE + sv));
@@ -825,7 +836,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 const int n_steps = ring[slot].n_steps;
                 mbar_arrive(bar(C::B_UE + slot));
                 if (kind == kUnitEnd) break;
-                if (n_steps == 0) continue;
+                if (n_steps == 0) {
+                    // The softmax writes the previous unit's epilogue while it handles
+                    // this empty unit, and that needs the held-back PV: issue it now
+                    // rather than after a later unit's first QK^T (which may wait on
+                    // ring slots the softmax has not released yet).
+                    if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
+                    pend = -1;
+                    continue;
+                }
                 const uint32_t ob = qcnt & 1;
                 if (!(ok = wait_one(bar(C::B_QF), qcnt & 1, ctl))) break;
                 tc_fence_after();
@@ -834,26 +853,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     const uint32_t sk = g % C::KST, sb = g % C::NS;
                     if (!(ok = wait_one(bar(C::B_KF + sk), (g / C::KST) & 1, ctl))) break;
                     tc_fence_after();
-                    const uint32_t ka = tbase + C::K_OFF + sk * C::TILE_BYTES;
+                    const uint32_t ka = tbase + C::K_OFF + sk * C::KV_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kRegionBytes + (kk & 3) * 32;
-                        mma_bf16_ss(tmem + sb * kBN, desc_sw128(qa + off, 16), desc_sw128(ka + off, 16), idesc_qk,
-                                    kk > 0 ? 1u : 0u);
+                        const uint32_t qoff = (kk >> 2) * kRegionBytes + (kk & 3) * 32;
+                        const uint32_t koff = (kk >> 2) * C::KV_REGION + (kk & 3) * 32;
+                        mma_bf16_ss(tmem + sb * C::KB, desc_sw128(qa + qoff, 16), desc_sw128(ka + koff, 16),
+                                    idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(C::B_KE + sk));
                     mma_commit(bar(C::B_SF + sb));
                     if (t == n_steps - 1) mma_commit(bar(C::B_QE));
-                    if (C::NS == 1) {
-                        // one S buffer: P_g overwrites S_g, so PV_g precedes S_{g+1}
-                        if (!(ok = issue_pv(g, t == 0, ob))) break;
-                    } else {
-                        // two S buffers: S_{g} overlaps the softmax of step g-1
-                        if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
-                        pend = (int)g;
-                        pend_first = (t == 0);
-                        pend_ob = ob;
-                    }
+                    // two S slots: S_g overlaps the softmax of step g-1, then PV_{g-1}
+                    if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
+                    pend = (int)g;
+                    pend_first = (t == 0);
+                    pend_ob = ob;
                 }
                 ++qcnt;
             }
@@ -1035,8 +1050,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             float m_ref = -CUDART_INF_F, l = 0.f;
             const uint32_t obase = tmem + lane_base + C::O_COL + cur.ob * D;
             for (int t = 0; t < ui.n_steps; ++t, ++g) {
-                const uint32_t ii = g % kSI, sb = g % C::NS;
-                if (!(ok = wait_warp(bar(C::B_IF + ii), (g / kSI) & 1, ctl))) break;
+                const uint32_t ii = g % C::SI, sb = g % C::NS;
+                if (!(ok = wait_warp(bar(C::B_IF + ii), (g / C::SI) & 1, ctl))) break;
                 const uint32_t allow = steps[ii].allow;
                 uint64_t km0 = ~0ull, km1 = ~0ull, gm0 = 0ull, gm1 = 0ull;
                 int y0 = 0, y1 = 0;
@@ -1056,21 +1071,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(C::B_IE + ii));
                 if (!(ok = wait_warp(bar(C::B_SF + sb), (g / C::NS) & 1, ctl))) break;
                 tc_fence_after();
-                // The buffer holding S_g receives P_g; PV of step g - NS must have
-                // read the previous P there (completes before S_g in issue order;
-                // the wait also establishes that PV_{g-1} completed when NS == 1).
+                // The slot holding S_g receives P_g; PV of step g - NS must have
+                // read the previous P there (it completes before S_g in issue order).
                 if (g >= (uint32_t)C::NS &&
                     !(ok = wait_warp(bar(C::B_PV + sb), ((g - C::NS) / C::NS) & 1, ctl)))
                     break;
-                const uint32_t sa = tmem + lane_base + sb * kBN;
-                // Stream the two 64-key halves: each is loaded, reduced and
-                // exponentiated against the running reference m_ref, then
-                // written back as bf16 P over the first 64 columns of S_g.
+                const uint32_t sa = tmem + lane_base + sb * C::KB;
+                // Stream the step's 64-key sub-blocks ("halves"; one for d = 64):
+                // each is loaded, reduced and exponentiated against the running
+                // reference m_ref, then written back as bf16 P over the first
+                // KB / 2 columns of S_g.
                 float alpha = 1.f;
                 bool resc = false;  // O needs a rescale by alpha
                 float lsum = 0.f;
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < C::SUB; ++half) {
                     const bool w_ok = (allow >> (2 * half + hf)) & 1u;  // warp-uniform
                     uint32_t pk[32];
                     if (w_ok) {
@@ -1192,8 +1207,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 tc_fence_before();
                 mbar_arrive(bar(C::B_PF + sb));
                 if (t == 0 && pe.kind != kUnitEnd) {  // previous unit's epilogue, now off the critical path
-                    // NS == 1: the P-buffer wait above already saw PV of step g-1 complete
-                    if (!(ok = epilogue(pe, C::NS != 1))) break;
+                    if (!(ok = epilogue(pe, true))) break;
                     pe.kind = kUnitEnd;
                 }
             }

@@ -76,8 +76,9 @@ Geometry longformer_geometry(const Problem &p, const TcConfig &cfg) {
     G.ng = p.n_global;
     G.gtiles = (p.n_global + kBM - 1) / kBM;
     G.nkb = (p.n + 63) / 64;
-    G.steps_full = (p.n + kBN - 1) / kBN;
-    int s0 = (G.steps_full + kTargetChunkSteps - 1) / kTargetChunkSteps;
+    const int kb = keys_per_step(p.d), target_steps = kTargetChunkKeys / kb;
+    G.steps_full = (p.n + kb - 1) / kb;
+    int s0 = (G.steps_full + target_steps - 1) / target_steps;
     if (s0 > cfg.max_splits) s0 = cfg.max_splits;
     if (s0 < 1) s0 = 1;
     G.steps_per_chunk = (G.steps_full + s0 - 1) / s0;

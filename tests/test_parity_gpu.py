@@ -83,6 +83,22 @@ def test_bigbird_fully_padded_sequence(path):
     bigbird_case(B, 1, n, 64, 64, 2, 3, 3, key_mask=km, path=path)
 
 
+@pytest.mark.parametrize("d,b", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("grid", [1, 3])
+def test_bigbird_padded_runs_few_ctas(d, b, grid):
+    # A persistent CTA meets long runs of fully padded tiles (empty units)
+    # right after tiles with work: batch 0 is valid up to token 1000, batch 1
+    # is all padding. With one or three CTAs every tile walks those runs.
+    B, n = 2, 4096
+    km = torch.zeros(B, n, dtype=torch.uint8)
+    km[0, :1000] = 1
+    sa.set_option(sa.SA_OPT_GRID_CTAS, grid)
+    try:
+        bigbird_case(B, 2, n, d, b, 2, 3, 3, key_mask=km, path="tc", cfg_id=84)
+    finally:
+        sa.set_option(sa.SA_OPT_GRID_CTAS, 0)
+
+
 # ------------------------------------------------------------- Longformer, small full compares
 
 LONGFORMER_SMALL = [
