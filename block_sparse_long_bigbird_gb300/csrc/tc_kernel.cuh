@@ -91,6 +91,10 @@ struct Cfg {
     // (one tile's softmax overlaps the other's waits and MMAs), one for d = 128.
     static constexpr int NT = (D == 64) ? 2 : 1;
     static constexpr int THREADS = 128 + 128 * NT;  // control warps + one softmax warpgroup per tile
+    // With one tile the spare control warps 2 and 3 issue the V and K copies:
+    // a thread's bulk copies complete one after another (a few hundred cycles
+    // each), so a producer that also decodes units cannot keep d = 128 fed.
+    static constexpr bool LOADERS = (NT == 1);
     static constexpr int KB = keys_per_step(D);     // keys per step
     static constexpr int SUB = KB / 64;             // 64-key sub-blocks per step
     static constexpr int NS = 2;                    // S slots per tile (QK^T of step g+1 overlaps softmax g)
@@ -344,12 +348,24 @@ __device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1,
     const bool a0 = valid && (j0 < G.g || v < G.g || abs(v - j0) <= G.half || in_r0);
     const bool a1 = valid && j1 >= 0 && (j1 < G.g || v < G.g || abs(v - j1) <= G.half || in_r1);
     const unsigned vm = __ballot_sync(kFull, valid);
-    int pos = 0;
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) {
-        const int vj = __shfl_sync(kFull, v, j);
-        pos += ((vm >> j) & 1u) && vj < v;
+    // Rank among the survivors = survivors holding a smaller block, found by
+    // comparing block indices bit by bit from the top (one ballot per bit;
+    // far cheaper than a shuffle per lane beside busy softmax warps): `eq`
+    // keeps the survivors equal to v on the bits seen so far, `less` collects
+    // those found smaller. Valid indices are < nb <= 2^nbits.
+    unsigned eq = vm, less = 0u;
+    const int nbits = 32 - __clz(max(G.nb - 1, 1));
+    for (int bb = nbits - 1; bb >= 0; --bb) {
+        const bool one = (v >> bb) & 1;
+        const unsigned ones = __ballot_sync(kFull, one);
+        if (one) {
+            less |= eq & ~ones;
+            eq &= ones;
+        } else {
+            eq &= ~ones;
+        }
     }
+    const int pos = __popc(less);
     if (valid) list[pos] = (uint32_t)v | (a0 ? (1u << 30) : 0u) | (a1 ? (1u << 31) : 0u);
     __syncwarp();
     return __popc(vm);
@@ -429,7 +445,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             }
             for (int i = 0; i < C::SI; ++i) {
                 mbar_init(bar(C::B_IF + i), 1);
-                mbar_init(bar(C::B_IE + i), 4);  // one arrival per softmax warp
+                mbar_init(bar(C::B_IE + i), 4 + (C::LOADERS ? 2 : 0));  // softmax warps (+ loaders)
             }
             for (int i = 0; i < C::NS; ++i) {
                 mbar_init(bar(C::B_SF + i), 1);
@@ -438,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             }
             for (int i = 0; i < kNU; ++i) {
                 mbar_init(bar(C::B_UF + i), 1);
-                mbar_init(bar(C::B_UE + i), 1 + 128);
+                mbar_init(bar(C::B_UE + i), 1 + 128 + (C::LOADERS ? 2 : 0));  // MMA, softmax (+ loaders)
             }
             mbar_init(bar(C::B_DRAIN), 1);
         }
@@ -458,10 +474,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     tc_fence_after();
 
     // Role and tile of this warp: warps 2x and 2x+1 are tile x's producer and
-    // MMA issuer; warps 4 + 4x .. 7 + 4x its softmax warpgroup.
-    int role = -1, x = 0;  // 0 producer, 1 MMA, 2 softmax
+    // MMA issuer (with one tile, warps 2 and 3 load V and K); warps
+    // 4 + 4x .. 7 + 4x its softmax warpgroup.
+    int role = -1, x = 0;  // 0 producer, 1 MMA, 2 softmax, 3 V loader, 4 K loader
     if (warp < 4) {
-        if ((warp >> 1) < C::NT) {
+        if (C::LOADERS) {
+            role = (warp < 2) ? warp : (warp == 2 ? 3 : 4);
+        } else if ((warp >> 1) < C::NT) {
             role = warp & 1;
             x = warp >> 1;
         }
@@ -615,8 +634,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         UnitInfo cur = decode_next(0, list, slow_cur);
         for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
             uint32_t *lcur = list + (ui_idx & 1) * 32;
-            const UnitInfo nxt = decode_next(ui_idx + 1, list + ((ui_idx + 1) & 1) * 32, slow_nxt);
-            if (!ok) break;
+            // The next unit is decoded one unit ahead. With loader warps it is
+            // decoded once this unit's first steps are out (the loaders then
+            // run ahead meanwhile); otherwise first, because this warp's own
+            // copies and step records must not pause mid-unit.
+            UnitInfo nxt;
+            bool have_nxt = false;
+            auto decode_ahead = [&]() {
+                if (!have_nxt) {
+                    nxt = decode_next(ui_idx + 1, list + ((ui_idx + 1) & 1) * 32, slow_nxt);
+                    have_nxt = true;
+                }
+            };
+            if (!C::LOADERS) {
+                decode_ahead();
+                if (!ok) break;
+            }
             if (cur.n_steps > 0) {
                 const UnitPtrs up = unit_ptrs(p, cur);
                 const int nlist = cur.pad0;
@@ -766,6 +799,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         }
                         mbar_arrive(bar(C::B_IF + ii));
                     }
+                    if constexpr (!C::LOADERS) {
                     // K
                     const uint32_t sk = g % C::KST;
                     if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
@@ -790,8 +824,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                             si.y[s], cur.bh);
                     }
                     ++v_arms[sv];
+                    }
+                    if (t == 1) {
+                        decode_ahead();
+                        if (!ok) break;
+                    }
                 }
             }
+            if (!ok) break;
+            decode_ahead();
+            if (!ok) break;
             cur = nxt;
             slow_cur = slow_nxt;
         }
@@ -877,6 +919,45 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             mma_commit(bar(C::B_DRAIN));
             wait_drain(bar(C::B_DRAIN), 0, G.wait_ns);
         }
+    } else if (role == 3 || role == 4) {
+        // ================================================================ V (3) / K (4) loader
+        // Follows the unit ring and the step records; one box per lane.
+        const bool is_k = (role == 4);
+        const CUtensorMap *tmap = is_k ? &tmK : &tmV;
+        const uint32_t buf0 = tbase + (is_k ? C::K_OFF : C::V_OFF);
+        const int bf = is_k ? C::B_KF : C::B_VF, be = is_k ? C::B_KE : C::B_VE;
+        static_assert(C::KST == C::VST, "one stage count for both loaders");
+        uint32_t arms[C::KST] = {};
+        uint32_t g = 0;
+        bool ok = true;
+        for (uint32_t ui_idx = 0; ok; ++ui_idx) {
+            const uint32_t slot = ui_idx % kNU;
+            if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
+            const int kind = ring[slot].kind, n_steps = ring[slot].n_steps, bh = ring[slot].bh;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_UE + slot));
+            if (kind == kUnitEnd) break;
+            for (int t = 0; t < n_steps; ++t, ++g) {
+                const uint32_t ii = g % C::SI;
+                if (!(ok = wait_warp(bar(C::B_IF + ii), (g / C::SI) & 1, ctl))) break;
+                const int y0 = steps[ii].y[0], y1 = steps[ii].y[1];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_IE + ii));
+                const uint32_t st = g % C::KST;
+                if (g >= (uint32_t)C::KST && !(ok = wait_warp(bar(be + st), ((g / C::KST) - 1) & 1, ctl))) break;
+                const uint32_t dst = buf0 + st * C::KV_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(bar(bf + st), C::KV_BYTES);
+                __syncwarp();
+                if (lane < C::SUB * (D / 64)) {
+                    const int s = lane / (D / 64), dc = lane % (D / 64);
+                    tma_load_3d(dst + dc * C::KV_REGION + s * 8192, tmap, bar(bf + st), dc * 64, s ? y1 : y0, bh);
+                }
+                ++arms[st];
+            }
+        }
+        if (!ok && lane == 0)  // abort: wait for the copies still in flight
+            for (int i = 0; i < C::KST; ++i)
+                if (arms[i]) wait_drain(bar(bf + i), (arms[i] - 1) & 1, G.wait_ns);
     } else if (role == 2) {
         // ================================================================ softmax / epilogue (tile x)
         const int tid = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
