@@ -867,7 +867,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     const uint64_t b = desc_sw128(va + kk * 2048, C::KV_REGION);
                     mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
                 }
-                mma_commit(bar(C::B_VE + sv));
                 mma_commit(bar(C::B_PV + sb));
                 return true;
             };
@@ -903,7 +902,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         mma_bf16_ss(tmem + sb * C::KB, desc_sw128(qa + qoff, 16), desc_sw128(ka + koff, 16),
                                     idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(C::B_KE + sk));
                     mma_commit(bar(C::B_SF + sb));
                     if (t == n_steps - 1) mma_commit(bar(C::B_QE));
                     // two S slots: S_g overlaps the softmax of step g-1, then PV_{g-1}
@@ -1152,11 +1150,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(C::B_IE + ii));
                 if (!(ok = wait_warp(bar(C::B_SF + sb), (g / C::NS) & 1, ctl))) break;
                 tc_fence_after();
-                // The slot holding S_g receives P_g; PV of step g - NS must have
-                // read the previous P there (it completes before S_g in issue order).
-                if (g >= (uint32_t)C::NS &&
-                    !(ok = wait_warp(bar(C::B_PV + sb), ((g - C::NS) / C::NS) & 1, ctl)))
-                    break;
+                // MMAs of one thread complete in issue order (S_g, PV_{g-1},
+                // S_{g+1}, ...), so S_g complete means: K_g is consumed, PV_{g-2}
+                // has read the P that S_g's slot held and its V stage is free.
+                // The stage releases go out from here rather than as tensor-core
+                // commits, each of which costs the shared MMA front end about as
+                // much as an MMA.
+                if (tid == 0) {
+                    mbar_arrive(bar(C::B_KE + g % C::KST));
+                    if (g >= 2) mbar_arrive(bar(C::B_VE + (g - 2) % C::VST));
+                }
                 const uint32_t sa = tmem + lane_base + sb * C::KB;
                 // Stream the step's 64-key sub-blocks ("halves"; one for d = 64):
                 // each is loaded, reduced and exponentiated against the running
