@@ -800,30 +800,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         mbar_arrive(bar(C::B_IF + ii));
                     }
                     if constexpr (!C::LOADERS) {
-                    // K
-                    const uint32_t sk = g % C::KST;
-                    if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
-                    if (lane == 0) {
-                        const uint32_t kdst = tbase + C::K_OFF + sk * C::KV_BYTES;
-                        mbar_arrive_expect_tx(bar(C::B_KF + sk), C::KV_BYTES);
-                        for (int s = 0; s < C::SUB; ++s)
-                            for (int dc = 0; dc < D / 64; ++dc)
-                                tma_load_3d(kdst + dc * C::KV_REGION + s * 8192, &tmK, bar(C::B_KF + sk), dc * 64,
-                                            si.y[s], cur.bh);
-                    }
-                    ++k_arms[sk];
-                    // V
-                    const uint32_t sv = g % C::VST;
-                    if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
-                    if (lane == 0) {
-                        const uint32_t vdst = tbase + C::V_OFF + sv * C::KV_BYTES;
-                        mbar_arrive_expect_tx(bar(C::B_VF + sv), C::KV_BYTES);
-                        for (int s = 0; s < C::SUB; ++s)
-                            for (int dc = 0; dc < D / 64; ++dc)
-                                tma_load_3d(vdst + dc * C::KV_REGION + s * 8192, &tmV, bar(C::B_VF + sv), dc * 64,
-                                            si.y[s], cur.bh);
-                    }
-                    ++v_arms[sv];
+                        // K and V of the step in one copy instruction, one box per
+                        // lane: a thread's bulk copies complete one after another,
+                        // different lanes' copies overlap
+                        const uint32_t sk = g % C::KST, sv = g % C::VST;
+                        if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
+                        if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
+                        if (lane == 0) mbar_arrive_expect_tx(bar(C::B_KF + sk), C::KV_BYTES);
+                        if (lane == 1) mbar_arrive_expect_tx(bar(C::B_VF + sv), C::KV_BYTES);
+                        __syncwarp();
+                        constexpr int BOXES = C::SUB * (D / 64);  // boxes per K (or V) stage
+                        if (lane < 2 * BOXES) {
+                            const bool is_v = lane & 1;
+                            const int bx = lane >> 1, s = bx / (D / 64), dc = bx % (D / 64);
+                            const uint32_t dst = is_v ? tbase + C::V_OFF + sv * C::KV_BYTES
+                                                      : tbase + C::K_OFF + sk * C::KV_BYTES;
+                            tma_load_3d(dst + dc * C::KV_REGION + s * 8192, is_v ? &tmV : &tmK,
+                                        bar(is_v ? C::B_VF + sv : C::B_KF + sk), dc * 64, si.y[s], cur.bh);
+                        }
+                        ++k_arms[sk];
+                        ++v_arms[sv];
                     }
                     if (t == 1) {
                         decode_ahead();
