@@ -1203,15 +1203,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                 s1[i] = ((hi >> i) & 1u) ? s1[i] : -CUDART_INF_F;
                             }
                         }
-                        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+                        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            mx0 = fmaxf(mx0, s0[i]);
-                            mx1 = fmaxf(mx1, s0[i + 1]);
-                            mx2 = fmaxf(mx2, s1[i]);
-                            mx3 = fmaxf(mx3, s1[i + 1]);
+                            mx0 = fmax3(mx0, s0[i], s0[i + 1]);
+                            mx1 = fmax3(mx1, s1[i], s1[i + 1]);
                         }
-                        const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+                        const float m_new = fmaxf(m_ref, fmaxf(mx0, mx1) * sl2);
                         float fix = 1.f;  // factor for this row's first-half P (second half only)
                         if (m_new > m_ref + kRescaleLog2) {
                             const float a = ex2(m_ref - m_new);  // 0 when m_ref was -inf
@@ -1242,23 +1240,29 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                             tmem_st32u(sa, q);
                         }
                         const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
-                        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+                        // s * scale - m on element pairs, exponentials, pair sums
+                        const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
+                        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            const float p0 = ex2(fmaf(s0[i], sl2, neg_m));
-                            const float p1 = ex2(fmaf(s0[i + 1], sl2, neg_m));
-                            const float p2 = ex2(fmaf(s1[i], sl2, neg_m));
-                            const float p3 = ex2(fmaf(s1[i + 1], sl2, neg_m));
-                            ls0 += p0;
-                            ls1 += p1;
-                            ls2 += p2;
-                            ls3 += p3;
+                            float p0, p1, p2, p3;
+                            f2_unpack(f2_fma(f2_pack(s0[i], s0[i + 1]), sc2, nm2), p0, p1);
+                            f2_unpack(f2_fma(f2_pack(s1[i], s1[i + 1]), sc2, nm2), p2, p3);
+                            p0 = ex2(p0);
+                            p1 = ex2(p1);
+                            p2 = ex2(p2);
+                            p3 = ex2(p3);
+                            acc0 = f2_add(acc0, f2_pack(p0, p1));
+                            acc1 = f2_add(acc1, f2_pack(p2, p3));
                             __nv_bfloat162 b01 = __floats2bfloat162_rn(p0, p1);
                             __nv_bfloat162 b23 = __floats2bfloat162_rn(p2, p3);
                             pk[i >> 1] = *reinterpret_cast<uint32_t *>(&b01);
                             pk[16 + (i >> 1)] = *reinterpret_cast<uint32_t *>(&b23);
                         }
-                        lsum += (ls0 + ls1) + (ls2 + ls3);
+                        float a0x, a0y, a1x, a1y;
+                        f2_unpack(acc0, a0x, a0y);
+                        f2_unpack(acc1, a1x, a1y);
+                        lsum += (a0x + a0y) + (a1x + a1y);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) pk[i] = 0u;
