@@ -16,9 +16,11 @@ Sources (web pages on block-sparse long-sequence attention):
   * The BigBird blog summary (Sec. 2.1-2.3, Sec. 4): random, window and global
     components restated where the paper's own Sec. 2 text is garbled.
   * "Longformer: The Long-Document Transformer" (Beltagy et al.): sliding
-    window and symmetric global attention (Sec. 3.1), scaled dot-product
-    attention (Sec. 3.1, Eq. 1), and the slow per-diagonal "loop" variant used
-    only for testing (Sec. 3.2, App. A), whose role this oracle plays.
+    window and symmetric global attention (Sec. 3.1), the dilated sliding
+    window (Sec. 3.1, Fig. 2(c); per-head dilation, Tab. 12), the
+    autoregressive mode (App. B), scaled dot-product attention (Sec. 3.1,
+    Eq. 1), and the slow per-diagonal "loop" variant used only for testing
+    (Sec. 3.2, App. A), whose role this oracle plays.
 
 Every function pinned by a test that does not reuse this code; the pins are in
 ``tests/test_oracle.py`` and ``tests/golden/``. Parity status per function:
@@ -28,7 +30,10 @@ Every function pinned by a test that does not reuse this code; the pins are in
   bigbird_allowed          pinned (pure-Python enumeration, closed-form pair
                            counts, coverage => full attention)
   longformer_allowed       pinned (pure-Python enumeration, band/global
-                           invariants, closed-form pair count)
+                           invariants, closed-form pair counts; dilation and
+                           causal mode: enumeration of the window positions,
+                           torch is_causal attention, per-residue-class full
+                           attention, hand-derived pair counts)
   masked_attention         pinned (torch float64 scaled_dot_product_attention
                            on full/block-diagonal/truncated cases, scalar-loop
                            brute force, single-key and row-sum identities)

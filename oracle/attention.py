@@ -70,19 +70,29 @@ def bigbird_allowed(n, b, g, w, rand_row, rows=None):
     return blk[rows[:, None] // b, cols[None, :] // b]
 
 
-def longformer_allowed(n, window, global_idx, rows=None):
+def longformer_allowed(n, window, global_idx, rows=None, dilation=0, causal=False):
     """Longformer mask, bool [len(rows), n] (Longformer Sec. 3.1).
 
     Token i sees token j when i or j carries global attention (symmetric: a
-    global token attends all tokens and all tokens attend it), or when
-    |i - j| <= window // 2 (window / 2 tokens on each side, clipped at the ends).
+    global token attends all tokens and all tokens attend it), or when j lies in
+    i's sliding window: window // 2 positions on each side, clipped at the ends.
+    Dilated sliding window (Sec. 3.1, Fig. 2(c)): the window has gaps of size
+    `dilation` between attended positions, so the positions are i + k (dilation
+    + 1) for |k| <= window // 2 (dilation 0 is the plain window, as in Tab. 12).
+    Autoregressive mode (App. B: each token attends to previous tokens only):
+    with `causal`, nothing with j > i is allowed, global tokens included.
     """
     rows = np.arange(n) if rows is None else np.asarray(rows)
     cols = np.arange(n)
     is_global = np.zeros(n, dtype=bool)
     is_global[np.asarray(global_idx, dtype=np.int64)] = True
-    band = np.abs(rows[:, None] - cols[None, :]) <= window // 2
-    return band | is_global[rows][:, None] | is_global[None, :]
+    stride = int(dilation) + 1
+    diff = rows[:, None] - cols[None, :]  # i - j
+    band = (np.abs(diff) <= (window // 2) * stride) & (diff % stride == 0)
+    allowed = band | is_global[rows][:, None] | is_global[None, :]
+    if causal:
+        allowed &= diff >= 0
+    return allowed
 
 
 # ---------------------------------------------------------------------------
@@ -154,20 +164,28 @@ def oracle_bigbird(Q, K, V, b, g, w, rand_table, key_mask=None, rows=None,
 
 
 def oracle_longformer(Q, K, V, window, global_idx, key_mask=None, rows=None,
-                      row_chunk=1024):
-    """Longformer sliding-window + global attention forward, float64."""
+                      row_chunk=1024, dilation=None, causal=False):
+    """Longformer sliding-window + global attention forward, float64.
+
+    ``dilation``: per-head dilation [H] (None: 0 for every head); ``causal``:
+    autoregressive mode. See ``longformer_allowed``.
+    """
     Q, K, V = _as_f64(Q), _as_f64(K), _as_f64(V)
     B, H, n, d = Q.shape
+    dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
     rows = np.arange(n) if rows is None else np.asarray(rows)
     out = np.zeros((B, H, len(rows), d), dtype=np.float64)
     for beta in range(B):
         kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
         for c0 in range(0, len(rows), row_chunk):
             rr = rows[c0:c0 + row_chunk]
-            mask = _apply_validity(longformer_allowed(n, window, global_idx, rr), rr, kv)
+            masks = {}
             for h in range(H):
+                if dil[h] not in masks:
+                    masks[dil[h]] = _apply_validity(
+                        longformer_allowed(n, window, global_idx, rr, dilation=dil[h], causal=causal), rr, kv)
                 out[beta, h, c0:c0 + len(rr)] = masked_attention(
-                    Q[beta, h, rr], K[beta, h], V[beta, h], mask)
+                    Q[beta, h, rr], K[beta, h], V[beta, h], masks[dil[h]])
     return out
 
 
@@ -192,12 +210,15 @@ def bigbird_attended_pairs(n, b, g, w, rand_table, key_mask=None, B=1):
     return total
 
 
-def longformer_attended_pairs(n, window, global_idx, key_mask=None, B=1, H=1):
+def longformer_attended_pairs(n, window, global_idx, key_mask=None, B=1, H=1, dilation=None,
+                              causal=False):
+    dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
     total = 0
-    for beta in range(B):
-        kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
-        for c0 in range(0, n, 1024):
-            rr = np.arange(c0, min(n, c0 + 1024))
-            total += int(_apply_validity(
-                longformer_allowed(n, window, global_idx, rr), rr, kv).sum())
-    return total * H
+    for h in range(H):
+        for beta in range(B):
+            kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+            for c0 in range(0, n, 1024):
+                rr = np.arange(c0, min(n, c0 + 1024))
+                total += int(_apply_validity(
+                    longformer_allowed(n, window, global_idx, rr, dilation=dil[h], causal=causal), rr, kv).sum())
+    return total

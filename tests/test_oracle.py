@@ -239,6 +239,74 @@ def test_longformer_matches_sdpa_with_band_mask():
     np.testing.assert_allclose(out[0, 0], _sdpa(Q[0, 0], K[0, 0], V[0, 0], mask=band), rtol=0, atol=1e-12)
 
 
+# ------------------------------------------------- Longformer dilation / causal
+
+@pytest.mark.parametrize("dilation,causal", [(0, True), (1, False), (2, True), (3, False)])
+def test_longformer_dilated_causal_mask_by_enumeration(dilation, causal):
+    # pure-Python enumeration of the window positions i + k (dilation + 1)
+    n, window = 70, 8
+    G = [4, 33]
+    m = longformer_allowed(n, window, G, dilation=dilation, causal=causal)
+    for i in range(n):
+        seen = set()
+        for k in range(-(window // 2), window // 2 + 1):
+            j = i + k * (dilation + 1)
+            if 0 <= j < n:
+                seen.add(j)
+        if i in G:
+            seen = set(range(n))
+        seen |= set(G)
+        if causal:
+            seen = {j for j in seen if j <= i}
+        assert set(np.nonzero(m[i])[0].tolist()) == seen, (i, dilation, causal)
+
+
+def test_longformer_causal_wide_window_matches_sdpa_is_causal():
+    # every previous token in reach: plain causal attention (library routine)
+    B, H, n, d = 1, 1, 160, 16
+    Q, K, V = _rand((B, H, n, d), 20), _rand((B, H, n, d), 21), _rand((B, H, n, d), 22)
+    out = oracle_longformer(Q, K, V, 2 * n, [], causal=True)
+    q, k, v = (torch.as_tensor(x[0, 0]) for x in (Q, K, V))
+    ref = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True).numpy()[0]
+    np.testing.assert_allclose(out[0, 0], ref, rtol=0, atol=1e-12)
+
+
+def test_longformer_wide_dilated_window_splits_into_residue_classes():
+    # a dilated window reaching every position of its residue class is full
+    # attention within each class i mod (dilation + 1), computed here class by class
+    B, H, n, d, dil = 1, 2, 150, 16, 2
+    Q, K, V = _rand((B, H, n, d), 23), _rand((B, H, n, d), 24), _rand((B, H, n, d), 25)
+    out = oracle_longformer(Q, K, V, 2 * n, [], dilation=[dil, dil])
+    s = dil + 1
+    for h in range(H):
+        for r in range(s):
+            idx = np.arange(r, n, s)
+            ref = _sdpa(Q[0, h, idx], K[0, h, idx], V[0, h, idx])
+            np.testing.assert_allclose(out[0, h, idx], ref, rtol=0, atol=1e-12)
+
+
+def test_longformer_dilated_pair_counts_closed_form():
+    # no globals: sum over k in [-w/2, w/2] of the tokens i with 0 <= i + k s < n
+    n, window = 64, 8
+    for dil, causal in [(1, False), (1, True), (3, False)]:
+        s = dil + 1
+        ks = range(0, window // 2 + 1) if causal else range(-(window // 2), window // 2 + 1)
+        expect = sum(max(0, n - abs(k) * s) for k in ks)
+        assert longformer_attended_pairs(n, window, [], dilation=[dil], causal=causal) == expect
+    # the numbers for (dilation 1, plain) and (dilation 1, causal), by hand:
+    assert longformer_attended_pairs(n, window, [], dilation=[1]) == 536
+    assert longformer_attended_pairs(n, window, [], dilation=[1], causal=True) == 300
+
+
+def test_longformer_causal_globals_only_see_the_past():
+    n, window = 50, 4
+    G = [10, 30]
+    m = longformer_allowed(n, window, G, causal=True)
+    assert not np.triu(m, 1).any(), "nothing above the diagonal"
+    assert m[30, :31].all() and not m[30, 31:].any()
+    assert m[40, 10] and m[40, 30] and not m[5, 10]
+
+
 # ------------------------------------------------------------ softmax core
 
 def test_softmax_rows_sum_to_one_and_single_key():
