@@ -76,10 +76,13 @@ def bigbird_attn_fwd(Q, K, V, b, g, w, r, rand_idx, key_mask=None, out=None, str
     return out
 
 
-def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, stream=None):
+def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, stream=None, dilation=None,
+                        causal=False):
     """Longformer sliding-window + global attention forward; returns O.
 
     global_idx: int32 CUDA tensor of sorted unique positions (may be empty or None).
+    dilation: int32 CUDA tensor [H] of per-head dilations, or None (all 0).
+    causal: autoregressive mode (no key after the query).
     """
     _check_qkv(Q, K, V)
     B, H, n, d = Q.shape
@@ -92,11 +95,14 @@ def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, st
     if key_mask is not None and (not key_mask.is_cuda or key_mask.dtype != torch.uint8
                                  or not key_mask.is_contiguous()):
         raise ValueError("key_mask must be a contiguous uint8 CUDA tensor")
-    st = _lib.lib().longformer_attn_fwd(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, n, d, window,
+    if dilation is not None and (not dilation.is_cuda or dilation.dtype != torch.int32
+                                 or not dilation.is_contiguous() or dilation.numel() != H):
+        raise ValueError("dilation must be a contiguous int32 CUDA tensor with one entry per head")
+    st = _lib.lib().longformer_attn_fwd_ex(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, n, d, window, _ptr(dilation), 1 if causal else 0,
         _ptr(global_idx if n_global else None), n_global, _ptr(key_mask), _DTYPE[Q.dtype],
         _stream_handle(stream, Q.device))
-    _lib.check(st, "longformer_attn_fwd")
+    _lib.check(st, "longformer_attn_fwd_ex")
     return out
 
 

@@ -38,6 +38,7 @@ SIGNATURES = {
     "build_bigbird_pattern": (_I, [ctypes.c_uint64, _I, _I, _I, _I, _I, _I, _VP]),
     "bigbird_attn_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _I, _VP]),
     "longformer_attn_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP]),
+    "longformer_attn_fwd_ex": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I, _VP]),
     "sa_bigbird_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "sa_longformer_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "sa_set_workspace": (_I, [_VP, ctypes.c_size_t]),

@@ -195,7 +195,15 @@ sa_status bigbird_attn_fwd(const void *Q, const void *K, const void *V, void *O,
 sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
                               int window, const int32_t *global_idx, int n_global, const uint8_t *key_mask,
                               sa_dtype dtype, sa_stream_t stream) {
+    return longformer_attn_fwd_ex(Q, K, V, O, B, H, n, d, window, nullptr, 0, global_idx, n_global, key_mask,
+                                  dtype, stream);
+}
+
+sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
+                                 int window, const int32_t *dilation, int causal, const int32_t *global_idx,
+                                 int n_global, const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream) {
     if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
     sa_status s = check_tensors(Q, K, V, O);
     if (s != SA_OK) return s;
     s = longformer_args_ok(B, H, n, d, window, global_idx, n_global);
@@ -207,6 +215,8 @@ sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void 
     p.window = window;
     p.global_idx = n_global > 0 ? global_idx : nullptr;
     p.n_global = n_global;
+    p.dilation = dilation;
+    p.causal = causal;
     p.key_mask = key_mask;
     return run(p, dtype, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -11,6 +11,9 @@ namespace sa {
 enum PatternKind { kBigBird = 0, kLongformer = 1 };
 
 // Device status bits latched by kernels (OR-ed into the per-device word).
+// Largest accepted Longformer dilation (window stride dilation + 1 <= 64).
+constexpr int kMaxDilation = 63;
+
 enum DeviceStatusBits : unsigned int {
     kDevTimeout = 1u << 0,
     kDevBadIndex = 1u << 1,
@@ -29,6 +32,8 @@ struct Problem {
     int window;
     const int32_t *global_idx;
     int n_global;
+    const int32_t *dilation;  // device [H] or NULL (dilated sliding window)
+    int causal;               // autoregressive mode
     // both
     const uint8_t *key_mask;
     unsigned int *status;  // device status word

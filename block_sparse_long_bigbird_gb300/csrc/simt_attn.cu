@@ -238,7 +238,9 @@ __global__ void __launch_bounds__(kThreads) bigbird_simt_kernel(Problem p) {
 // ---------------------------------------------------------------- Longformer
 // One CTA = 64 query rows [i0, i0 + 64) of one (batch, head). Chunks needed:
 // all of them if a row is global, else those meeting the clipped band
-// [i0 - half, i0 + 63 + half] plus those holding a global key.
+// [i0 - reach, i0 + 63 + reach] plus those holding a global key, where
+// reach = (window / 2) (dilation + 1) ("Longformer", Sec. 3.1: dilated
+// window); the causal mode (App. B) drops everything after the query.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
     constexpr int BQ = 64;
@@ -251,6 +253,15 @@ __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
     const int n = p.n;
     const int nch = (n + kChunk - 1) / kChunk;
     const int half = p.window / 2;
+    // this head's window stride (dilation + 1); out-of-range dilations latch
+    int dil = p.dilation ? p.dilation[bh % p.H] : 0;
+    if (dil < 0 || dil > kMaxDilation) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, kDevBadIndex);
+        dil = 0;
+    }
+    const int stride = dil + 1;
+    const int reach = (int)min((long long)half * stride, (long long)n);
+    const bool causal = p.causal != 0;
     const size_t head_off = (size_t)bh * n * D;
     const T *Qh = static_cast<const T *>(p.Q) + head_off;
     const T *Kh = static_cast<const T *>(p.K) + head_off;
@@ -282,8 +293,9 @@ __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
     __syncthreads();
     const bool tile_has_global = (misc[0] | misc[1]) != 0u;
     {
-        const int lo = tile_has_global ? 0 : max(0, i0 - half) / kChunk;
-        const int hi = tile_has_global ? nch - 1 : min(n - 1, i0 + BQ - 1 + half) / kChunk;
+        const int lo = tile_has_global ? 0 : max(0, i0 - reach) / kChunk;
+        const int hi = causal ? min(n - 1, i0 + BQ - 1) / kChunk
+                              : (tile_has_global ? nch - 1 : min(n - 1, i0 + BQ - 1 + reach) / kChunk);
         for (int c = lo + threadIdx.x; c <= hi; c += kThreads) atomicOr(&bmap[c >> 5], 1u << (c & 31));
     }
     load_q_tile<T, D, BQ>(Qh, i0, n, sm);
@@ -336,7 +348,9 @@ __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
                 if (!qvalid[rr] || !kvalid[kl]) return false;
                 const unsigned gbit = ((kl < 32 ? gk0 : gk1) >> (kl & 31)) & 1u;
                 const int i = i0 + row0 + rr;
-                return qglobal[rr] || gbit != 0u || abs(i - key) <= half;
+                if (causal && key > i) return false;
+                const int dk = i - key;
+                return qglobal[rr] || gbit != 0u || (abs(dk) <= reach && dk % stride == 0);
             });
             __syncthreads();
         }

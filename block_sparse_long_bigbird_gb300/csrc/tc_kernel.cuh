@@ -145,6 +145,7 @@ struct Geometry {
     int total_units;
     int ng;               // Longformer: entries of the global list
     int nkb;              // Longformer: 64-key blocks, ceil(n / 64)
+    int causal;           // Longformer: autoregressive mode
     float scale_log2;
     unsigned long long wait_ns;
 };
@@ -166,6 +167,7 @@ struct Params {
     // global key (gpre[kb], gpre[nkb] = total) and those blocks in order
     // (glist); all three written by longformer_prep before the main kernel.
     const __nv_bfloat16 *Q;
+    const int32_t *dilation;  // Longformer: per-head dilation [H] or NULL
     const int32_t *gidx;
     const unsigned long long *gbits;
     const int *gpre;
@@ -563,13 +565,23 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && km[ui.q0 + t] != 0;
                         any_row = __any_sync(kFull, a);
                     }
-                    const int blo = max(0, ui.q0 - G.half) >> 6;
-                    const int bhi = min(G.n - 1, ui.q0 + kBM - 1 + G.half) >> 6;
+                    // this head's window stride (dilation + 1) and reach
+                    int dil = p.dilation ? __ldg(p.dilation + ui.bh % G.H) : 0;
+                    if (dil < 0 || dil > kMaxDilation) {
+                        if (lane == 0) atomicOr(p.status, kDevBadIndex);
+                        dil = 0;
+                    }
+                    const int reach = (int)min((long long)G.half * (dil + 1), (long long)G.n);
+                    ui.pad[1] = dil + 1;
+                    ui.pad[2] = reach;
+                    const int blo = max(0, ui.q0 - reach) >> 6;
+                    const int bhi = min(G.n - 1, ui.q0 + kBM - 1 + (G.causal ? 0 : reach)) >> 6;
                     int before = 0, after0 = 0, after = 0;
                     if (G.ng > 0) {
                         before = __ldg(p.gpre + blo);
                         after0 = __ldg(p.gpre + bhi + 1);
-                        after = __ldg(p.gpre + G.nkb) - after0;
+                        // causal: blocks after the band hold only keys after every row
+                        after = G.causal ? 0 : __ldg(p.gpre + G.nkb) - after0;
                     }
                     ui.j0 = blo;
                     ui.j1 = bhi;
@@ -1102,6 +1114,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 }
             }
             const bool row_valid = qpos < G.n && (!PADDED || p.key_mask[(size_t)beta * G.n + qpos] != 0);
+            // Longformer band units: window stride, reach and the stride pattern
+            // (bits 0, s, 2s, ... of a 64-key block)
+            int lstride = 1, lreach = G.half;
+            uint64_t lpat = ~0ull;
+            if (LF && ui.step0 < 0) {
+                lstride = ui.pad[1];
+                lreach = ui.pad[2];
+                lpat = 1ull;  // bits 0, s, 2s, ...: doubled until the word is full
+                for (int sh = lstride; sh < 64; sh *= 2) lpat |= lpat << sh;
+            }
             Pend cur;
             cur.kind = ui.kind;
             cur.bh = ui.bh;
@@ -1179,11 +1201,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                             uint64_t kmh = 0ull;
                             if (row_valid) {
                                 const int yh = half ? y1 : y0;
-                                const uint64_t bandm = ((bandb >> half) & 1u)
-                                                           ? bits_below(qpos + G.half - yh + 1) &
-                                                                 ~bits_below(qpos - G.half - yh)
-                                                           : 0ull;
+                                uint64_t bandm = 0ull;
+                                if ((bandb >> half) & 1u) {
+                                    bandm = bits_below(qpos + (G.causal ? 0 : lreach) - yh + 1) &
+                                            ~bits_below(qpos - lreach - yh);
+                                    if (lstride > 1) {  // dilated: keys k with k = qpos (mod stride)
+                                        const int c0 = ((qpos - yh) % lstride + lstride) % lstride;
+                                        bandm &= lpat << c0;
+                                    }
+                                }
                                 kmh = (half ? km1 : km0) & ((half ? gm1 : gm0) | bandm);
+                                if (G.causal) kmh &= bits_below(qpos - yh + 1);  // nothing after the query
                             }
                             if (!__all_sync(kFull, kmh == ~0ull)) {
                                 const uint32_t lo = (uint32_t)kmh, hi = (uint32_t)(kmh >> 32);

@@ -74,6 +74,7 @@ Geometry longformer_geometry(const Problem &p, const TcConfig &cfg) {
     G.half = p.window / 2 < p.n ? p.window / 2 : p.n;  // |i - k| < n always: a wider window changes nothing
     G.tiles = (p.n + kBM - 1) / kBM;
     G.ng = p.n_global;
+    G.causal = p.causal;
     G.gtiles = (p.n_global + kBM - 1) / kBM;
     G.nkb = (p.n + 63) / 64;
     const int kb = keys_per_step(p.d), target_steps = kTargetChunkKeys / kb;
@@ -139,6 +140,7 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
     prm.status = p.status;
     prm.Q = static_cast<const __nv_bfloat16 *>(p.Q);
     prm.gidx = p.global_idx;
+    prm.dilation = p.dilation;
     unsigned long long *gbits = reinterpret_cast<unsigned long long *>(base + L.gbits);
     int *gpre = reinterpret_cast<int *>(base + L.gpre);
     int *glist = reinterpret_cast<int *>(base + L.glist);

@@ -136,6 +136,31 @@ sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void 
                               const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
 
 /*
+ * longformer_attn_fwd_ex - longformer_attn_fwd with the dilated sliding window
+ * and the autoregressive mode.
+ *
+ * Source: "Longformer", Sec. 3.1 and Fig. 2(c) (dilated sliding window: gaps
+ * of size `dilation` between the window positions; per-head dilation as in
+ * Tab. 12, where dilation 0 is the plain window) and App. B (autoregressive
+ * mode: each token attends to previous tokens only).
+ *
+ * Token i sees token j iff (i or j is global, or j = i + k (dilation[h] + 1)
+ * for some |k| <= window / 2) and, when `causal` is nonzero, j <= i (global
+ * tokens included: nothing after the query is ever seen).
+ *
+ * dilation: DEVICE int32 [H] or NULL (all heads 0). Values outside [0, 63]
+ *   latch SA_ERR_BAD_INDEX and are taken as 0.
+ * causal: 0 or 1.
+ * Other arguments, layout, ownership and errors: as for longformer_attn_fwd,
+ * which is this call with dilation NULL and causal 0.
+ */
+sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O,
+                                 int B, int H, int n, int d, int window,
+                                 const int32_t *dilation, int causal,
+                                 const int32_t *global_idx, int n_global,
+                                 const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
+
+/*
  * Scratch (workspace) sizing. The split-KV partials of the global rows and the
  * kernel's work counters need device scratch. By default the library allocates
  * it once per device (cudaMalloc, zeroed) and grows it on demand; a caller that

@@ -29,13 +29,16 @@ def gpu_bigbird(Q, K, V, b, g, w, r, table, key_mask=None, path="tc"):
     return O
 
 
-def gpu_longformer(Q, K, V, window, gidx, key_mask=None, path="tc"):
+def gpu_longformer(Q, K, V, window, gidx, key_mask=None, path="tc", dilation=None, causal=False):
     dev = torch.device("cuda:0")
     set_path(path)
     try:
         O = sa.longformer_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), window,
                                    None if gidx is None else gidx.to(dev),
-                                   None if key_mask is None else key_mask.to(dev))
+                                   None if key_mask is None else key_mask.to(dev),
+                                   dilation=None if dilation is None else
+                                   torch.as_tensor(dilation, dtype=torch.int32).to(dev),
+                                   causal=causal)
         torch.cuda.synchronize()
         assert sa.get_last_device_status() == 0
     finally:
@@ -76,15 +79,16 @@ def bigbird_case(B, H, n, d, b, g, w, r, dtype="bf16", sigma=1.0, cfg_id=50, key
 
 
 def longformer_case(B, H, n, d, window, gidx, dtype="bf16", cfg_id=60, key_mask=None, path="tc",
-                    rows=None, heads=None, tol=(2e-2, 2e-3), sigma=1.0):
+                    rows=None, heads=None, tol=(2e-2, 2e-3), sigma=1.0, dilation=None, causal=False):
     Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
-    O = gpu_longformer(Q, K, V, window, gidx, key_mask, path).float().cpu()
+    O = gpu_longformer(Q, K, V, window, gidx, key_mask, path, dilation, causal).float().cpu()
     heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
     g_np = np.zeros(0, dtype=np.int64) if gidx is None else gidx.numpy()
     for beta, h in heads:
         km = None if key_mask is None else key_mask[beta:beta + 1].numpy()
         ref = oracle_longformer(Q[beta:beta + 1, h:h + 1], K[beta:beta + 1, h:h + 1], V[beta:beta + 1, h:h + 1],
-                                window, g_np, key_mask=km, rows=rows)[0, 0]
+                                window, g_np, key_mask=km, rows=rows,
+                                dilation=None if dilation is None else [dilation[h]], causal=causal)[0, 0]
         got = O[beta, h].numpy() if rows is None else O[beta, h].numpy()[np.asarray(rows)]
         assert_close(got, ref, *tol, what=f"longformer beta={beta} h={h}")
         if key_mask is not None:

@@ -113,6 +113,20 @@ def test_longformer_invalid_args(lib, bad):
     assert _lf(lib, **bad) == 1
 
 
+def _lfx(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, O=FAKE + 0x300000, B=1, H=2, n=1024, d=64,
+             window=64, dil=FAKE + 0x500000, causal=1, gidx=FAKE + 0x400000, ng=4, km=None, dtype=0)
+    a.update(kw)
+    return lib.longformer_attn_fwd_ex(a["Q"], a["K"], a["V"], a["O"], a["B"], a["H"], a["n"], a["d"],
+                                      a["window"], a["dil"], a["causal"], a["gidx"], a["ng"], a["km"],
+                                      a["dtype"], None)
+
+
+@pytest.mark.parametrize("bad", [dict(causal=2), dict(causal=-1), dict(window=-2), dict(dtype=5), dict(V=None)])
+def test_longformer_ex_invalid_args(lib, bad):
+    assert _lfx(lib, **bad) == 1
+
+
 def test_workspace_and_option_entry_points(lib):
     assert lib.sa_bigbird_workspace_bytes(1, 1, 1000, 64, 64, 2) == 0  # invalid sizes
     assert lib.sa_set_option(999, 1) == 1

@@ -197,6 +197,53 @@ def test_longformer_wide_score_range(path, d):
     longformer_case(1, 2, 1000, d, 64, gidx, sigma=4.0, cfg_id=83, path=path, tol=WIDE_TOL)
 
 
+# ------------------------------------------------- Longformer dilation / autoregressive mode
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_dilated_per_head(path):
+    gidx = torch.tensor([0, 5, 500], dtype=torch.int32)
+    longformer_case(1, 4, 1000, 64, 64, gidx, path=path, dilation=[0, 1, 2, 3], cfg_id=85)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_longformer_causal_padded(path, d):
+    B, n = 2, 777
+    gidx = torch.tensor([3, 400], dtype=torch.int32)
+    km = make_key_mask(B, n, seed=31)
+    longformer_case(B, 2, n, d, 100, gidx, key_mask=km, path=path, dilation=[0, 2], causal=True, cfg_id=86)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_causal_no_globals(path):
+    longformer_case(1, 2, 1536, 64, 256, None, path=path, causal=True, cfg_id=87)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_dilation_two_heads_n4096(path):
+    # dilation on two heads only (Longformer Tab. 12), causal, sampled rows
+    H, n = 12, 4096
+    dil = [0] * H
+    dil[10], dil[11] = 2, 3
+    gidx = torch.arange(16, dtype=torch.int32)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([np.arange(0, 200), np.arange(n - 200, n), rng.choice(n, 300, replace=False)]))
+    longformer_case(1, H, n, 64, 512, gidx, path=path, rows=rows, heads=[(0, 0), (0, 10), (0, 11)],
+                    dilation=dil, causal=True, cfg_id=88)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bad_dilation_latches_status(path):
+    Q, K, V = (t.cuda() for t in make_qkv(1, 2, 512, 64, "bf16", cfg_id=72))
+    dil = torch.tensor([-1, 64], dtype=torch.int32).cuda()
+    sa.set_option(sa.SA_OPT_FORCE_SIMT, 1 if path == "simt" else 0)
+    try:
+        sa.longformer_attn_fwd(Q, K, V, 64, None, dilation=dil)
+        assert sa.get_last_device_status() == sa._lib.SA_ERR_BAD_INDEX
+    finally:
+        sa.set_option(sa.SA_OPT_FORCE_SIMT, 0)
+
+
 # ------------------------------------------------------------- full-size workloads (sampled rows)
 
 @pytest.mark.parametrize("path", PATHS)
