@@ -37,6 +37,12 @@ Every function pinned by a test that does not reuse this code; the pins are in
   masked_attention         pinned (torch float64 scaled_dot_product_attention
                            on full/block-diagonal/truncated cases, scalar-loop
                            brute force, single-key and row-sum identities)
+  masked_attention_grads,  pinned (central finite differences of the pinned
+  oracle_*_bwd             forward on tiny cases with padding, dilation and
+                           causal mode; torch float64 autograd through
+                           scaled_dot_product_attention with the same mask;
+                           shift invariance sum_j dK_j = 0 and sum_j dV_j =
+                           sum of dO over rows with an allowed key)
 """
 
 from .pattern import SplitMix64, splitmix64_stream, bigbird_random_table
@@ -47,6 +53,9 @@ from .attention import (
     masked_softmax_probs,
     oracle_bigbird,
     oracle_longformer,
+    masked_attention_grads,
+    oracle_bigbird_bwd,
+    oracle_longformer_bwd,
     bigbird_attended_pairs,
     longformer_attended_pairs,
 )
@@ -61,6 +70,9 @@ __all__ = [
     "masked_softmax_probs",
     "oracle_bigbird",
     "oracle_longformer",
+    "masked_attention_grads",
+    "oracle_bigbird_bwd",
+    "oracle_longformer_bwd",
     "bigbird_attended_pairs",
     "longformer_attended_pairs",
 ]

@@ -190,6 +190,96 @@ def oracle_longformer(Q, K, V, window, global_idx, key_mask=None, rows=None,
 
 
 # ---------------------------------------------------------------------------
+# Backward pass: gradients of the forward above
+# ---------------------------------------------------------------------------
+#
+# The pages train every model through this attention (BigBird App. E.1, MLM
+# pretraining; Longformer Sec. 5, continued MLM pretraining with gradient
+# updates) but print no backward formulas: the backward is the exact
+# derivative of the forward definition. For a loss L with upstream gradient
+# dO = dL/dO and the row-wise masked softmax P of the forward:
+#
+#     dV      = P^T dO                      (O = P V is linear in V)
+#     dP      = dO V^T
+#     D_i     = sum_j P_ij dP_ij            (= dO_i . O_i)
+#     dS_ij   = P_ij (dP_ij - D_i)          (softmax Jacobian on the allowed keys;
+#                                            P_ij = 0 off the mask, so dS_ij = 0 there)
+#     dQ      = dS K / sqrt(d),  dK = dS^T Q / sqrt(d)
+#
+# Rows without an allowed key (padded queries) have P_i = 0, hence zero
+# gradient, matching their constant zero output.
+
+def masked_attention_grads(q, k, v, mask, dout):
+    """(dq, dk, dv) of O = masked_attention(q, k, v, mask) for dL/dO = dout, float64.
+
+    q, dout: [m, d]; k, v: [n, d]; mask: bool [m, n].
+    """
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    scale = 1.0 / math.sqrt(q.shape[1])
+    p = masked_softmax_probs(q, k, mask)
+    dv = p.T @ dout
+    dp = dout @ v.T
+    rowdot = (p * dp).sum(axis=1)
+    ds = p * (dp - rowdot[:, None])
+    return scale * (ds @ k), scale * (ds.T @ q), dv
+
+
+def _grads_over_rows(Qh, Kh, Vh, dOh, mask_of_rows, n, row_chunk):
+    """Sum the per-row contributions to dK and dV over row chunks of one head
+    (dQ rows are independent); the chunks only bound memory."""
+    dQ = np.zeros_like(Qh)
+    dK = np.zeros_like(Kh)
+    dV = np.zeros_like(Vh)
+    for c0 in range(0, n, row_chunk):
+        rr = np.arange(c0, min(n, c0 + row_chunk))
+        dq, dk, dv = masked_attention_grads(Qh[rr], Kh, Vh, mask_of_rows(rr), dOh[rr])
+        dQ[rr] = dq
+        dK += dk
+        dV += dv
+    return dQ, dK, dV
+
+
+def oracle_bigbird_bwd(Q, K, V, dO, b, g, w, rand_table, key_mask=None, row_chunk=1024):
+    """Gradients (dQ, dK, dV), float64 [B, H, n, d], of the BigBird-ITC forward
+    ``oracle_bigbird`` for the upstream gradient dO [B, H, n, d]."""
+    Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
+    rand_table = np.asarray(rand_table)
+    B, H, n, d = Q.shape
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h in range(H):
+        blk = bigbird_block_allowed(n // b, g, w, rand_table[h])
+        for beta in range(B):
+            kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+
+            def mask_of_rows(rr):
+                return _apply_validity(blk[rr[:, None] // b, np.arange(n)[None, :] // b], rr, kv)
+
+            dQ[beta, h], dK[beta, h], dV[beta, h] = _grads_over_rows(
+                Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], mask_of_rows, n, row_chunk)
+    return dQ, dK, dV
+
+
+def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilation=None,
+                          causal=False, row_chunk=1024):
+    """Gradients (dQ, dK, dV), float64 [B, H, n, d], of ``oracle_longformer``."""
+    Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
+    B, H, n, d = Q.shape
+    dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h in range(H):
+        for beta in range(B):
+            kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+
+            def mask_of_rows(rr):
+                return _apply_validity(longformer_allowed(n, window, global_idx, rr, dilation=dil[h],
+                                                          causal=causal), rr, kv)
+
+            dQ[beta, h], dK[beta, h], dV[beta, h] = _grads_over_rows(
+                Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], mask_of_rows, n, row_chunk)
+    return dQ, dK, dV
+
+
+# ---------------------------------------------------------------------------
 # Work accounting: attended (valid query, allowed valid key) pairs
 # ---------------------------------------------------------------------------
 

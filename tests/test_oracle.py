@@ -382,3 +382,114 @@ def test_padded_pair_count_matches_mask():
             m = bigbird_allowed(n, b, g, w, t[h]) & valid[None, :] & valid[:, None]
             total += int(m.sum())
     assert bigbird_attended_pairs(n, b, g, w, t, key_mask=km, B=2) == total
+
+
+# ---------------------------------------------------------------------------
+# Backward pass: the oracle's gradients against the derivative's definition
+# (central finite differences of the pinned forward) and torch autograd.
+# ---------------------------------------------------------------------------
+
+def _central_diff_grads(fwd, Q, K, V, dO, eps=1e-5):
+    """d(sum(fwd(Q, K, V) * dO)) by central differences, one element at a time."""
+    grads = []
+    args = [Q.copy(), K.copy(), V.copy()]
+    for which in range(3):
+        x = args[which]
+        g = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = float((fwd(*args) * dO).sum())
+            x[idx] = old - eps
+            lm = float((fwd(*args) * dO).sum())
+            x[idx] = old
+            g[idx] = (lp - lm) / (2 * eps)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("padded", [False, True])
+def test_bigbird_grads_match_finite_differences(padded):
+    from oracle import oracle_bigbird_bwd
+    n, b, g, w, r, d = 16, 4, 1, 1, 1, 4
+    table = bigbird_random_table(3, 1, n, b, g, w, r)
+    Q, K, V, dO = (_rand((1, 1, n, d), s) for s in (11, 12, 13, 14))
+    km = None
+    if padded:
+        km = np.ones((1, n), dtype=np.uint8)
+        km[0, 13:] = 0
+    fwd = lambda q, k, v: oracle_bigbird(q, k, v, b, g, w, table, key_mask=km)
+    want = _central_diff_grads(fwd, Q, K, V, dO)
+    got = oracle_bigbird_bwd(Q, K, V, dO, b, g, w, table, key_mask=km)
+    for gw, gg, name in zip(want, got, "QKV"):
+        np.testing.assert_allclose(gg, gw, atol=1e-8, rtol=1e-6, err_msg=f"d{name}")
+    if padded:
+        assert np.all(got[0][0, 0, 13:] == 0) and np.all(got[1][0, 0, 13:] == 0) and np.all(got[2][0, 0, 13:] == 0)
+
+
+@pytest.mark.parametrize("dilation,causal,padded", [(0, False, False), (1, True, True), (2, False, True)])
+def test_longformer_grads_match_finite_differences(dilation, causal, padded):
+    from oracle import oracle_longformer_bwd
+    n, window, d = 12, 4, 4
+    gidx = np.array([2])
+    Q, K, V, dO = (_rand((1, 1, n, d), s) for s in (21, 22, 23, 24))
+    km = None
+    if padded:
+        km = np.ones((1, n), dtype=np.uint8)
+        km[0, 10:] = 0
+    fwd = lambda q, k, v: oracle_longformer(q, k, v, window, gidx, key_mask=km, dilation=[dilation], causal=causal)
+    want = _central_diff_grads(fwd, Q, K, V, dO)
+    got = oracle_longformer_bwd(Q, K, V, dO, window, gidx, key_mask=km, dilation=[dilation], causal=causal)
+    for gw, gg, name in zip(want, got, "QKV"):
+        np.testing.assert_allclose(gg, gw, atol=1e-8, rtol=1e-6, err_msg=f"d{name}")
+
+
+def _sdpa_grads(q, k, v, mask, dout):
+    """torch float64 autograd through scaled_dot_product_attention (library routine)."""
+    q, k, v = (torch.tensor(np.asarray(x, dtype=np.float64), requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(q[None], k[None], v[None],
+                                                         attn_mask=torch.as_tensor(mask))[0]
+    o.backward(torch.as_tensor(np.asarray(dout, dtype=np.float64)))
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+def test_bigbird_grads_match_torch_autograd():
+    from oracle import oracle_bigbird_bwd
+    n, b, g, w, r, d, H = 192, 16, 2, 3, 2, 16, 2
+    table = bigbird_random_table(5, H, n, b, g, w, r)
+    Q, K, V, dO = (_rand((1, H, n, d), s) for s in (31, 32, 33, 34))
+    got = oracle_bigbird_bwd(Q, K, V, dO, b, g, w, table, row_chunk=40)
+    for h in range(H):
+        mask = bigbird_allowed(n, b, g, w, table[h])
+        want = _sdpa_grads(Q[0, h], K[0, h], V[0, h], mask, dO[0, h])
+        for gw, gg in zip(want, got):
+            np.testing.assert_allclose(gg[0, h], gw, atol=1e-12, rtol=1e-9)
+
+
+@pytest.mark.parametrize("dilation,causal", [(0, False), (3, False), (1, True)])
+def test_longformer_grads_match_torch_autograd(dilation, causal):
+    from oracle import oracle_longformer_bwd
+    n, window, d = 160, 16, 8
+    gidx = np.array([0, 1, 77])
+    Q, K, V, dO = (_rand((1, 1, n, d), s) for s in (41, 42, 43, 44))
+    got = oracle_longformer_bwd(Q, K, V, dO, window, gidx, dilation=[dilation], causal=causal)
+    mask = longformer_allowed(n, window, gidx, dilation=dilation, causal=causal)
+    want = _sdpa_grads(Q[0, 0], K[0, 0], V[0, 0], mask, dO[0, 0])
+    for gw, gg in zip(want, got):
+        np.testing.assert_allclose(gg[0, 0], gw, atol=1e-12, rtol=1e-9)
+
+
+def test_grads_shift_invariance_and_value_sum():
+    """Adding one vector c to every key shifts each row's scores by a constant,
+    which the softmax ignores, so sum_j dK_j = 0; the rows of P sum to 1 (or are
+    0 for a row without keys), so sum_j dV_j = sum of dO over rows with a key."""
+    from oracle import oracle_bigbird_bwd
+    n, b, g, w, r, d = 256, 32, 1, 3, 2, 8
+    table = bigbird_random_table(9, 1, n, b, g, w, r)
+    Q, K, V, dO = (_rand((1, 1, n, d), s) for s in (51, 52, 53, 54))
+    km = np.ones((1, n), dtype=np.uint8)
+    km[0, 200:] = 0
+    dQ, dK, dV = oracle_bigbird_bwd(Q, K, V, dO, b, g, w, table, key_mask=km, row_chunk=100)
+    np.testing.assert_allclose(dK[0, 0].sum(axis=0), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dV[0, 0].sum(axis=0), dO[0, 0, :200].sum(axis=0), atol=1e-12)
+    assert np.all(dQ[0, 0, 200:] == 0) and np.all(dK[0, 0, 200:] == 0) and np.all(dV[0, 0, 200:] == 0)
