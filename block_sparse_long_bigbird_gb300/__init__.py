@@ -1,4 +1,4 @@
-"""GB300-native sparse long-sequence attention forward (BigBird-ITC and Longformer).
+"""GB300-native sparse long-sequence attention, forward and backward (BigBird-ITC and Longformer).
 
 Python binding of the C ABI declared in ``include/sparse_attn.h``. The names
 mirror the C entry points; the wrappers only marshal torch tensors (device
@@ -104,6 +104,60 @@ def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, st
         _stream_handle(stream, Q.device))
     _lib.check(st, "longformer_attn_fwd_ex")
     return out
+
+
+def _check_bwd(Q, K, V, dO):
+    _check_qkv(Q, K, V)
+    if not dO.is_cuda or not dO.is_contiguous() or dO.dtype != Q.dtype or dO.shape != Q.shape \
+            or dO.device != Q.device:
+        raise ValueError("dO must be a contiguous CUDA tensor shaped and typed like Q")
+
+
+def _grad_outputs(Q, out):
+    if out is None:
+        return torch.empty_like(Q), torch.empty_like(Q), torch.empty_like(Q)
+    dQ, dK, dV = out
+    for t in (dQ, dK, dV):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != Q.dtype or t.shape != Q.shape:
+            raise ValueError("gradient outputs must be contiguous CUDA tensors shaped and typed like Q")
+    return dQ, dK, dV
+
+
+def bigbird_attn_bwd(Q, K, V, dO, b, g, w, r, rand_idx, key_mask=None, out=None, stream=None):
+    """Gradients (dQ, dK, dV) of bigbird_attn_fwd at (Q, K, V) for the upstream gradient dO.
+
+    The pattern arguments are those of the forward call; out: optional (dQ, dK, dV) tensors.
+    """
+    _check_bwd(Q, K, V, dO)
+    B, H, n, d = Q.shape
+    dQ, dK, dV = _grad_outputs(Q, out)
+    st = _lib.lib().bigbird_attn_bwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), B, H, n, d, b, g, w, r,
+        _ptr(rand_idx), _ptr(key_mask), _DTYPE[Q.dtype], _stream_handle(stream, Q.device))
+    _lib.check(st, "bigbird_attn_bwd")
+    return dQ, dK, dV
+
+
+def longformer_attn_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilation=None, causal=False,
+                        out=None, stream=None):
+    """Gradients (dQ, dK, dV) of longformer_attn_fwd at (Q, K, V) for the upstream gradient dO."""
+    _check_bwd(Q, K, V, dO)
+    B, H, n, d = Q.shape
+    dQ, dK, dV = _grad_outputs(Q, out)
+    n_global = 0 if global_idx is None else int(global_idx.numel())
+    if dilation is not None and (not dilation.is_cuda or dilation.dtype != torch.int32
+                                 or not dilation.is_contiguous() or dilation.numel() != H):
+        raise ValueError("dilation must be a contiguous int32 CUDA tensor with one entry per head")
+    st = _lib.lib().longformer_attn_bwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), B, H, n, d, window,
+        _ptr(dilation), 1 if causal else 0, _ptr(global_idx if n_global else None), n_global, _ptr(key_mask),
+        _DTYPE[Q.dtype], _stream_handle(stream, Q.device))
+    _lib.check(st, "longformer_attn_bwd")
+    return dQ, dK, dV
+
+
+def attn_bwd_workspace_bytes(B, H, n, d):
+    return int(_lib.lib().sa_attn_bwd_workspace_bytes(B, H, n, d))
 
 
 def get_last_device_status(stream=None, device=None):

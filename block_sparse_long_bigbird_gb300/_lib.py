@@ -1,6 +1,6 @@
 """ctypes binding of ``libsparse_attn.so`` (the C ABI in include/sparse_attn.h).
 
-Argument marshalling only: every step of the attention forward runs in the
+Argument marshalling only: every step of the attention forward and backward runs in the
 library's CUDA kernels. There is no fallback: if the compiled library is
 missing, every call raises.
 """
@@ -39,6 +39,11 @@ SIGNATURES = {
     "bigbird_attn_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _I, _VP]),
     "longformer_attn_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP]),
     "longformer_attn_fwd_ex": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I, _VP]),
+    "bigbird_attn_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _I,
+                              _VP]),
+    "longformer_attn_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I,
+                                 _VP]),
+    "sa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "sa_bigbird_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "sa_longformer_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "sa_set_workspace": (_I, [_VP, ctypes.c_size_t]),

@@ -75,6 +75,8 @@ bool size_ok(int B, int H, int n, int d) {
     return true;
 }
 
+size_t bwd_stats_bytes(int B, int H, int n) { return 2 * sizeof(float) * (size_t)B * H * n; }
+
 sa_status bigbird_args_ok(int B, int H, int n, int d, int b, int g, int w, int r, const int32_t *rand_idx) {
     if (!size_ok(B, H, n, d)) return SA_ERR_INVALID_ARG;
     if (b != 64 && b != 128) return SA_ERR_INVALID_ARG;
@@ -169,6 +171,47 @@ sa_status run(const sa::Problem &prob_in, sa_dtype dtype, cudaStream_t stream) {
     return SA_OK;
 }
 
+// Backward: scratch holds the per-row statistics (2 * B * H * n floats) at
+// offset 0, so the forward's counters must be cleared before its next use.
+sa_status run_bwd(const sa::Problem &prob_in, sa_dtype dtype, cudaStream_t stream) {
+    int dev = 0;
+    DeviceState *st = nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    sa_status s = current_device(&dev, &st);
+    if (s != SA_OK) return s;
+    if (st->cc_major != 10 || st->cc_minor != 3) return SA_ERR_UNSUPPORTED;
+    sa::Problem prob = prob_in;
+    prob.status = st->status;
+    void *ws = nullptr;
+    const size_t need = bwd_stats_bytes(prob.B, prob.H, prob.n);
+    s = get_workspace(*st, need, &ws);
+    if (s != SA_OK) return s;
+    prob.row_stats = static_cast<float *>(ws);
+    size_t *clean = (ws == st->user_ws) ? &st->user_ws_clean : &st->ws_clean;
+    *clean = 0;
+    int launches = 0;
+    const cudaError_t e = sa::launch_simt_bwd(prob, dtype, stream, &launches);
+    if (e != cudaSuccess) return SA_ERR_CUDA;
+    g_last_launches = launches;
+    return SA_OK;
+}
+
+sa_status check_bwd_tensors(const void *Q, const void *K, const void *V, const void *dO, const void *dQ,
+                            const void *dK, const void *dV) {
+    const void *in[4] = {Q, K, V, dO};
+    const void *out[3] = {dQ, dK, dV};
+    for (const void *t : in)
+        if (!t || !aligned16(t)) return SA_ERR_INVALID_ARG;
+    for (int a = 0; a < 3; ++a) {
+        if (!out[a] || !aligned16(out[a])) return SA_ERR_INVALID_ARG;
+        for (const void *t : in)
+            if (out[a] == t) return SA_ERR_INVALID_ARG;
+        for (int b = 0; b < a; ++b)
+            if (out[a] == out[b]) return SA_ERR_INVALID_ARG;
+    }
+    return SA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -219,6 +262,55 @@ sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, vo
     p.causal = causal;
     p.key_mask = key_mask;
     return run(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sa_status bigbird_attn_bwd(const void *Q, const void *K, const void *V, const void *dO, void *dQ, void *dK,
+                           void *dV, int B, int H, int n, int d, int b, int g, int w, int r,
+                           const int32_t *rand_idx, const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    sa_status s = check_bwd_tensors(Q, K, V, dO, dQ, dK, dV);
+    if (s != SA_OK) return s;
+    s = bigbird_args_ok(B, H, n, d, b, g, w, r, rand_idx);
+    if (s != SA_OK) return s;
+    if (!aligned16(key_mask)) return SA_ERR_INVALID_ARG;
+    sa::Problem p = {};
+    p.kind = sa::kBigBird;
+    p.Q = Q; p.K = K; p.V = V;
+    p.dO = dO; p.dQ = dQ; p.dK = dK; p.dV = dV;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.b = b; p.g = g; p.w = w; p.r = r;
+    p.rand_idx = r > 0 ? rand_idx : nullptr;
+    p.key_mask = key_mask;
+    return run_bwd(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sa_status longformer_attn_bwd(const void *Q, const void *K, const void *V, const void *dO, void *dQ, void *dK,
+                              void *dV, int B, int H, int n, int d, int window,
+                              const int32_t *dilation, int causal, const int32_t *global_idx, int n_global,
+                              const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+    sa_status s = check_bwd_tensors(Q, K, V, dO, dQ, dK, dV);
+    if (s != SA_OK) return s;
+    s = longformer_args_ok(B, H, n, d, window, global_idx, n_global);
+    if (s != SA_OK) return s;
+    sa::Problem p = {};
+    p.kind = sa::kLongformer;
+    p.Q = Q; p.K = K; p.V = V;
+    p.dO = dO; p.dQ = dQ; p.dK = dK; p.dV = dV;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.window = window;
+    p.global_idx = n_global > 0 ? global_idx : nullptr;
+    p.n_global = n_global;
+    p.dilation = dilation;
+    p.causal = causal;
+    p.key_mask = key_mask;
+    return run_bwd(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sa_attn_bwd_workspace_bytes(int B, int H, int n, int d) {
+    if (!size_ok(B, H, n, d)) return 0;
+    return bwd_stats_bytes(B, H, n);
 }
 
 size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g) {

@@ -37,10 +37,20 @@ struct Problem {
     // both
     const uint8_t *key_mask;
     unsigned int *status;  // device status word
+    // backward only: dO is the upstream gradient; row_stats holds 2 * B * H * n
+    // floats of scratch (per-row log2-domain log-sum-exp, then per-row
+    // D = sum_j P_ij dO_i . V_j).
+    const void *dO;
+    void *dQ, *dK, *dV;
+    float *row_stats;
 };
 
 // Exact SIMT kernels (fp32 arithmetic; bf16 or fp32 storage).
 cudaError_t launch_simt(const Problem &p, sa_dtype dtype, cudaStream_t stream, int *launches);
+
+// Exact SIMT backward (two launches: row pass for dQ and the row statistics,
+// then key pass for dK and dV).
+cudaError_t launch_simt_bwd(const Problem &p, sa_dtype dtype, cudaStream_t stream, int *launches);
 
 // Tensor-core (tcgen05/TMEM/TMA) kernels for bf16.
 struct TcConfig {

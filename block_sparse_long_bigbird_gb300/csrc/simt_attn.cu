@@ -16,6 +16,7 @@
 #include <math_constants.h>
 
 #include "internal.h"
+#include "simt_common.cuh"
 
 namespace sa {
 namespace {
@@ -23,33 +24,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 64;  // keys staged per step
-constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void store_val(float *p, float v) { *p = v; }
-__device__ __forceinline__ void store_val(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
-
-// First index t in sorted idx[0..cnt) with idx[t] >= key.
-__device__ __forceinline__ int lower_bound_i32(const int32_t *idx, int cnt, int key) {
-    int lo = 0, hi = cnt;
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if (idx[mid] < key) lo = mid + 1; else hi = mid;
-    }
-    return lo;
-}
+using simt::kFull;
+using simt::lower_bound_i32;
+using simt::store_val;
+using simt::to_f32;
+using simt::warp_max;
+using simt::warp_sum;
 
 // Shared-memory layout of one CTA (float offsets).
 template <int D, int BQ>

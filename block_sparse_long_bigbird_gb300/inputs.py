@@ -9,6 +9,8 @@ Longformer paper Sec. 3 train on text that is out of scope here):
   * Q, K, V: ``torch.randn(B, H, n, d)`` in float32 from three CPU generators
     seeded ``1000 + 10 * cfg + {0, 1, 2}``, scaled by ``sigma``, then cast
     (round-to-nearest-even) to the working dtype.
+  * Upstream gradient dO (backward): ``torch.randn(B, H, n, d)`` from a CPU
+    generator seeded ``5000 + 10 * cfg``, cast like Q, K, V.
   * Key padding: per-sequence valid lengths ``L ~ U{n/2, ..., n}`` from a CPU
     generator seeded 2000; ``key_mask[beta, t] = t < L[beta]``.
   * BigBird random table: drawn by ``build_bigbird_pattern`` from seed 0.
@@ -30,6 +32,14 @@ def make_qkv(B, H, n, d, dtype="bf16", sigma=1.0, cfg_id=0):
             x = x * sigma
         out.append(x.to(DTYPES[dtype]).contiguous())
     return tuple(out)
+
+
+def make_grad_out(B, H, n, d, dtype="bf16", cfg_id=0):
+    """Return a CPU tensor dO of shape [B, H, n, d] in ``dtype`` (upstream gradient)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(5000 + 10 * cfg_id)
+    x = torch.randn(B, H, n, d, generator=gen, dtype=torch.float32)
+    return x.to(DTYPES[dtype]).contiguous()
 
 
 def make_lengths(B, n, seed=2000, low=None):

@@ -161,6 +161,58 @@ sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, vo
                                  const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
 
 /*
+ * bigbird_attn_bwd - gradients of bigbird_attn_fwd.
+ *
+ * Source: the pages train through this attention ("Big Bird", App. E.1, MLM
+ * pretraining; "Longformer", Sec. 5, pretraining with gradient updates) but
+ * print no backward formulas; this is the exact derivative of the forward
+ * above at (Q, K, V). With P the forward's masked softmax (P_ij = 0 outside
+ * N(i)) and dO the upstream gradient dL/dO:
+ *
+ *     D_i = sum_j P_ij (dO_i . V_j),   dS_ij = P_ij (dO_i . V_j - D_i),
+ *     dQ = dS K / sqrt(d),   dK = dS^T Q / sqrt(d),   dV = P^T dO.
+ *
+ * P and D are recomputed from Q, K, V and dO in fp32, so the forward's
+ * output O is not an argument: the result does not depend on how O was
+ * rounded.
+ *
+ * Q, K, V, dO: DEVICE [B][H][n][d] inputs; dQ, dK, dV: DEVICE [B][H][n][d]
+ *   outputs, all of one dtype, contiguous, 16-byte aligned. The outputs must
+ *   not alias an input or each other. Every element of the outputs is
+ *   written: padded queries get dQ = 0, padded keys dK = dV = 0.
+ * Other arguments: as for bigbird_attn_fwd (same pattern, same rand_idx and
+ *   key_mask as the forward call).
+ * Arithmetic: fp32 softmax statistics and accumulation (bf16 inputs are
+ *   widened exactly; outputs are rounded to the storage dtype).
+ *   Deterministic: no atomics; every sum runs in a fixed order.
+ * Scratch: 2 * B * H * n floats of per-row statistics in the workspace
+ *   (sa_attn_bwd_workspace_bytes).
+ * Errors: as for bigbird_attn_fwd, plus SA_ERR_INVALID_ARG when an output
+ *   aliases an input or another output.
+ */
+sa_status bigbird_attn_bwd(const void *Q, const void *K, const void *V, const void *dO,
+                           void *dQ, void *dK, void *dV,
+                           int B, int H, int n, int d, int b, int g, int w, int r,
+                           const int32_t *rand_idx, const uint8_t *key_mask,
+                           sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * longformer_attn_bwd - gradients of longformer_attn_fwd_ex (sliding window,
+ * dilation, autoregressive mode, symmetric global attention).
+ *
+ * Formulas, tensors, numerics, scratch and errors as for bigbird_attn_bwd;
+ * the pattern arguments (window, dilation, causal, global_idx, n_global,
+ * key_mask) are those of longformer_attn_fwd_ex and must match the forward
+ * call.
+ */
+sa_status longformer_attn_bwd(const void *Q, const void *K, const void *V, const void *dO,
+                              void *dQ, void *dK, void *dV,
+                              int B, int H, int n, int d, int window,
+                              const int32_t *dilation, int causal,
+                              const int32_t *global_idx, int n_global,
+                              const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
+
+/*
  * Scratch (workspace) sizing. The split-KV partials of the global rows and the
  * kernel's work counters need device scratch. By default the library allocates
  * it once per device (cudaMalloc, zeroed) and grows it on demand; a caller that
@@ -169,6 +221,8 @@ sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, vo
  */
 size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g);
 size_t sa_longformer_workspace_bytes(int B, int H, int n, int d, int n_global);
+/* Scratch bytes of one bigbird_attn_bwd / longformer_attn_bwd call (both patterns). */
+size_t sa_attn_bwd_workspace_bytes(int B, int H, int n, int d);
 
 /*
  * sa_set_workspace - use a caller-owned, device-resident scratch region on the

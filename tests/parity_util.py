@@ -106,3 +106,110 @@ def sampled_bigbird_rows(n, b, g, n_random_blocks=8, seed=0):
     blocks = set(range(min(g, nb))) | {min(g, nb - 1), nb - 2, nb - 1}
     blocks |= set(int(x) for x in rng.choice(np.arange(nb), size=min(n_random_blocks, nb), replace=False))
     return np.concatenate([np.arange(j * b, (j + 1) * b) for j in sorted(blocks) if 0 <= j < nb])
+
+
+# --------------------------------------------------------------------------- backward
+# Gradient tolerance. The gradients' scale follows dO and the pattern (a global
+# key's dV sums over every row), so the bound is relative to the reference
+# tensor's RMS, with the forward's numbers (bf16: 2e-2 max, 2e-3 mean; fp32:
+# 1e-4) applied in those units, plus a per-element relative term that covers
+# rounding the output itself to bf16 (a relative 2^-9) and the bf16 rounding
+# of P and dS before the tensor-core products.
+GRAD_TOL = {"bf16": (2e-2, 2e-3, 2.0 ** -7), "fp32": (1e-4, 1e-5, 1e-5)}
+
+
+def assert_close_grad(got, ref, dtype, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite gradient"
+    tmax, tmean, trel = GRAD_TOL[dtype]
+    rms = max(float(np.sqrt(np.mean(ref ** 2))), 1e-30)
+    err = np.abs(got - ref)
+    excess = err - (tmax * rms + trel * np.abs(ref))
+    assert excess.max() <= 0 and err.mean() <= tmean * rms, \
+        f"{what}: max|err|/rms {err.max() / rms:.3e} (worst excess {excess.max():.3e}), " \
+        f"mean|err|/rms {err.mean() / rms:.3e} (tol {tmax}, {tmean}, rel {trel})"
+    return err.max() / rms, err.mean() / rms
+
+
+def gpu_bigbird_bwd(Q, K, V, dO, b, g, w, r, table, key_mask=None, path="tc"):
+    """Forward then backward through the library; returns (O, dQ, dK, dV) on the CPU."""
+    dev = torch.device("cuda:0")
+    set_path(path)
+    try:
+        q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+        tab = table.to(dev) if r > 0 else None
+        km = None if key_mask is None else key_mask.to(dev)
+        O = sa.bigbird_attn_fwd(q, k, v, b, g, w, r, tab, km)
+        dQ, dK, dV = sa.bigbird_attn_bwd(q, k, v, do, b, g, w, r, tab, km)
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    return tuple(t.float().cpu() for t in (O, dQ, dK, dV))
+
+
+def gpu_longformer_bwd(Q, K, V, dO, window, gidx, key_mask=None, path="tc", dilation=None, causal=False):
+    dev = torch.device("cuda:0")
+    set_path(path)
+    try:
+        q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+        gi = None if gidx is None else gidx.to(dev)
+        km = None if key_mask is None else key_mask.to(dev)
+        dil = None if dilation is None else torch.as_tensor(dilation, dtype=torch.int32).to(dev)
+        O = sa.longformer_attn_fwd(q, k, v, window, gi, km, dilation=dil, causal=causal)
+        dQ, dK, dV = sa.longformer_attn_bwd(q, k, v, do, window, gi, km, dilation=dil, causal=causal)
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    return tuple(t.float().cpu() for t in (O, dQ, dK, dV))
+
+
+def _check_grads(got, ref, dtype, key_mask, beta, what):
+    for name, gg, rr in zip(("dQ", "dK", "dV"), got, ref):
+        assert_close_grad(gg, rr, dtype, what=f"{what} {name}")
+    if key_mask is not None:
+        pad = np.nonzero(key_mask[beta].numpy() == 0)[0]
+        for name, gg in zip(("dQ", "dK", "dV"), got):
+            assert np.all(gg[pad] == 0.0), f"{what}: padded positions must have {name} exactly 0"
+
+
+def bigbird_bwd_case(B, H, n, d, b, g, w, r, dtype="bf16", sigma=1.0, cfg_id=70, key_mask=None, seed=0,
+                     path="tc", heads=None):
+    from block_sparse_long_bigbird_gb300.inputs import make_grad_out
+    from oracle import oracle_bigbird_bwd
+
+    Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
+    dO = make_grad_out(B, H, n, d, dtype, cfg_id=cfg_id)
+    table = sa.build_bigbird_pattern(seed, H, n, b, g, w, r)
+    _, dQ, dK, dV = gpu_bigbird_bwd(Q, K, V, dO, b, g, w, r, table, key_mask, path)
+    heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
+    for beta, h in heads:
+        sl = (slice(beta, beta + 1), slice(h, h + 1))
+        km = None if key_mask is None else key_mask[beta:beta + 1].numpy()
+        ref = oracle_bigbird_bwd(Q[sl], K[sl], V[sl], dO[sl], b, g, w, table.numpy()[h:h + 1], key_mask=km)
+        _check_grads([t[beta, h].numpy() for t in (dQ, dK, dV)], [t[0, 0] for t in ref], dtype, key_mask, beta,
+                     f"bigbird bwd beta={beta} h={h}")
+    return dQ, dK, dV
+
+
+def longformer_bwd_case(B, H, n, d, window, gidx, dtype="bf16", cfg_id=80, key_mask=None, path="tc",
+                        heads=None, sigma=1.0, dilation=None, causal=False):
+    from block_sparse_long_bigbird_gb300.inputs import make_grad_out
+    from oracle import oracle_longformer_bwd
+
+    Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
+    dO = make_grad_out(B, H, n, d, dtype, cfg_id=cfg_id)
+    _, dQ, dK, dV = gpu_longformer_bwd(Q, K, V, dO, window, gidx, key_mask, path, dilation, causal)
+    heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
+    g_np = np.zeros(0, dtype=np.int64) if gidx is None else gidx.numpy()
+    for beta, h in heads:
+        sl = (slice(beta, beta + 1), slice(h, h + 1))
+        km = None if key_mask is None else key_mask[beta:beta + 1].numpy()
+        ref = oracle_longformer_bwd(Q[sl], K[sl], V[sl], dO[sl], window, g_np, key_mask=km,
+                                    dilation=None if dilation is None else [dilation[h]], causal=causal)
+        _check_grads([t[beta, h].numpy() for t in (dQ, dK, dV)], [t[0, 0] for t in ref], dtype, key_mask, beta,
+                     f"longformer bwd beta={beta} h={h}")
+    return dQ, dK, dV

@@ -143,3 +143,44 @@ def test_status_codes_match_header():
                       ("SA_ERR_TIMEOUT", _lib.SA_ERR_TIMEOUT), ("SA_ERR_BAD_INDEX", _lib.SA_ERR_BAD_INDEX),
                       ("SA_BF16", _lib.SA_BF16), ("SA_FP32", _lib.SA_FP32)]:
         assert re.search(rf"\b{name}\s*=\s*{val}\b", text), name
+
+
+def _bbb(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, dO=FAKE + 0x400000,
+             dQ=FAKE + 0x500000, dK=FAKE + 0x600000, dV=FAKE + 0x700000, B=1, H=1, n=1024, d=64,
+             b=64, g=2, w=3, r=3, rand=FAKE + 0x800000, km=None, dtype=0)
+    a.update(kw)
+    return lib.bigbird_attn_bwd(a["Q"], a["K"], a["V"], a["dO"], a["dQ"], a["dK"], a["dV"], a["B"],
+                                a["H"], a["n"], a["d"], a["b"], a["g"], a["w"], a["r"], a["rand"], a["km"],
+                                a["dtype"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Q=None), dict(dO=None), dict(dQ=None), dict(dV=FAKE + 8), dict(dQ=FAKE), dict(dK=FAKE + 0x400000),
+    dict(dV=FAKE + 0x500000), dict(n=1000), dict(d=32), dict(w=2), dict(r=-1), dict(rand=None), dict(dtype=2),
+])
+def test_bigbird_bwd_invalid_args(lib, bad):
+    assert _bbb(lib, **bad) == 1
+
+
+def _lfb(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, dO=FAKE + 0x400000,
+             dQ=FAKE + 0x500000, dK=FAKE + 0x600000, dV=FAKE + 0x700000, B=1, H=2, n=1024, d=64,
+             window=64, dil=None, causal=0, gidx=FAKE + 0x800000, ng=4, km=None, dtype=0)
+    a.update(kw)
+    return lib.longformer_attn_bwd(a["Q"], a["K"], a["V"], a["dO"], a["dQ"], a["dK"], a["dV"], a["B"],
+                                   a["H"], a["n"], a["d"], a["window"], a["dil"], a["causal"], a["gidx"], a["ng"],
+                                   a["km"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(causal=2), dict(window=3), dict(ng=-1), dict(gidx=None), dict(dK=FAKE + 0x100000), dict(K=None),
+    dict(d=100), dict(dtype=9),
+])
+def test_longformer_bwd_invalid_args(lib, bad):
+    assert _lfb(lib, **bad) == 1
+
+
+def test_bwd_workspace_bytes(lib):
+    assert lib.sa_attn_bwd_workspace_bytes(8, 12, 4096, 64) == 2 * 4 * 8 * 12 * 4096
+    assert lib.sa_attn_bwd_workspace_bytes(1, 1, 100, 96) == 0

@@ -1,0 +1,125 @@
+"""GPU parity of the backward pass (dQ, dK, dV) against the float64 oracle.
+
+The bound is relative to each reference gradient's RMS (see
+``parity_util.GRAD_TOL``). Every case runs through the C ABI (the forward, then
+the backward at the same inputs).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_long_bigbird_gb300 as sa
+from block_sparse_long_bigbird_gb300.inputs import make_grad_out, make_key_mask, make_qkv, make_random_key_mask
+from parity_util import PATHS, bigbird_bwd_case, gpu_bigbird_bwd, longformer_bwd_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    sa._lib.lib()
+    yield
+    sa.set_option(sa.SA_OPT_FORCE_SIMT, 0)
+
+
+BIGBIRD_BWD = [
+    # B, H, n,    d,   b,   g, w, r
+    (2, 2, 1024, 64, 64, 2, 3, 3),
+    (1, 2, 192, 64, 64, 1, 3, 3),      # nb = 3
+    (1, 2, 1024, 128, 128, 2, 3, 3),
+    (1, 1, 768, 128, 64, 1, 5, 2),
+    (1, 2, 1024, 64, 128, 2, 3, 3),
+    (2, 1, 640, 64, 64, 0, 1, 0),      # block-diagonal
+    (1, 1, 512, 64, 64, 1, 1, 8),      # r >= nb: full attention
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", BIGBIRD_BWD, ids=lambda c: "B{}H{}n{}d{}b{}g{}w{}r{}".format(*c))
+def test_bigbird_bwd_small(case, path):
+    bigbird_bwd_case(*case, dtype="bf16", path=path)
+
+
+@pytest.mark.parametrize("d,b", [(64, 64), (128, 128)])
+def test_bigbird_bwd_fp32(d, b):
+    bigbird_bwd_case(1, 2, 1024, d, b, 2, 3, 3, dtype="fp32", path="simt")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_bwd_prefix_padding(path):
+    B, n = 2, 2048
+    bigbird_bwd_case(B, 2, n, 64, 64, 2, 3, 3, key_mask=make_key_mask(B, n), path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_bwd_random_padding_d128(path):
+    B, n = 1, 1024
+    bigbird_bwd_case(B, 2, n, 128, 128, 2, 3, 3, key_mask=make_random_key_mask(B, n), path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_bwd_headline_sampled_heads(path):
+    """B=8 H=12 n=4096 d=64 (the headline forward workload), two heads compared in full."""
+    bigbird_bwd_case(8, 12, 4096, 64, 64, 2, 3, 3, path=path, heads=[(0, 0), (7, 11)], cfg_id=71)
+
+
+LONGFORMER_BWD = [
+    # B, H, n,    d,   window, globals,        dilation, causal
+    (2, 2, 1000, 64, 128, [0, 5, 500], None, False),
+    (1, 2, 777, 128, 64, [3, 400, 776], None, False),
+    (1, 2, 1000, 64, 96, [0, 5, 500], [0, 2], False),
+    (1, 2, 1000, 64, 128, [0, 5, 500], None, True),
+    (1, 2, 900, 64, 64, [1, 450], [1, 3], True),
+    (1, 1, 300, 64, 0, [], None, False),           # window 0, no globals: each token sees itself
+    (1, 1, 256, 64, 1024, [], None, False),        # window wider than the sequence: full attention
+]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", LONGFORMER_BWD, ids=lambda c: "B{}H{}n{}d{}win{}dil{}c{}".format(
+    *c[:5], c[6], int(c[7])))
+def test_longformer_bwd_small(case, path):
+    B, H, n, d, window, globals_, dilation, causal = case
+    gidx = torch.tensor(globals_, dtype=torch.int32) if globals_ else None
+    longformer_bwd_case(B, H, n, d, window, gidx, path=path, dilation=dilation, causal=causal)
+
+
+def test_longformer_bwd_fp32_padded():
+    B, n = 2, 1000
+    longformer_bwd_case(B, 2, n, 64, 128, torch.tensor([0, 7, 640], dtype=torch.int32), dtype="fp32",
+                        key_mask=make_key_mask(B, n), path="simt", dilation=[0, 1], causal=False)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_bwd_headline_sampled_heads(path):
+    """B=4 H=12 n=4096 d=64 window 512, globals {0..15}; two heads compared in full."""
+    longformer_bwd_case(4, 12, 4096, 64, 512, torch.arange(16, dtype=torch.int32), path=path,
+                        heads=[(0, 0), (3, 11)], cfg_id=81)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bwd_is_deterministic(path):
+    B, H, n, d = 2, 2, 1024, 64
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=72)
+    dO = make_grad_out(B, H, n, d, "bf16", cfg_id=72)
+    table = sa.build_bigbird_pattern(0, H, n, 64, 2, 3, 3)
+    first = gpu_bigbird_bwd(Q, K, V, dO, 64, 2, 3, 3, table, path=path)
+    second = gpu_bigbird_bwd(Q, K, V, dO, 64, 2, 3, 3, table, path=path)
+    for a, b in zip(first, second):
+        assert torch.equal(a, b)
+
+
+def test_bwd_bad_random_entry_latches_status():
+    dev = torch.device("cuda:0")
+    B, H, n, d = 1, 1, 512, 64
+    Q, K, V = (t.to(dev) for t in make_qkv(B, H, n, d, "bf16", cfg_id=73))
+    dO = make_grad_out(B, H, n, d, "bf16", cfg_id=73).to(dev)
+    table = sa.build_bigbird_pattern(0, H, n, 64, 2, 3, 3)
+    O = sa.bigbird_attn_fwd(Q, K, V, 64, 2, 3, 3, table.to(dev))
+    torch.cuda.synchronize()
+    assert sa.get_last_device_status() == 0
+    table[0, 4, 0] = 99  # out of range: skipped and latched
+    sa.bigbird_attn_bwd(Q, K, V, dO, 64, 2, 3, 3, table.to(dev))
+    assert sa.get_last_device_status() == sa._lib.SA_ERR_BAD_INDEX
+    assert sa.get_last_device_status() == 0
