@@ -190,7 +190,12 @@ sa_status run_bwd(const sa::Problem &prob_in, sa_dtype dtype, cudaStream_t strea
     size_t *clean = (ws == st->user_ws) ? &st->user_ws_clean : &st->ws_clean;
     *clean = 0;
     int launches = 0;
-    const cudaError_t e = sa::launch_simt_bwd(prob, dtype, stream, &launches);
+    cudaError_t e;
+    if (dtype == SA_FP32 || g_force_simt.load())
+        e = sa::launch_simt_bwd(prob, dtype, stream, &launches);
+    else
+        e = sa::launch_tc_bwd(prob, tc_config(st), stream, &launches);
+    if (e == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return SA_ERR_CUDA;
     g_last_launches = launches;
     return SA_OK;

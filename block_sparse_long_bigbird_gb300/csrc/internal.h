@@ -58,6 +58,8 @@ struct TcConfig {
     int max_splits;    // split-KV upper bound for global row tiles
     long long wait_limit;
 };
+// Tensor-core backward (bf16): row pass then key pass, two launches.
+cudaError_t launch_tc_bwd(const Problem &p, const TcConfig &cfg, cudaStream_t stream, int *launches);
 size_t tc_workspace_bytes(const Problem &p, const TcConfig &cfg);
 // Leading bytes of the tensor-core scratch that must be zero when a call
 // starts (scheduler and merge counters).

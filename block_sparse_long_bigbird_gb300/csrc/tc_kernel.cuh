@@ -47,11 +47,13 @@
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
+#include "tc_sync.cuh"
 
 namespace sa {
 namespace {
 
 using namespace ptx;
+using namespace tcsync;
 
 constexpr int kBM = 128;           // query rows per tile = TMEM lanes
 constexpr int kNU = 4;             // unit-info ring depth
@@ -59,7 +61,6 @@ constexpr int kTargetChunkKeys = 8192;  // keys per split-KV chunk (at most)
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (factor 256)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzled region
-constexpr uint32_t kSuspendNs = 100000;  // try_wait suspend hint
 
 enum UnitKind { kUnitEnd = 0, kUnitDirect = 1, kUnitSplit = 2 };
 
@@ -175,64 +176,6 @@ struct Params {
     __nv_bfloat16 *O;
     unsigned *status;
 };
-
-struct Ctl {
-    volatile int *abort;
-    unsigned *status;
-    unsigned long long limit_ns;
-};
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendNs)
-        : "memory");
-    return ok != 0;
-}
-
-// Per-thread wait, bounded in time: returns false (and leaves) once the CTA
-// aborts. The first probe has no suspend hint (cheapest when the phase is
-// already complete); later probes sleep in the hardware until the phase
-// completes or the hint expires. No warp-collective operation inside, so
-// lanes of one warp may call it independently.
-__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Ctl &c) {
-    if (mbar_try_wait(bar, parity)) return true;
-    unsigned long long t0 = 0;
-    while (!try_wait_hint(bar, parity)) {
-        if (*c.abort) return false;
-        const unsigned long long now = global_ns();
-        if (t0 == 0) {
-            t0 = now;
-        } else if (now - t0 > c.limit_ns) {
-            *c.abort = 1;
-            atomicOr(c.status, kDevTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-// Warp-uniform wait: every lane probes the barrier itself (a divergent
-// single-lane wait costs hundreds of cycles to reconverge), then one vote
-// gives all lanes the same answer.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl &c) {
-    const bool ok = wait_one(bar, parity, c);
-    return __all_sync(kFull, ok);
-}
-// Drain wait used on the abort path (ignores the abort flag, still bounded).
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > limit_ns) return;
-}
 
 // ---------------------------------------------------------------- producer helpers
 // Longformer global list entry t as a token position, or n when t is past the

@@ -43,6 +43,9 @@ Every function pinned by a test that does not reuse this code; the pins are in
                            scaled_dot_product_attention with the same mask;
                            shift invariance sum_j dK_j = 0 and sum_j dV_j =
                            sum of dO over rows with an allowed key)
+  masked_attention_grad_   pinned (brute-force sums of |term| and term^2 on
+  terms                    a tiny case; the exact gradient lies inside the
+                           rounding bound it yields for bf16-rounded P and dS)
 """
 
 from .pattern import SplitMix64, splitmix64_stream, bigbird_random_table
@@ -54,6 +57,7 @@ from .attention import (
     oracle_bigbird,
     oracle_longformer,
     masked_attention_grads,
+    masked_attention_grad_terms,
     oracle_bigbird_bwd,
     oracle_longformer_bwd,
     bigbird_attended_pairs,
@@ -71,6 +75,7 @@ __all__ = [
     "oracle_bigbird",
     "oracle_longformer",
     "masked_attention_grads",
+    "masked_attention_grad_terms",
     "oracle_bigbird_bwd",
     "oracle_longformer_bwd",
     "bigbird_attended_pairs",

@@ -224,28 +224,68 @@ def masked_attention_grads(q, k, v, mask, dout):
     return scale * (ds @ k), scale * (ds.T @ q), dv
 
 
-def _grads_over_rows(Qh, Kh, Vh, dOh, mask_of_rows, n, row_chunk):
+def masked_attention_grad_terms(q, k, v, mask, dout):
+    """Size of the sums behind each gradient element, for error analysis.
+
+    Every element of dQ, dK and dV is a sum of products (dQ_ic = sum_j t_j with
+    t_j = dS_ij K_jc / sqrt(d), dK_jc over i of dS_ij Q_ic / sqrt(d), dV_jc
+    over i of P_ij dO_ic). Returns, for (dq, dk, dv) in turn, the pair
+    (sum_t |t|, sqrt(sum_t t^2)): the first bounds the effect of rounding every
+    factor P or dS by a relative e (at most e * sum |t|), the second is the
+    scale of that effect when the roundings are independent.
+    """
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    scale = 1.0 / math.sqrt(q.shape[1])
+    p = masked_softmax_probs(q, k, mask)
+    dp = dout @ v.T
+    ds = p * (dp - (p * dp).sum(axis=1)[:, None])
+    a, a2 = np.abs(ds), ds * ds
+    return ((scale * (a @ np.abs(k)), scale * np.sqrt(a2 @ (k * k))),
+            (scale * (a.T @ np.abs(q)), scale * np.sqrt(a2.T @ (q * q))),
+            (p.T @ np.abs(dout), np.sqrt((p * p).T @ (dout * dout))))
+
+
+def _grads_over_rows(Qh, Kh, Vh, dOh, mask_of_rows, n, row_chunk, terms=False):
     """Sum the per-row contributions to dK and dV over row chunks of one head
-    (dQ rows are independent); the chunks only bound memory."""
+    (dQ rows are independent); the chunks only bound memory. With ``terms``,
+    also return the term sizes of ``masked_attention_grad_terms`` (the squared
+    sums add over chunks)."""
     dQ = np.zeros_like(Qh)
     dK = np.zeros_like(Kh)
     dV = np.zeros_like(Vh)
+    tq = [np.zeros_like(Qh), np.zeros_like(Qh)]
+    tk = [np.zeros_like(Kh), np.zeros_like(Kh)]
+    tv = [np.zeros_like(Vh), np.zeros_like(Vh)]
     for c0 in range(0, n, row_chunk):
         rr = np.arange(c0, min(n, c0 + row_chunk))
-        dq, dk, dv = masked_attention_grads(Qh[rr], Kh, Vh, mask_of_rows(rr), dOh[rr])
+        mask = mask_of_rows(rr)
+        dq, dk, dv = masked_attention_grads(Qh[rr], Kh, Vh, mask, dOh[rr])
         dQ[rr] = dq
         dK += dk
         dV += dv
-    return dQ, dK, dV
+        if terms:
+            (qa, qr), (ka, kr), (va, vr) = masked_attention_grad_terms(Qh[rr], Kh, Vh, mask, dOh[rr])
+            tq[0][rr], tq[1][rr] = qa, qr
+            tk[0] += ka
+            tk[1] += kr * kr
+            tv[0] += va
+            tv[1] += vr * vr
+    if not terms:
+        return dQ, dK, dV
+    tk[1], tv[1] = np.sqrt(tk[1]), np.sqrt(tv[1])
+    return (dQ, dK, dV), (tuple(tq), tuple(tk), tuple(tv))
 
 
-def oracle_bigbird_bwd(Q, K, V, dO, b, g, w, rand_table, key_mask=None, row_chunk=1024):
+def oracle_bigbird_bwd(Q, K, V, dO, b, g, w, rand_table, key_mask=None, row_chunk=1024, terms=False):
     """Gradients (dQ, dK, dV), float64 [B, H, n, d], of the BigBird-ITC forward
-    ``oracle_bigbird`` for the upstream gradient dO [B, H, n, d]."""
+    ``oracle_bigbird`` for the upstream gradient dO [B, H, n, d]. With
+    ``terms``, returns ((dQ, dK, dV), term sizes), the term sizes as in
+    ``masked_attention_grad_terms`` with a leading [B, H]."""
     Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
     rand_table = np.asarray(rand_table)
     B, H, n, d = Q.shape
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    T = [[np.zeros_like(Q), np.zeros_like(Q)] for _ in range(3)] if terms else None
     for h in range(H):
         blk = bigbird_block_allowed(n // b, g, w, rand_table[h])
         for beta in range(B):
@@ -254,18 +294,26 @@ def oracle_bigbird_bwd(Q, K, V, dO, b, g, w, rand_table, key_mask=None, row_chun
             def mask_of_rows(rr):
                 return _apply_validity(blk[rr[:, None] // b, np.arange(n)[None, :] // b], rr, kv)
 
-            dQ[beta, h], dK[beta, h], dV[beta, h] = _grads_over_rows(
-                Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], mask_of_rows, n, row_chunk)
-    return dQ, dK, dV
+            res = _grads_over_rows(Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], mask_of_rows, n,
+                                   row_chunk, terms)
+            if terms:
+                res, tt = res
+                for which in range(3):
+                    for kind in range(2):
+                        T[which][kind][beta, h] = tt[which][kind]
+            dQ[beta, h], dK[beta, h], dV[beta, h] = res
+    return ((dQ, dK, dV), T) if terms else (dQ, dK, dV)
 
 
 def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilation=None,
-                          causal=False, row_chunk=1024):
-    """Gradients (dQ, dK, dV), float64 [B, H, n, d], of ``oracle_longformer``."""
+                          causal=False, row_chunk=1024, terms=False):
+    """Gradients (dQ, dK, dV), float64 [B, H, n, d], of ``oracle_longformer``
+    (``terms``: as for ``oracle_bigbird_bwd``)."""
     Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
     B, H, n, d = Q.shape
     dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
     dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    T = [[np.zeros_like(Q), np.zeros_like(Q)] for _ in range(3)] if terms else None
     for h in range(H):
         for beta in range(B):
             kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
@@ -274,9 +322,15 @@ def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilati
                 return _apply_validity(longformer_allowed(n, window, global_idx, rr, dilation=dil[h],
                                                           causal=causal), rr, kv)
 
-            dQ[beta, h], dK[beta, h], dV[beta, h] = _grads_over_rows(
-                Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], mask_of_rows, n, row_chunk)
-    return dQ, dK, dV
+            res = _grads_over_rows(Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], mask_of_rows, n,
+                                   row_chunk, terms)
+            if terms:
+                res, tt = res
+                for which in range(3):
+                    for kind in range(2):
+                        T[which][kind][beta, h] = tt[which][kind]
+            dQ[beta, h], dK[beta, h], dV[beta, h] = res
+    return ((dQ, dK, dV), T) if terms else (dQ, dK, dV)
 
 
 # ---------------------------------------------------------------------------

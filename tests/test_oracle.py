@@ -493,3 +493,65 @@ def test_grads_shift_invariance_and_value_sum():
     np.testing.assert_allclose(dK[0, 0].sum(axis=0), 0.0, atol=1e-12)
     np.testing.assert_allclose(dV[0, 0].sum(axis=0), dO[0, 0, :200].sum(axis=0), atol=1e-12)
     assert np.all(dQ[0, 0, 200:] == 0) and np.all(dK[0, 0, 200:] == 0) and np.all(dV[0, 0, 200:] == 0)
+
+
+def test_grad_terms_match_scalar_bruteforce():
+    """Sum of |term| and sqrt(sum term^2) of every gradient element, from
+    scalar loops over the definitions (softmax, dS, then the products)."""
+    from oracle import masked_attention_grad_terms
+    m, n, d = 5, 6, 3
+    rng = np.random.default_rng(61)
+    q, k, v, do = rng.standard_normal((m, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d)), \
+        rng.standard_normal((m, d))
+    mask = rng.random((m, n)) < 0.6
+    mask[0, :] = False  # a row without keys
+    sc = 1.0 / math.sqrt(d)
+    P = np.zeros((m, n))
+    dS = np.zeros((m, n))
+    for i in range(m):
+        keys = [j for j in range(n) if mask[i, j]]
+        if not keys:
+            continue
+        s = {j: sc * sum(q[i, c] * k[j, c] for c in range(d)) for j in keys}
+        mx = max(s.values())
+        z = sum(math.exp(s[j] - mx) for j in keys)
+        for j in keys:
+            P[i, j] = math.exp(s[j] - mx) / z
+        dp = {j: sum(do[i, c] * v[j, c] for c in range(d)) for j in keys}
+        Di = sum(P[i, j] * dp[j] for j in keys)
+        for j in keys:
+            dS[i, j] = P[i, j] * (dp[j] - Di)
+    (qa, qr), (ka, kr), (va, vr) = masked_attention_grad_terms(q, k, v, mask, do)
+    for i in range(m):
+        for c in range(d):
+            t = [sc * dS[i, j] * k[j, c] for j in range(n)]
+            assert math.isclose(qa[i, c], sum(abs(x) for x in t), rel_tol=1e-12, abs_tol=1e-15)
+            assert math.isclose(qr[i, c], math.sqrt(sum(x * x for x in t)), rel_tol=1e-12, abs_tol=1e-15)
+    for j in range(n):
+        for c in range(d):
+            t = [sc * dS[i, j] * q[i, c] for i in range(m)]
+            u = [P[i, j] * do[i, c] for i in range(m)]
+            assert math.isclose(ka[j, c], sum(abs(x) for x in t), rel_tol=1e-12, abs_tol=1e-15)
+            assert math.isclose(kr[j, c], math.sqrt(sum(x * x for x in t)), rel_tol=1e-12, abs_tol=1e-15)
+            assert math.isclose(va[j, c], sum(abs(x) for x in u), rel_tol=1e-12, abs_tol=1e-15)
+            assert math.isclose(vr[j, c], math.sqrt(sum(x * x for x in u)), rel_tol=1e-12, abs_tol=1e-15)
+
+
+def test_bf16_rounded_factors_stay_inside_the_term_bound():
+    """Rounding P and dS to bf16 (a relative error of at most 2^-9 each)
+    moves every gradient element by at most 2^-9 * sum |term|."""
+    from oracle import masked_attention_grad_terms
+    n, d = 512, 64
+    rng = np.random.default_rng(62)
+    q, k, v, do = (rng.standard_normal((n, d)) for _ in range(4))
+    mask = bigbird_allowed(n, 64, 1, 3, bigbird_random_table(1, 1, n, 64, 1, 3, 2)[0])
+    sc = 1.0 / math.sqrt(d)
+    P = masked_softmax_probs(q, k, mask)
+    dp = do @ v.T
+    dS = P * (dp - (P * dp).sum(axis=1)[:, None])
+    to_bf16 = lambda x: torch.as_tensor(x).to(torch.bfloat16).to(torch.float64).numpy()
+    Pb, dSb = to_bf16(P), to_bf16(dS)
+    (qa, _), (ka, _), (va, _) = masked_attention_grad_terms(q, k, v, mask, do)
+    assert np.all(np.abs(sc * (dSb - dS) @ k) <= 2.0 ** -9 * qa + 1e-15)
+    assert np.all(np.abs(sc * (dSb - dS).T @ q) <= 2.0 ** -9 * ka + 1e-15)
+    assert np.all(np.abs((Pb - P).T @ do) <= 2.0 ** -9 * va + 1e-15)
