@@ -1,9 +1,11 @@
 #!/usr/bin/env python
-"""Throughput of the sparse-attention forward on GB300.
+"""Throughput of the sparse-attention forward (and backward) on GB300.
 
 One step = one `bigbird_attn_fwd` (or `longformer_attn_fwd`) call over the
 whole synthetic workload (default: BigBird-ITC, B=8, H=12, n=4096, d=64,
-b=64, g=2, w=3, r=3, bf16). Prints one JSON line on rank 0.
+b=64, g=2, w=3, r=3, bf16). The `*_bwd_*` workloads time one
+`bigbird_attn_bwd` / `longformer_attn_bwd` call instead (10*d useful FLOPs
+per attended pair). Prints one JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -33,6 +35,7 @@ if ROOT not in sys.path:
 from block_sparse_long_bigbird_gb300.workloads import HEADLINE, WORKLOADS  # noqa: E402
 
 METRIC = "useful TFLOP/s and tokens/s of sparse attn fwd at n=4096, % of bf16 tensor peak"
+METRIC_BWD = "useful TFLOP/s and tokens/s of sparse attn bwd (dQ, dK, dV) at n=4096, % of bf16 tensor peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 TC_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_kernel.cuh")
@@ -165,11 +168,13 @@ def make_problem(wl, rank=0):
 
     import block_sparse_long_bigbird_gb300 as sa
     from block_sparse_long_bigbird_gb300 import accounting
-    from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv
+    from block_sparse_long_bigbird_gb300.inputs import make_grad_out, make_key_mask, make_qkv
 
     Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, wl.dtype, sigma=wl.sigma, cfg_id=wl.cfg_id + 100 * rank)
     km = make_key_mask(wl.B, wl.n) if wl.padded else None
     prob = {"Q": Q, "K": K, "V": V, "key_mask": km}
+    if wl.grad:
+        prob["dO"] = make_grad_out(wl.B, wl.H, wl.n, wl.d, wl.dtype, cfg_id=wl.cfg_id + 100 * rank)
     if wl.kind == "bigbird":
         table = sa.build_bigbird_pattern(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
         prob["table"] = table
@@ -186,7 +191,8 @@ def make_problem(wl, rank=0):
             pairs *= wl.B
     tokens = wl.B * wl.n if km is None else int(km.sum())
     prob["pairs"] = pairs
-    prob["flops"] = 4.0 * wl.d * pairs
+    per_pair = accounting.BWD_FLOPS_PER_PAIR_PER_D if wl.grad else accounting.FWD_FLOPS_PER_PAIR_PER_D
+    prob["flops"] = float(per_pair) * wl.d * pairs
     prob["tokens"] = tokens
     return prob
 
@@ -194,6 +200,14 @@ def make_problem(wl, rank=0):
 def call(wl, dev_t, out, stream=None):
     import block_sparse_long_bigbird_gb300 as sa
 
+    if wl.grad:
+        if wl.kind == "bigbird":
+            sa.bigbird_attn_bwd(dev_t["Q"], dev_t["K"], dev_t["V"], dev_t["dO"], wl.b, wl.g, wl.w, wl.r,
+                                dev_t["table"], dev_t.get("key_mask"), out=out, stream=stream)
+        else:
+            sa.longformer_attn_bwd(dev_t["Q"], dev_t["K"], dev_t["V"], dev_t["dO"], wl.window, dev_t["gidx"],
+                                   dev_t.get("key_mask"), out=out, stream=stream)
+        return
     if wl.kind == "bigbird":
         sa.bigbird_attn_fwd(dev_t["Q"], dev_t["K"], dev_t["V"], wl.b, wl.g, wl.w, wl.r, dev_t["table"],
                             dev_t.get("key_mask"), out=out, stream=stream)
@@ -207,9 +221,10 @@ def cpu_oracle_sample(wl, prob, budget_s):
     import numpy as np
 
     from block_sparse_long_bigbird_gb300 import accounting
-    from oracle import oracle_bigbird, oracle_longformer
+    from oracle import oracle_bigbird, oracle_bigbird_bwd, oracle_longformer, oracle_longformer_bwd
 
     Q, K, V, km = prob["Q"], prob["K"], prob["V"], prob["key_mask"]
+    per_pair = float(accounting.BWD_FLOPS_PER_PAIR_PER_D if wl.grad else accounting.FWD_FLOPS_PER_PAIR_PER_D)
     heads = [(beta, h) for beta in range(wl.B) for h in range(wl.H)]
     done, flops = 0, 0.0
     t0 = time.perf_counter()
@@ -218,11 +233,18 @@ def cpu_oracle_sample(wl, prob, budget_s):
         kmb = None if km is None else km[beta:beta + 1].numpy()
         if wl.kind == "bigbird":
             tab = prob["table"].numpy()[h:h + 1]
-            oracle_bigbird(Q[sl], K[sl], V[sl], wl.b, wl.g, wl.w, tab, key_mask=kmb)
-            flops += 4.0 * wl.d * accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, tab, kmb)
+            if wl.grad:
+                oracle_bigbird_bwd(Q[sl], K[sl], V[sl], prob["dO"][sl], wl.b, wl.g, wl.w, tab, key_mask=kmb)
+            else:
+                oracle_bigbird(Q[sl], K[sl], V[sl], wl.b, wl.g, wl.w, tab, key_mask=kmb)
+            flops += per_pair * wl.d * accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, tab, kmb)
         else:
-            oracle_longformer(Q[sl], K[sl], V[sl], wl.window, prob["gidx"].numpy(), key_mask=kmb)
-            flops += 4.0 * wl.d * accounting.longformer_pairs(wl.n, wl.window, prob["gidx"].numpy(), kmb)
+            gi = prob["gidx"].numpy()
+            if wl.grad:
+                oracle_longformer_bwd(Q[sl], K[sl], V[sl], prob["dO"][sl], wl.window, gi, key_mask=kmb)
+            else:
+                oracle_longformer(Q[sl], K[sl], V[sl], wl.window, gi, key_mask=kmb)
+            flops += per_pair * wl.d * accounting.longformer_pairs(wl.n, wl.window, gi, kmb)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -254,7 +276,7 @@ def run_reference(args):
         vals.append(r["value"])
     value = statistics.mean(vals)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_BWD if wl.grad else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(wl),
@@ -267,7 +289,7 @@ def run_reference(args):
 
 
 def workload_config(wl):
-    cfg = {"workload": f"{wl.name}: {wl.kind} B={wl.B} H={wl.H} n={wl.n} d={wl.d}",
+    cfg = {"workload": f"{wl.name}: {wl.kind}{' backward' if wl.grad else ''} B={wl.B} H={wl.H} n={wl.n} d={wl.d}",
            "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "dtype": wl.dtype,
            "l2": "flushed between timed steps (256 MiB write), inputs resident in HBM"}
     if wl.kind == "bigbird":
@@ -298,7 +320,7 @@ def main(argv=None):
     wl = WORKLOADS[args.workload]
     prob = make_problem(wl, rank)
     dev_t = {k: v.to(dev) for k, v in prob.items() if hasattr(v, "to") and v is not None}
-    out = torch.empty_like(dev_t["Q"])
+    out = tuple(torch.empty_like(dev_t["Q"]) for _ in range(3)) if wl.grad else torch.empty_like(dev_t["Q"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -359,27 +381,33 @@ def main(argv=None):
     kernel_tflops = prob["flops"] / (my_ms * 1e-3) / 1e12
     kernel_name = "sparse_tc_fwd<{},{},{}>".format(wl.d, "padded" if wl.padded else "dense",
                                                    "longformer" if wl.kind == "longformer" else "bigbird")
+    if wl.grad:
+        # one call launches the row pass and the key pass; they are timed together
+        kernel_name = f"sparse_tc_bwd<{wl.d},rows> + sparse_tc_bwd<{wl.d},keys>"
     traffic = read_traffic(kernel_name, wl.name)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)", "kernel": kernel_name,
                 "algorithmic_flops_per_launch": prob["flops"]}
-    hbm_bytes = 4 * wl.B * wl.H * wl.n * wl.d * (2 if wl.dtype == "bf16" else 4)
+    hbm_bytes = (8 if wl.grad else 4) * wl.B * wl.H * wl.n * wl.d * (2 if wl.dtype == "bf16" else 4)
     roofline["hbm_frac_of_min_bytes"] = hbm_bytes / (my_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
 
     e2e = None
     if not args.no_e2e:
-        host = {k: prob[k].pin_memory() for k in ("Q", "K", "V")}
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        ins = ("Q", "K", "V", "dO") if wl.grad else ("Q", "K", "V")
+        outs = out if wl.grad else (out,)
+        host = {k: prob[k].pin_memory() for k in ins}
+        out_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
         e_ms = []
         for i in range(max(2, args.warmup) + args.steps):
             flush.fill_(i & 0xFF)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
-            for k in ("Q", "K", "V"):
+            for k in ins:
                 dev_t[k].copy_(host[k], non_blocking=True)
             call(wl, dev_t, out)
-            out_h.copy_(out, non_blocking=True)
+            for oh, o in zip(out_h, outs):
+                oh.copy_(o, non_blocking=True)
             e.record(stream)
             torch.cuda.synchronize(dev)
             if i >= max(2, args.warmup):
@@ -393,8 +421,8 @@ def main(argv=None):
             e_t = float(t.item())
         e2e = {"value": world * prob["flops"] / (e_t * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_t,
-               "h2d_bytes_per_step": sum(prob[k].numel() * prob[k].element_size() for k in ("Q", "K", "V")),
-               "d2h_bytes_per_step": out.numel() * out.element_size()}
+               "h2d_bytes_per_step": sum(prob[k].numel() * prob[k].element_size() for k in ins),
+               "d2h_bytes_per_step": sum(o.numel() * o.element_size() for o in outs)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -402,7 +430,7 @@ def main(argv=None):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": agg["tflops"], "unit": UNIT, "n_gpus": world,
+            "metric": METRIC_BWD if wl.grad else METRIC, "value": agg["tflops"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": agg["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic (seeded torch.randn inputs, pattern seed 0)",

@@ -1,13 +1,19 @@
-"""Useful-work accounting for the sparse-attention forward.
+"""Useful-work accounting for the sparse-attention forward and backward.
 
 Useful FLOPs = 4 * d per attended pair (a valid query and an allowed valid
-key): 2 d for the score Q_i . K_j and 2 d for accumulating P_ij V_j. The pair
+key): 2 d for the score Q_i . K_j and 2 d for accumulating P_ij V_j. The
+backward counts 10 * d per pair: the five products a backward needs (the
+score recomputed, dP_ij = dO_i . V_j, and the accumulations of dV, dQ and dK),
+whatever extra work an implementation does. The pair
 count follows the patterns' definitions ("Big Bird" Sec. 2 / App. D;
 "Longformer" Sec. 3.1) at block granularity for BigBird and row by row for
 Longformer; it is host-side bookkeeping and never enters a kernel.
 """
 
 import numpy as np
+
+FWD_FLOPS_PER_PAIR_PER_D = 4
+BWD_FLOPS_PER_PAIR_PER_D = 10
 
 
 def bigbird_block_sets(nb, g, w, rand_row):

@@ -75,7 +75,7 @@ bool size_ok(int B, int H, int n, int d) {
     return true;
 }
 
-size_t bwd_stats_bytes(int B, int H, int n) { return 2 * sizeof(float) * (size_t)B * H * n; }
+size_t bwd_stats_bytes(int B, int H, int n) { return 2 * sizeof(float) * (size_t)B * H * sa::stats_stride(n); }
 
 sa_status bigbird_args_ok(int B, int H, int n, int d, int b, int g, int w, int r, const int32_t *rand_idx) {
     if (!size_ok(B, H, n, d)) return SA_ERR_INVALID_ARG;

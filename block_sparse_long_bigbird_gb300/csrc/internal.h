@@ -37,13 +37,18 @@ struct Problem {
     // both
     const uint8_t *key_mask;
     unsigned int *status;  // device status word
-    // backward only: dO is the upstream gradient; row_stats holds 2 * B * H * n
-    // floats of scratch (per-row log2-domain log-sum-exp, then per-row
-    // D = sum_j P_ij dO_i . V_j).
+    // backward only: dO is the upstream gradient; row_stats holds
+    // 2 * B * H * stats_stride(n) floats of scratch (per-row log2-domain
+    // log-sum-exp, then per-row D = sum_j P_ij dO_i . V_j), rows of each head
+    // stats_stride(n) apart.
     const void *dO;
     void *dQ, *dK, *dV;
     float *row_stats;
 };
+
+// Row stride of the backward's per-row statistics: n rounded up to 64, so that
+// every 64-row chunk of them starts 256-B aligned.
+__host__ __device__ inline int stats_stride(int n) { return (n + 63) & ~63; }
 
 // Exact SIMT kernels (fp32 arithmetic; bf16 or fp32 storage).
 cudaError_t launch_simt(const Problem &p, sa_dtype dtype, cudaStream_t stream, int *launches);

@@ -159,8 +159,9 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(Problem p) {
     const T *Vh = static_cast<const T *>(p.V) + head_off;
     const T *dOh = static_cast<const T *>(p.dO) + head_off;
     T *dQh = static_cast<T *>(p.dQ) + head_off;
-    float *lse_out = p.row_stats + (size_t)bh * n;
-    float *dl_out = p.row_stats + (size_t)p.B * p.H * n + (size_t)bh * n;
+    const size_t sst = (size_t)stats_stride(n);
+    float *lse_out = p.row_stats + (size_t)bh * sst;
+    float *dl_out = p.row_stats + (size_t)p.B * p.H * sst + (size_t)bh * sst;
     const uint8_t *km = p.key_mask ? p.key_mask + (size_t)beta * n : nullptr;
 
     unsigned *misc = reinterpret_cast<unsigned *>(sm + L::misc_off);
@@ -380,8 +381,9 @@ __global__ void __launch_bounds__(kThreads) bwd_cols_kernel(Problem p) {
     const T *dOh = static_cast<const T *>(p.dO) + head_off;
     T *dKh = static_cast<T *>(p.dK) + head_off;
     T *dVh = static_cast<T *>(p.dV) + head_off;
-    const float *lse_in = p.row_stats + (size_t)bh * n;
-    const float *dl_in = p.row_stats + (size_t)p.B * p.H * n + (size_t)bh * n;
+    const size_t sst = (size_t)stats_stride(n);
+    const float *lse_in = p.row_stats + (size_t)bh * sst;
+    const float *dl_in = p.row_stats + (size_t)p.B * p.H * sst + (size_t)bh * sst;
     const uint8_t *km = p.key_mask ? p.key_mask + (size_t)beta * n : nullptr;
 
     unsigned *misc = reinterpret_cast<unsigned *>(sm + L::misc_off);

@@ -26,9 +26,10 @@
 // records (chunk position, the tile halves it is allowed for, validity and
 // global bits, and in the key pass the chunk rows' lse and D); warp 1 lane 0
 // issues the MMAs; warpgroups 1 and 2 (warps 4-7, 8-11) take even and odd
-// steps, each thread owning one TMEM lane (one tile row). X and Y are double
-// buffered in TMEM (slot = step % 2), so one warpgroup's elementwise work
-// overlaps the other step's products. Every wait is bounded in time.
+// steps, each thread owning one TMEM lane (one tile row). X and Y rotate
+// through NSL TMEM slots (three for d = 64, two for d = 128) and each step's
+// accumulate products are issued NSL - 1 steps late, so the MMA issuer runs
+// ahead of the elementwise work. Every wait is bounded in time.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -61,14 +62,13 @@ struct BwdStep {
     uint64_t vbits;   // valid entries of the chunk (position < n and not padded)
     uint64_t gbits;   // Longformer: global positions among the chunk's entries
     uint64_t pad;
-    float lse[kCN];   // key pass: the chunk rows' lse (log2 domain)
-    float dl[kCN];    // key pass: the chunk rows' D
 };
-static_assert(sizeof(BwdStep) == 32 + 2 * kCN * 4, "BwdStep layout");
+static_assert(sizeof(BwdStep) == 32, "BwdStep layout");
 
 template <int D>
 struct BwdCfg {
     static constexpr int NSTG = (D == 64) ? 6 : 3;  // chunk stages (one K/Q + one V/dO chunk each)
+    static constexpr int NSL = (D == 64) ? 3 : 2;   // X/Y slots in TMEM (128 columns each)
     static constexpr int TILE_BYTES = kTM * D * 2;
     static constexpr int CH_BYTES = kCN * D * 2;
     static constexpr int REG_T = kTM * 128;  // one 64-column swizzled region of a tile
@@ -77,20 +77,21 @@ struct BwdCfg {
     static constexpr int A2_OFF = TILE_BYTES;
     static constexpr int B1_OFF = 2 * TILE_BYTES;
     static constexpr int B2_OFF = B1_OFF + NSTG * CH_BYTES;
-    static constexpr int BIG = B2_OFF + NSTG * CH_BYTES;
+    static constexpr int LS_OFF = B2_OFF + NSTG * CH_BYTES;  // key pass: per stage the chunk rows' lse, D
+    static constexpr int BIG = LS_OFF + NSTG * 2 * kCN * 4;
     // barriers
-    static constexpr int B_TF = 0, B_F = 1, B_E = B_F + NSTG, B_SF = B_E + NSTG, B_PF = B_SF + 2,
-                         B_IF = B_PF + 2, B_IE = B_IF + kSI, B_DONE = B_IE + kSI, B_DRAIN = B_DONE + 1,
+    static constexpr int B_TF = 0, B_F = 1, B_E = B_F + NSTG, B_SF = B_E + NSTG, B_PF = B_SF + NSL,
+                         B_IF = B_PF + NSL, B_IE = B_IF + kSI, B_DONE = B_IE + kSI, B_DRAIN = B_DONE + 1,
                          B_COUNT = B_DRAIN + 1;
     static constexpr int BAR_OFF = BIG;
     static constexpr int STEP_OFF = (BAR_OFF + B_COUNT * 8 + 127) & ~127;
     static constexpr int STAT_OFF = STEP_OFF + kSI * (int)sizeof(BwdStep);  // [3][128] floats
     static constexpr int MISC_OFF = STAT_OFF + 3 * kTM * 4;                 // tmem addr, abort, nsteps
-    static constexpr int MAP_OFF = MISC_OFF + 16;                            // chunk bitmap
+    static constexpr int MAP_OFF = MISC_OFF + 16;  // chunk bitmap, then the per-chunk tables (chunk_tables)
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t ACC_COL = 256;  // after two X/Y slots of 128 columns
+    static constexpr uint32_t ACC_COL = NSL * 128;  // accumulators after the X/Y slots
     static_assert(ACC_COL + 2 * D <= TMEM_COLS, "TMEM columns");
-    static_assert(BIG % 1024 == 0, "buffers stay 1024-B aligned");
+    static_assert(LS_OFF % 1024 == 0, "buffers stay 1024-B aligned");
 };
 
 struct BwdParams {
@@ -110,6 +111,22 @@ struct BwdParams {
     unsigned *status;
 };
 
+// Per-chunk tables after the chunk bitmap (byte offsets from the bitmap):
+// validity bits [nch] (uint64), Longformer global bits [nch] (uint64), and
+// the tile halves each chunk is marked for [nch] (uint32; bit h: half h).
+struct ChunkTables {
+    int vb_off, gb_off, hv_off, bytes;
+};
+__host__ __device__ inline ChunkTables chunk_tables(int nch) {
+    ChunkTables t;
+    const int words = (nch + 31) / 32;
+    t.vb_off = ((words * 4) + 7) & ~7;
+    t.gb_off = t.vb_off + 8 * nch;
+    t.hv_off = t.gb_off + 8 * nch;
+    t.bytes = t.hv_off + 4 * nch;
+    return t;
+}
+
 // ----------------------------------------------------------------- pattern helpers
 __device__ __forceinline__ uint64_t bits_below64(int c) {
     return c <= 0 ? 0ull : (c >= 64 ? ~0ull : ((1ull << c) - 1ull));
@@ -125,17 +142,6 @@ __device__ __forceinline__ int rand_entry(const BwdParams &p, int h, int qb, int
         return INT_MAX;
     }
     return v;
-}
-
-// Does BigBird query block qb see key block kb ("Big Bird", App. D blocks)?
-// Warp-collective (the random list is searched by the lanes).
-__device__ __forceinline__ bool bb_allowed_warp(const BwdParams &p, int h, int qb, int kb) {
-    if (qb < 0 || qb >= p.nb || kb < 0 || kb >= p.nb) return false;
-    if (qb < p.g || kb < p.g || abs(qb - kb) <= p.half) return true;
-    bool hit = false;
-    if (p.rand_idx)
-        for (int e = threadIdx.x & 31; e < p.r; e += 32) hit |= rand_entry(p, h, qb, e) == kb;
-    return __any_sync(kFullMask, hit);
 }
 
 // Longformer window geometry of head h: stride dilation + 1 and reach
@@ -201,10 +207,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *nsteps_s = reinterpret_cast<int *>(smem + C::MISC_OFF + 8);
     unsigned *bmap = reinterpret_cast<unsigned *>(smem + C::MAP_OFF);
     const int words = (p.nch + 31) / 32;
+    const ChunkTables ct = chunk_tables(p.nch);
+    unsigned long long *vbt = reinterpret_cast<unsigned long long *>(smem + C::MAP_OFF + ct.vb_off);
+    unsigned long long *gbt = reinterpret_cast<unsigned long long *>(smem + C::MAP_OFF + ct.gb_off);
+    unsigned *hvt = reinterpret_cast<unsigned *>(smem + C::MAP_OFF + ct.hv_off);
     const Ctl ctl{abort_flag, p.status, p.wait_ns};
+    const int sst = stats_stride(n);
 
     // ---------------------------------------------------------- setup
     for (int t = threadIdx.x; t < words; t += kThreads) bmap[t] = 0u;
+    for (int t = threadIdx.x; t < p.nch; t += kThreads) hvt[t] = 0u;
+    if (LF)
+        for (int t = threadIdx.x; t < p.nch; t += kThreads) gbt[t] = 0ull;
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(bar(C::B_TF), 1);
@@ -212,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::B_F + i), 1);
             mbar_init(bar(C::B_E + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NSL; ++i) {
             mbar_init(bar(C::B_SF + i), 1);
             mbar_init(bar(C::B_PF + i), 4);  // the four warps of the step's warpgroup
         }
@@ -228,18 +242,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA1);
-        prefetch_tmap(&tmA2);
-        prefetch_tmap(&tmB1);
-        prefetch_tmap(&tmB2);
-    }
     __syncthreads();
+    // The resident tile does not depend on the chunk list: start its copy now.
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tmB1);
+            prefetch_tmap(&tmB2);
+            mbar_arrive_expect_tx(bar(C::B_TF), 2 * C::TILE_BYTES);
+        }
+        __syncwarp();
+        if (lane < 4 * (D / 64)) {  // 2 tensors x 2 row halves x D/64 column regions
+            const int tsel = lane / (2 * (D / 64)), rem = lane % (2 * (D / 64));
+            const int rh = rem / (D / 64), dc = rem % (D / 64);
+            const uint32_t dst = sbase + (tsel ? C::A2_OFF : C::A1_OFF) + dc * C::REG_T + rh * 8192;
+            tma_load_3d(dst, tsel ? &tmA2 : &tmA1, bar(C::B_TF), dc * 64, t0 + rh * 64, bh);
+        }
+    }
 
-    // Mark the 64-row chunks this tile streams.
-    auto mark = [&](int lo, int hi) {  // chunks [lo, hi]
+    // Mark the 64-row chunks this tile streams, with the tile halves (64
+    // rows each) whose neighbourhood holds them.
+    auto mark = [&](int lo, int hi, unsigned halves) {  // chunks [lo, hi]
         for (int c = max(lo, 0) + (int)threadIdx.x; c <= min(hi, p.nch - 1); c += kThreads)
-            atomicOr(&bmap[c >> 5], 1u << (c & 31));
+            atomicOr(&hvt[c], halves);
     };
     int lstride = 1, lreach = 0;
     if (LF) {
@@ -256,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tile == 0 && bh == 0) atomicOr(p.status, kDevBadIndex);
                 continue;
             }
-            atomicOr(&bmap[(gp >> 6) >> 5], 1u << ((gp >> 6) & 31));
+            atomicOr(&hvt[gp >> 6], 3u);
+            atomicOr(&gbt[gp >> 6], 1ull << (gp & 63));
             tile_global |= (gp >= t0 && gp < t0 + kTM);
         }
         tile_global = __syncthreads_or(tile_global);
@@ -265,60 +290,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             // rows see: everything (a global row), else their band; causal: nothing later
             const int lo = tile_global ? 0 : max(0, t0 - lreach) >> 6;
             const int hi = p.causal ? last >> 6 : (tile_global ? p.nch - 1 : min(n - 1, last + lreach) >> 6);
-            mark(lo, hi);
+            mark(lo, hi, 3u);
         } else {
             // keys are seen by: every row (a global key), else the rows of their band;
             // causal: only rows at or after the key
             const int lo = p.causal ? (t0 >> 6) : (tile_global ? 0 : max(0, t0 - lreach) >> 6);
             const int hi = tile_global ? p.nch - 1 : min(n - 1, last + lreach) >> 6;
-            mark(lo, hi);
+            mark(lo, hi, 3u);
         }
     } else {
         const int cpb = p.b / 64;  // chunks per block
         const int nblk_tile = (p.b == 64) ? 2 : 1;
         for (int hb = 0; hb < nblk_tile; ++hb) {
             const int tb = (p.b == 64) ? 2 * tile + hb : tile;  // tile block (query or key)
+            const unsigned bit = (p.b == 64) ? (1u << hb) : 3u;
             if (tb >= p.nb) continue;
             if (PASS == kRowPass) {
+                // the key blocks query block tb sees
                 if (tb < p.g) {
-                    mark(0, p.nch - 1);
+                    mark(0, p.nch - 1, bit);
                 } else {
-                    mark(0, p.g * cpb - 1);
-                    mark(max(0, tb - p.half) * cpb, (min(p.nb - 1, tb + p.half) + 1) * cpb - 1);
+                    mark(0, p.g * cpb - 1, bit);
+                    mark(max(0, tb - p.half) * cpb, (min(p.nb - 1, tb + p.half) + 1) * cpb - 1, bit);
                     if (p.rand_idx)
                         for (int e = threadIdx.x; e < p.r; e += kThreads) {
                             const int kb = rand_entry(p, h, tb, e);
                             if (kb != INT_MAX)
-                                for (int c = kb * cpb; c < (kb + 1) * cpb; ++c)
-                                    atomicOr(&bmap[c >> 5], 1u << (c & 31));
+                                for (int c = kb * cpb; c < (kb + 1) * cpb; ++c) atomicOr(&hvt[c], bit);
                         }
                 }
             } else {
-                mark(0, p.g * cpb - 1);                 // global rows see everything
-                if (tb < p.g) mark(0, p.nch - 1);       // a global key block is seen by all
-                mark(max(0, tb - p.half) * cpb, (min(p.nb - 1, tb + p.half) + 1) * cpb - 1);
+                // the query blocks that see key block tb
+                mark(0, p.g * cpb - 1, bit);                // global rows see everything
+                if (tb < p.g) mark(0, p.nch - 1, bit);      // a global key block is seen by all
+                mark(max(0, tb - p.half) * cpb, (min(p.nb - 1, tb + p.half) + 1) * cpb - 1, bit);
                 if (p.rand_idx) {
                     const int cnt = (p.nb - p.g) * p.r;
                     for (int t = threadIdx.x; t < cnt; t += kThreads) {
                         const int qb = p.g + t / p.r;
                         if (rand_entry(p, h, qb, t % p.r) == tb)
-                            for (int c = qb * cpb; c < (qb + 1) * cpb; ++c) atomicOr(&bmap[c >> 5], 1u << (c & 31));
+                            for (int c = qb * cpb; c < (qb + 1) * cpb; ++c) atomicOr(&hvt[c], bit);
                     }
                 }
             }
         }
     }
     __syncthreads();
-    // Drop chunks without a valid entry (padding), then count the steps.
-    if (km) {
-        for (int c = threadIdx.x; c < p.nch; c += kThreads) {
-            if (!((bmap[c >> 5] >> (c & 31)) & 1u)) continue;
-            bool any = false;
-            for (int e = 0; e < kCN && !any; ++e) any = pos_valid(km, c * kCN + e, n);
-            if (!any) atomicAnd(&bmap[c >> 5], ~(1u << (c & 31)));
+    // Per marked chunk: validity bits; a chunk without a valid entry is
+    // dropped, the others go into the bitmap the roles walk.
+    for (int c = threadIdx.x; c < p.nch; c += kThreads) {
+        if (hvt[c] == 0u) continue;
+        const int y = c * kCN;
+        uint64_t vb = bits_below64(n - y);
+        if (km) {
+            vb = 0ull;
+            for (int e = 0; e < kCN && y + e < n; ++e) vb |= (uint64_t)(km[y + e] != 0) << e;
         }
-        __syncthreads();
+        vbt[c] = vb;
+        if (vb != 0ull) atomicOr(&bmap[c >> 5], 1u << (c & 31));
     }
+    __syncthreads();
     if (warp == 0) {
         int cnt = 0;
         for (int t = lane; t < words; t += 32) cnt += __popc(bmap[t]);
@@ -350,18 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ======================================================== producer
         uint32_t arms[C::NSTG] = {};
-        bool tile_armed = false, ok = true;
-        if (total > 0) {
-            if (lane == 0) mbar_arrive_expect_tx(bar(C::B_TF), 2 * C::TILE_BYTES);
-            __syncwarp();
-            if (lane < 4 * (D / 64)) {  // 2 tensors x 2 row halves x D/64 column regions
-                const int tsel = lane / (2 * (D / 64)), rem = lane % (2 * (D / 64));
-                const int rh = rem / (D / 64), dc = rem % (D / 64);
-                const uint32_t dst = sbase + (tsel ? C::A2_OFF : C::A1_OFF) + dc * C::REG_T + rh * 8192;
-                tma_load_3d(dst, tsel ? &tmA2 : &tmA1, bar(C::B_TF), dc * 64, t0 + rh * 64, bh);
-            }
-            tile_armed = true;
-        }
+        bool ok = true;
         Walk wk{0, bmap[0]};
         for (int g = 0; g < total && ok; ++g) {
             if (g == nsteps) wk = Walk{0, bmap[0]};  // row pass: second sweep
@@ -369,123 +389,115 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int y = c * kCN;
             const uint32_t st = g % C::NSTG;
             if (g >= C::NSTG && !(ok = wait_warp(bar(C::B_E + st), ((g / C::NSTG) - 1) & 1, ctl))) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar(C::B_F + st), 2 * C::CH_BYTES);
+            const uint32_t tx = 2 * C::CH_BYTES + (PASS == kKeyPass ? 2 * kCN * 4 : 0);
+            if (lane == 0) mbar_arrive_expect_tx(bar(C::B_F + st), tx);
             __syncwarp();
             if (lane < 2 * (D / 64)) {
                 const int tsel = lane / (D / 64), dc = lane % (D / 64);
                 const uint32_t dst = sbase + (tsel ? C::B2_OFF : C::B1_OFF) + st * C::CH_BYTES + dc * C::REG_C;
                 tma_load_3d(dst, tsel ? &tmB2 : &tmB1, bar(C::B_F + st), dc * 64, y, bh);
+            } else if (PASS == kKeyPass && lane < 2 * (D / 64) + 2) {
+                // the chunk rows' lse and D (rows of the padded stride; rows at
+                // or past n hold lse = +inf, D = 0)
+                const int which = lane - 2 * (D / 64);
+                const float *src = (which ? p.dl : p.lse) + (size_t)bh * sst + y;
+                bulk_load(sbase + C::LS_OFF + st * (2 * kCN * 4) + which * kCN * 4, src, kCN * 4, bar(C::B_F + st));
             }
             ++arms[st];
             // step record
             const uint32_t ii = g % kSI;
             if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
-            BwdStep &rec = steps[ii];
-            const unsigned lo = __ballot_sync(kFullMask, pos_valid(km, y + lane, n));
-            const unsigned hi = __ballot_sync(kFullMask, pos_valid(km, y + 32 + lane, n));
-            uint32_t allow = 3u;
-            uint64_t gb = 0ull;
-            if (LF) {
-                // global positions among [y, y + 64)
-                bool g0 = false, g1 = false;
-                if (p.ng > 0) {
-                    g0 = lf_is_global(p, y + lane);
-                    g1 = lf_is_global(p, y + 32 + lane);
-                }
-                gb = ((uint64_t)__ballot_sync(kFullMask, g1) << 32) | __ballot_sync(kFullMask, g0);
-            } else {
-                const int cb = c / (p.b / 64);  // chunk's block
-                allow = 0u;
-                for (int hb = 0; hb < 2; ++hb) {
-                    const int tb = (p.b == 64) ? 2 * tile + hb : tile;
-                    const bool a = (PASS == kRowPass) ? bb_allowed_warp(p, h, tb, cb) : bb_allowed_warp(p, h, cb, tb);
-                    allow |= a ? (1u << hb) : 0u;
-                }
-            }
-            if (PASS == kKeyPass) {
-                const float *lse = p.lse + (size_t)bh * n;
-                const float *dl = p.dl + (size_t)bh * n;
-                for (int e = lane; e < kCN; e += 32) {
-                    const bool v = y + e < n;
-                    rec.lse[e] = v ? __ldg(lse + y + e) : CUDART_INF_F;
-                    rec.dl[e] = v ? __ldg(dl + y + e) : 0.f;
-                }
-            }
             if (lane == 0) {
+                BwdStep &rec = steps[ii];
                 rec.y = y;
-                rec.allow = allow;
-                rec.vbits = ((uint64_t)hi << 32) | lo;
-                rec.gbits = gb;
+                rec.allow = hvt[c];
+                rec.vbits = vbt[c];
+                rec.gbits = LF ? gbt[c] : 0ull;
+                mbar_arrive(bar(C::B_IF + ii));
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_IF + ii));
         }
         if (!ok || *abort_flag) {
             // drain our copies in flight before the CTA leaves
             for (int i = 0; i < C::NSTG; ++i)
                 if (arms[i]) wait_drain(bar(C::B_F + i), (arms[i] - 1) & 1, p.wait_ns);
-            if (tile_armed) wait_drain(bar(C::B_TF), 0, p.wait_ns);
         }
+        // the resident tile copy was issued at start-up; with no steps (or on
+        // abort) nothing else waits for it
+        if (total == 0 || !ok || *abort_flag) wait_drain(bar(C::B_TF), 0, p.wait_ns);
     } else if (warp == 1) {
         // ======================================================== MMA issuer
-        if (lane == 0 && total > 0) {
+        // The whole warp runs the loop and the waits (so the descriptors and
+        // TMEM addresses stay warp-uniform); one elected lane, the same every
+        // time, issues the MMAs and the commits that track them.
+        if (total > 0) {
             constexpr uint32_t idesc_xy = idesc_bf16(kTM, kCN, false);
             constexpr uint32_t idesc_acc = idesc_bf16(kTM, D, true);
-            bool ok = wait_one(bar(C::B_TF), 0, ctl);
+            const bool leader = elect_one();
+            bool ok = wait_warp(bar(C::B_TF), 0, ctl);
             auto has_ts = [&](int g) { return PASS == kKeyPass || g >= nsteps; };
             const int first_ts = (PASS == kKeyPass) ? 0 : nsteps;
+            // Descriptors: built once, then advanced by the byte offset >> 4
+            // (the start-address field; every address stays below 256 KB).
+            const uint64_t dA1 = desc_sw128(sbase + C::A1_OFF, 16), dA2 = desc_sw128(sbase + C::A2_OFF, 16);
+            const uint64_t dB1 = desc_sw128(sbase + C::B1_OFF, 16), dB2 = desc_sw128(sbase + C::B2_OFF, 16);
+            const uint64_t dB1m = desc_sw128(sbase + C::B1_OFF, C::REG_C), dB2m = desc_sw128(sbase + C::B2_OFF, C::REG_C);
             auto issue_ts = [&](int hs) -> bool {
-                const uint32_t sl = hs & 1, st = hs % C::NSTG;
-                if (!wait_one(bar(C::B_PF + sl), (hs / 2) & 1, ctl)) return false;
+                const uint32_t sl = hs % C::NSL, st = hs % C::NSTG;
+                if (!wait_warp(bar(C::B_PF + sl), (hs / C::NSL) & 1, ctl)) return false;
                 tc_fence_after();
                 const uint32_t x = tmem + sl * 128;
-                const uint32_t b1 = sbase + C::B1_OFF + st * C::CH_BYTES;
-                const uint32_t b2 = sbase + C::B2_OFF + st * C::CH_BYTES;
+                const uint64_t so = (uint64_t)((st * C::CH_BYTES) >> 4);
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < kCN / 16; ++kk) {
-                    const uint32_t acc = (hs == first_ts && kk == 0) ? 0u : 1u;
-                    if (PASS == kRowPass) {
-                        // dQ += dS K
-                        mma_bf16_ts(tmem + C::ACC_COL, x + kk * 8, desc_sw128(b1 + kk * 2048, C::REG_C), idesc_acc,
-                                    acc);
-                    } else {
-                        // dV += P^T dO,  dK += dS^T Q
-                        mma_bf16_ts(tmem + C::ACC_COL, x + kk * 8, desc_sw128(b2 + kk * 2048, C::REG_C), idesc_acc,
-                                    acc);
-                        mma_bf16_ts(tmem + C::ACC_COL + D, x + 64 + kk * 8, desc_sw128(b1 + kk * 2048, C::REG_C),
-                                    idesc_acc, acc);
+                    for (int kk = 0; kk < kCN / 16; ++kk) {
+                        const uint32_t acc = (hs == first_ts && kk == 0) ? 0u : 1u;
+                        const uint64_t ko = so + (uint64_t)((kk * 2048) >> 4);
+                        if (PASS == kRowPass) {
+                            mma_bf16_ts(tmem + C::ACC_COL, x + kk * 8, dB1m + ko, idesc_acc, acc);  // dQ += dS K
+                        } else {
+                            mma_bf16_ts(tmem + C::ACC_COL, x + kk * 8, dB2m + ko, idesc_acc, acc);  // dV += P^T dO
+                            mma_bf16_ts(tmem + C::ACC_COL + D, x + 64 + kk * 8, dB1m + ko, idesc_acc,
+                                        acc);  // dK += dS^T Q
+                        }
                     }
+                    mma_commit(bar(C::B_E + st));
                 }
-                mma_commit(bar(C::B_E + st));
+                __syncwarp();
                 return true;
             };
-            int pend = -1;
+            // Step g's accumulate products are issued after X and Y of step
+            // g + NSL - 1 (in order, so before X of step g + NSL reuses the slot).
+            int next_ts = first_ts;  // oldest step whose accumulate products are pending
             for (int g = 0; g < total && ok; ++g) {
-                const uint32_t st = g % C::NSTG, sl = g & 1;
-                if (!(ok = wait_one(bar(C::B_F + st), (g / C::NSTG) & 1, ctl))) break;
-                // slot sl is free once step g-2's elementwise pass read it (its
-                // tensor-core products, if any, were issued before this point)
-                if (g >= 2 && !has_ts(g - 2) && !(ok = wait_one(bar(C::B_PF + sl), ((g - 2) / 2) & 1, ctl))) break;
+                const uint32_t st = g % C::NSTG, sl = g % C::NSL;
+                if (!(ok = wait_warp(bar(C::B_F + st), (g / C::NSTG) & 1, ctl))) break;
+                // a statistics step's slot is free once its elementwise pass read it
+                if (g >= C::NSL && !has_ts(g - C::NSL) &&
+                    !(ok = wait_warp(bar(C::B_PF + sl), ((g - C::NSL) / C::NSL) & 1, ctl)))
+                    break;
                 tc_fence_after();
-                const uint32_t b1 = sbase + C::B1_OFF + st * C::CH_BYTES;
-                const uint32_t b2 = sbase + C::B2_OFF + st * C::CH_BYTES;
+                const uint64_t so = (uint64_t)((st * C::CH_BYTES) >> 4);
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t toff = (kk >> 2) * C::REG_T + (kk & 3) * 32;
-                    const uint32_t coff = (kk >> 2) * C::REG_C + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + sl * 128, desc_sw128(sbase + C::A1_OFF + toff, 16), desc_sw128(b1 + coff, 16),
-                                idesc_xy, kk > 0 ? 1u : 0u);
-                    mma_bf16_ss(tmem + sl * 128 + 64, desc_sw128(sbase + C::A2_OFF + toff, 16),
-                                desc_sw128(b2 + coff, 16), idesc_xy, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t to = (uint64_t)(((kk >> 2) * C::REG_T + (kk & 3) * 32) >> 4);
+                        const uint64_t co = so + (uint64_t)(((kk >> 2) * C::REG_C + (kk & 3) * 32) >> 4);
+                        mma_bf16_ss(tmem + sl * 128, dA1 + to, dB1 + co, idesc_xy, kk > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + sl * 128 + 64, dA2 + to, dB2 + co, idesc_xy, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(C::B_SF + sl));
+                    if (!has_ts(g)) mma_commit(bar(C::B_E + st));
                 }
-                mma_commit(bar(C::B_SF + sl));
-                if (!has_ts(g)) mma_commit(bar(C::B_E + st));
-                if (pend >= 0 && !(ok = issue_ts(pend))) break;
-                pend = has_ts(g) ? g : -1;
+                __syncwarp();
+                while (ok && next_ts <= g - (C::NSL - 1)) ok = issue_ts(next_ts++);
             }
-            if (ok && pend >= 0) ok = issue_ts(pend);
-            mma_commit(bar(C::B_DONE));
-            mma_commit(bar(C::B_DRAIN));
+            while (ok && next_ts < total) ok = issue_ts(next_ts++);
+            if (leader) {
+                mma_commit(bar(C::B_DONE));
+                mma_commit(bar(C::B_DRAIN));
+            }
+            __syncwarp();
             wait_drain(bar(C::B_DRAIN), 0, p.wait_ns);
         }
         __syncwarp();
@@ -522,13 +534,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (row pass, first sweep) or form P and dS (bf16) and write them back
         // over the slot's first columns for the accumulate products.
         auto run_step = [&](int g, bool stats) -> bool {
-            const uint32_t ii = g % kSI, sl = g & 1;
+            const uint32_t ii = g % kSI, sl = g % C::NSL;
             if (!wait_warp(bar(C::B_IF + ii), (g / kSI) & 1, ctl)) return false;
             const BwdStep &rec = steps[ii];
             const uint64_t mk = step_mask(rec);
-            if (!wait_warp(bar(C::B_SF + sl), (g / 2) & 1, ctl)) return false;
+            if (!wait_warp(bar(C::B_SF + sl), (g / C::NSL) & 1, ctl)) return false;
             tc_fence_after();
             const uint32_t xa = tmem + lane_addr + sl * 128;
+            // key pass: the chunk rows' lse and D, landed with the stage (the
+            // MMA waited for the stage before X and Y, so SF implies them)
+            const float *lsd = reinterpret_cast<const float *>(smem + C::LS_OFF + (g % C::NSTG) * (2 * kCN * 4));
             uint32_t pw[32], dw[32];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -538,38 +553,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 const uint32_t mh = (uint32_t)(mk >> (32 * hh));
                 if (stats) {
+                    // scaled scores (masked: -inf), their maximum, then the
+                    // rescaled sums l and u in packed fp32 pairs
+                    const uint64_t c2 = f2_pack(sl2, sl2);
                     float mx = -CUDART_INF_F;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        xv[j] = ((mh >> j) & 1u) ? xv[j] * sl2 : -CUDART_INF_F;
-                        mx = fmaxf(mx, xv[j]);
+                    for (int j = 0; j < 32; j += 2) {
+                        float a, b;
+                        f2_unpack(f2_fma(f2_pack(xv[j], xv[j + 1]), c2, 0ull), a, b);
+                        xv[j] = ((mh >> j) & 1u) ? a : -CUDART_INF_F;
+                        xv[j + 1] = ((mh >> (j + 1)) & 1u) ? b : -CUDART_INF_F;
+                        mx = fmax3(mx, xv[j], xv[j + 1]);
                     }
                     const float mn = fmaxf(m, mx);
                     if (mn != -CUDART_INF_F) {
                         const float alpha = ex2(m - mn);
-                        float ls = 0.f, us = 0.f;
+                        uint64_t ls2 = 0ull, us2 = 0ull;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float e = ex2(xv[j] - mn);
-                            ls += e;
-                            us = fmaf(e, yv[j], us);
+                        for (int j = 0; j < 32; j += 2) {
+                            const uint64_t e2 = f2_pack(ex2(xv[j] - mn), ex2(xv[j + 1] - mn));
+                            ls2 = f2_add(ls2, e2);
+                            us2 = f2_fma(e2, f2_pack(yv[j], yv[j + 1]), us2);
                         }
-                        l = fmaf(l, alpha, ls);
-                        u = fmaf(u, alpha, us);
+                        float la, lb, ua, ub;
+                        f2_unpack(ls2, la, lb);
+                        f2_unpack(us2, ua, ub);
+                        l = fmaf(l, alpha, la + lb);
+                        u = fmaf(u, alpha, ua + ub);
                         m = mn;
                     }
                 } else {
+                    // P = 2^(s c - lse) on the allowed columns, dS = P (dP - D)
+                    const uint64_t c2 = f2_pack(sl2, sl2);
+                    const uint64_t nl_row = f2_pack(-lse, -lse), nd_row = f2_pack(-dlv, -dlv);
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
                         const int c = 32 * hh + j;
-                        const float la = (PASS == kRowPass) ? lse : rec.lse[c];
-                        const float lb = (PASS == kRowPass) ? lse : rec.lse[c + 1];
-                        const float da = (PASS == kRowPass) ? dlv : rec.dl[c];
-                        const float db = (PASS == kRowPass) ? dlv : rec.dl[c + 1];
-                        const float p0 = ((mh >> j) & 1u) ? ex2(fmaf(xv[j], sl2, -la)) : 0.f;
-                        const float p1 = ((mh >> (j + 1)) & 1u) ? ex2(fmaf(xv[j + 1], sl2, -lb)) : 0.f;
+                        uint64_t nl = nl_row, nd = nd_row;
+                        if (PASS == kKeyPass) {
+                            const float2 lv = *reinterpret_cast<const float2 *>(lsd + c);
+                            const float2 dv = *reinterpret_cast<const float2 *>(lsd + kCN + c);
+                            nl = f2_pack(-lv.x, -lv.y);
+                            nd = f2_pack(-dv.x, -dv.y);
+                        }
+                        float ta, tb;
+                        f2_unpack(f2_fma(f2_pack(xv[j], xv[j + 1]), c2, nl), ta, tb);
+                        const float p0 = ((mh >> j) & 1u) ? ex2(ta) : 0.f;
+                        const float p1 = ((mh >> (j + 1)) & 1u) ? ex2(tb) : 0.f;
+                        const uint64_t p2 = f2_pack(p0, p1);
+                        float da, db;
+                        f2_unpack(f2_fma(p2, f2_add(f2_pack(yv[j], yv[j + 1]), nd), 0ull), da, db);
                         __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-                        __nv_bfloat162 dd = __floats2bfloat162_rn(p0 * (yv[j] - da), p1 * (yv[j + 1] - db));
+                        __nv_bfloat162 dd = __floats2bfloat162_rn(da, db);
                         pw[c >> 1] = *reinterpret_cast<uint32_t *>(&pp);
                         dw[c >> 1] = *reinterpret_cast<uint32_t *>(&dd);
                     }
@@ -618,9 +653,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dlv = lt > 0.f ? ut / lt : 0.f;
                     stat[row] = lse;
                     stat[kTM + row] = dlv;
-                    if (pos < n) {
-                        p.lse[(size_t)bh * n + pos] = lse;
-                        p.dl[(size_t)bh * n + pos] = dlv;
+                    if (pos < sst) {
+                        p.lse[(size_t)bh * sst + pos] = lse;
+                        p.dl[(size_t)bh * sst + pos] = dlv;
                     }
                 }
                 named_bar_sync(1, 256);
@@ -672,9 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (PASS == kRowPass && nsteps == 0 && pos < n && wg == 0) {
-            p.lse[(size_t)bh * n + pos] = CUDART_INF_F;
-            p.dl[(size_t)bh * n + pos] = 0.f;
+        if (PASS == kRowPass && nsteps == 0 && pos < sst && wg == 0) {
+            p.lse[(size_t)bh * sst + pos] = CUDART_INF_F;
+            p.dl[(size_t)bh * sst + pos] = 0.f;
         }
     }
     tc_fence_before();
@@ -716,7 +751,7 @@ bool make_map(CUtensorMap *m, const void *base, int BH, int n, int d) {
 
 template <int D>
 size_t bwd_smem_bytes(int nch) {
-    return (size_t)BwdCfg<D>::MAP_OFF + 4 * (size_t)((nch + 31) / 32) + 1024;  // + alignment slack
+    return (size_t)BwdCfg<D>::MAP_OFF + (size_t)chunk_tables(nch).bytes + 1024;  // + alignment slack
 }
 
 template <int D>
@@ -773,7 +808,7 @@ cudaError_t launch_tc_bwd(const Problem &pr, const TcConfig &cfg, cudaStream_t s
     bp.dK = static_cast<__nv_bfloat16 *>(pr.dK);
     bp.dV = static_cast<__nv_bfloat16 *>(pr.dV);
     bp.lse = pr.row_stats;
-    bp.dl = pr.row_stats + (size_t)pr.B * pr.H * pr.n;
+    bp.dl = pr.row_stats + (size_t)pr.B * pr.H * stats_stride(pr.n);
     bp.status = pr.status;
     *launches = 2;
     if (pr.d == 64) return launch_d<64>(pr, bp, stream);

@@ -4,7 +4,8 @@ BigBird-ITC shapes follow the paper's App. E Tab. 8 (block b = 64, g = 2b,
 w = 3b, r = 3b tokens, i.e. 2 global, 3 window and 3 random blocks, n = 4096,
 12 heads) and Longformer's Sec. 3.1 (window 512, i.e. 256 tokens each side,
 global attention on a few chosen positions). The long and padded variants
-stretch the same pattern to n = 16384 and n = 65536.
+stretch the same pattern to n = 16384 and n = 65536. The two ``*_bwd_*``
+workloads time the backward (dQ, dK, dV) on the n = 4096 shapes.
 """
 
 from dataclasses import dataclass, field
@@ -31,6 +32,7 @@ class Workload:
     cfg_id: int = 0
     tol_max: float = 2e-2
     tol_mean: float = 2e-3
+    grad: bool = False   # time the backward instead of the forward
 
 
 WORKLOADS = {
@@ -48,6 +50,11 @@ WORKLOADS = {
     "bigbird_bf16_n65536_d128": Workload(
         "bigbird_bf16_n65536_d128", "bigbird", B=1, H=16, n=65536, d=128, dtype="bf16",
         sigma=0.5, b=128, cfg_id=5),
+    "bigbird_bwd_bf16_n4096": Workload(
+        "bigbird_bwd_bf16_n4096", "bigbird", B=8, H=12, n=4096, d=64, dtype="bf16", cfg_id=2, grad=True),
+    "longformer_bwd_bf16_n4096": Workload(
+        "longformer_bwd_bf16_n4096", "longformer", B=4, H=12, n=4096, d=64, dtype="bf16",
+        window=512, n_global=16, cfg_id=3, grad=True),
 }
 
 HEADLINE = "bigbird_bf16_n4096"

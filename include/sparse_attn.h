@@ -185,8 +185,8 @@ sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, vo
  * Arithmetic: fp32 softmax statistics and accumulation (bf16 inputs are
  *   widened exactly; outputs are rounded to the storage dtype).
  *   Deterministic: no atomics; every sum runs in a fixed order.
- * Scratch: 2 * B * H * n floats of per-row statistics in the workspace
- *   (sa_attn_bwd_workspace_bytes).
+ * Scratch: 2 * B * H * n64 floats of per-row statistics in the workspace,
+ *   n64 = n rounded up to a multiple of 64 (sa_attn_bwd_workspace_bytes).
  * Errors: as for bigbird_attn_fwd, plus SA_ERR_INVALID_ARG when an output
  *   aliases an input or another output.
  */

@@ -183,4 +183,5 @@ def test_longformer_bwd_invalid_args(lib, bad):
 
 def test_bwd_workspace_bytes(lib):
     assert lib.sa_attn_bwd_workspace_bytes(8, 12, 4096, 64) == 2 * 4 * 8 * 12 * 4096
+    assert lib.sa_attn_bwd_workspace_bytes(1, 2, 1000, 64) == 2 * 4 * 2 * 1024  # rows padded to 64
     assert lib.sa_attn_bwd_workspace_bytes(1, 1, 100, 96) == 0
