@@ -797,36 +797,48 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
     } else if (role == 1) {
         // ================================================================ MMA issuer (tile x)
-        if (lane == 0) {
+        // The whole warp runs the loop and the waits, so descriptors and TMEM
+        // addresses stay warp-uniform; one elected lane, the same every time,
+        // issues the MMAs and the commits that track them.
+        {
             constexpr uint32_t idesc_qk = idesc_bf16(128, C::KB, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
+            const bool leader = elect_one();
             uint32_t g = 0, qcnt = 0;
             int pend = -1;
             bool pend_first = false;
             uint32_t pend_ob = 0;
             bool ok = true;
+            // descriptors built once and advanced by (byte offset >> 4): the
+            // start-address field, every address below 256 KB
+            const uint64_t dQ0 = desc_sw128(tbase + C::Q_OFF, 16);
+            const uint64_t dK0 = desc_sw128(tbase + C::K_OFF, 16);
+            const uint64_t dV0 = desc_sw128(tbase + C::V_OFF, C::KV_REGION);
             // O_ob (+)= P_h V_h; P_h is read from TMEM over S buffer h % NS
             auto issue_pv = [&](uint32_t h, bool first, uint32_t ob) -> bool {
                 const uint32_t sv = h % C::VST, sb = h % C::NS;
-                if (!wait_one(bar(C::B_PF + sb), (h / C::NS) & 1, ctl)) return false;
-                if (!wait_one(bar(C::B_VF + sv), (h / C::VST) & 1, ctl)) return false;
+                if (!wait_warp(bar(C::B_PF + sb), (h / C::NS) & 1, ctl)) return false;
+                if (!wait_warp(bar(C::B_VF + sv), (h / C::VST) & 1, ctl)) return false;
                 tc_fence_after();
                 const uint32_t pt = tmem + sb * C::KB;
-                const uint32_t va = tbase + C::V_OFF + sv * C::KV_BYTES;
+                const uint64_t vo = (uint64_t)((sv * C::KV_BYTES) >> 4);
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < C::KB / 16; ++kk) {
-                    const uint64_t b = desc_sw128(va + kk * 2048, C::KV_REGION);
-                    mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < C::KB / 16; ++kk)
+                        mma_bf16_ts(tmem + C::O_COL + ob * D, pt + kk * 8, dV0 + vo + (uint64_t)((kk * 2048) >> 4),
+                                    idesc_pv, (first && kk == 0) ? 0u : 1u);
+                    mma_commit(bar(C::B_PV + sb));
                 }
-                mma_commit(bar(C::B_PV + sb));
+                __syncwarp();
                 return true;
             };
             for (uint32_t ui_idx = 0; ok; ++ui_idx) {
                 const uint32_t slot = ui_idx % kNU;
-                if (!(ok = wait_one(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
+                if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
                 const int kind = ring[slot].kind;
                 const int n_steps = ring[slot].n_steps;
-                mbar_arrive(bar(C::B_UE + slot));
+                __syncwarp();
+                if (leader) mbar_arrive(bar(C::B_UE + slot));
                 if (kind == kUnitEnd) break;
                 if (n_steps == 0) {
                     // The softmax writes the previous unit's epilogue while it handles
@@ -838,23 +850,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     continue;
                 }
                 const uint32_t ob = qcnt & 1;
-                if (!(ok = wait_one(bar(C::B_QF), qcnt & 1, ctl))) break;
+                if (!(ok = wait_warp(bar(C::B_QF), qcnt & 1, ctl))) break;
                 tc_fence_after();
-                const uint32_t qa = tbase + C::Q_OFF;
                 for (int t = 0; t < n_steps; ++t, ++g) {
                     const uint32_t sk = g % C::KST, sb = g % C::NS;
-                    if (!(ok = wait_one(bar(C::B_KF + sk), (g / C::KST) & 1, ctl))) break;
+                    if (!(ok = wait_warp(bar(C::B_KF + sk), (g / C::KST) & 1, ctl))) break;
                     tc_fence_after();
-                    const uint32_t ka = tbase + C::K_OFF + sk * C::KV_BYTES;
+                    const uint64_t ko = (uint64_t)((sk * C::KV_BYTES) >> 4);
+                    if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qoff = (kk >> 2) * kRegionBytes + (kk & 3) * 32;
-                        const uint32_t koff = (kk >> 2) * C::KV_REGION + (kk & 3) * 32;
-                        mma_bf16_ss(tmem + sb * C::KB, desc_sw128(qa + qoff, 16), desc_sw128(ka + koff, 16),
-                                    idesc_qk, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t qoff = (uint64_t)(((kk >> 2) * kRegionBytes + (kk & 3) * 32) >> 4);
+                            const uint64_t koff = ko + (uint64_t)(((kk >> 2) * C::KV_REGION + (kk & 3) * 32) >> 4);
+                            mma_bf16_ss(tmem + sb * C::KB, dQ0 + qoff, dK0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(C::B_SF + sb));
+                        if (t == n_steps - 1) mma_commit(bar(C::B_QE));
                     }
-                    mma_commit(bar(C::B_SF + sb));
-                    if (t == n_steps - 1) mma_commit(bar(C::B_QE));
+                    __syncwarp();
                     // two S slots: S_g overlaps the softmax of step g-1, then PV_{g-1}
                     if (pend >= 0 && !(ok = issue_pv((uint32_t)pend, pend_first, pend_ob))) break;
                     pend = (int)g;
@@ -864,8 +877,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 ++qcnt;
             }
             if (ok && pend >= 0) issue_pv((uint32_t)pend, pend_first, pend_ob);
-            // drain: every MMA issued by this thread has completed once this arrives
-            mma_commit(bar(C::B_DRAIN));
+            // drain: every MMA issued by the leader has completed once this arrives
+            if (leader) mma_commit(bar(C::B_DRAIN));
+            __syncwarp();
             wait_drain(bar(C::B_DRAIN), 0, G.wait_ns);
         }
     } else if (role == 3 || role == 4) {
