@@ -39,6 +39,7 @@ METRIC_BWD = "useful TFLOP/s and tokens/s of sparse attn bwd (dQ, dK, dV) at n=4
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 TC_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_kernel.cuh")
+TC_BWD_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_bwd.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -94,13 +95,13 @@ def file_sha(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def read_traffic(kernel, workload):
+def read_traffic(kernel, workload, source=TC_SOURCE):
     """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         entries = json.load(f)
-    sha = file_sha(TC_SOURCE)
+    sha = file_sha(source)
     for e in entries:
         if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source_sha") == sha:
             return e.get("dram_bytes_per_launch")
@@ -384,7 +385,7 @@ def main(argv=None):
     if wl.grad:
         # one call launches the row pass and the key pass; they are timed together
         kernel_name = f"sparse_tc_bwd<{wl.d},rows> + sparse_tc_bwd<{wl.d},keys>"
-    traffic = read_traffic(kernel_name, wl.name)
+    traffic = read_traffic(kernel_name, wl.name, TC_BWD_SOURCE if wl.grad else TC_SOURCE)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 dense burst (cuBLAS)", "kernel": kernel_name,
