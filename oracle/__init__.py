@@ -18,6 +18,7 @@ Sources (web pages on block-sparse long-sequence attention):
   * "Longformer: The Long-Document Transformer" (Beltagy et al.): sliding
     window and symmetric global attention (Sec. 3.1), the dilated sliding
     window (Sec. 3.1, Fig. 2(c); per-head dilation, Tab. 12), the
+    separate projections for global attention (Sec. 3.1), the
     autoregressive mode (App. B), scaled dot-product attention (Sec. 3.1,
     Eq. 1), and the slow per-diagonal "loop" variant used only for testing
     (Sec. 3.2, App. A), whose role this oracle plays.
@@ -34,6 +35,9 @@ Every function pinned by a test that does not reuse this code; the pins are in
                            causal mode: enumeration of the window positions,
                            torch is_causal attention, per-residue-class full
                            attention, hand-derived pair counts)
+  oracle_longformer with   pinned (global rows = torch SDPA of Qg, Kg, Vg over
+  separate global          their keys; other rows identical to the single-
+  projections              projection oracle; same tensors give the same result)
   masked_attention         pinned (torch float64 scaled_dot_product_attention
                            on full/block-diagonal/truncated cases, scalar-loop
                            brute force, single-key and row-sum identities)

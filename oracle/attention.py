@@ -164,16 +164,28 @@ def oracle_bigbird(Q, K, V, b, g, w, rand_table, key_mask=None, rows=None,
 
 
 def oracle_longformer(Q, K, V, window, global_idx, key_mask=None, rows=None,
-                      row_chunk=1024, dilation=None, causal=False):
+                      row_chunk=1024, dilation=None, causal=False, Qg=None, Kg=None, Vg=None):
     """Longformer sliding-window + global attention forward, float64.
 
     ``dilation``: per-head dilation [H] (None: 0 for every head); ``causal``:
     autoregressive mode. See ``longformer_allowed``.
+
+    Separate projections for global attention (Longformer Sec. 3.1, "Linear
+    Projections for Global Attention"): with ``Qg``, ``Kg``, ``Vg`` given
+    ([B, H, n, d] each), the row of a global token is computed from Qg against
+    Kg and Vg over every key it may see, and every other row from Q, K, V as
+    usual (including its scores against global keys). Without them the global
+    rows use Q, K, V.
     """
     Q, K, V = _as_f64(Q), _as_f64(K), _as_f64(V)
+    sep = Qg is not None
+    if sep:
+        Qg, Kg, Vg = _as_f64(Qg), _as_f64(Kg), _as_f64(Vg)
     B, H, n, d = Q.shape
     dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
     rows = np.arange(n) if rows is None else np.asarray(rows)
+    is_global = np.zeros(n, dtype=bool)
+    is_global[np.asarray(global_idx, dtype=np.int64)] = True
     out = np.zeros((B, H, len(rows), d), dtype=np.float64)
     for beta in range(B):
         kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
@@ -184,8 +196,13 @@ def oracle_longformer(Q, K, V, window, global_idx, key_mask=None, rows=None,
                 if dil[h] not in masks:
                     masks[dil[h]] = _apply_validity(
                         longformer_allowed(n, window, global_idx, rr, dilation=dil[h], causal=causal), rr, kv)
-                out[beta, h, c0:c0 + len(rr)] = masked_attention(
-                    Q[beta, h, rr], K[beta, h], V[beta, h], masks[dil[h]])
+                mask = masks[dil[h]]
+                o = masked_attention(Q[beta, h, rr], K[beta, h], V[beta, h], mask)
+                if sep:
+                    g = is_global[rr]
+                    if g.any():
+                        o[g] = masked_attention(Qg[beta, h, rr[g]], Kg[beta, h], Vg[beta, h], mask[g])
+                out[beta, h, c0:c0 + len(rr)] = o
     return out
 
 

@@ -555,3 +555,27 @@ def test_bf16_rounded_factors_stay_inside_the_term_bound():
     assert np.all(np.abs(sc * (dSb - dS) @ k) <= 2.0 ** -9 * qa + 1e-15)
     assert np.all(np.abs(sc * (dSb - dS).T @ q) <= 2.0 ** -9 * ka + 1e-15)
     assert np.all(np.abs((Pb - P).T @ do) <= 2.0 ** -9 * va + 1e-15)
+
+
+# ---------------------------------------------------------------------------
+# Longformer separate projections for global attention (Sec. 3.1)
+# ---------------------------------------------------------------------------
+
+def test_longformer_global_projections_split_rows():
+    """Global rows equal full softmax attention of (Qg, Kg, Vg) over the keys
+    they see (torch SDPA); the other rows equal the single-projection oracle
+    and ignore Qg, Kg, Vg."""
+    n, window, d = 200, 16, 8
+    gidx = np.array([0, 3, 150])
+    Q, K, V, Qg, Kg, Vg = (_rand((1, 1, n, d), s) for s in (71, 72, 73, 74, 75, 76))
+    for causal in (False, True):
+        got = oracle_longformer(Q, K, V, window, gidx, causal=causal, Qg=Qg, Kg=Kg, Vg=Vg)[0, 0]
+        plain = oracle_longformer(Q, K, V, window, gidx, causal=causal)[0, 0]
+        other = np.setdiff1d(np.arange(n), gidx)
+        np.testing.assert_allclose(got[other], plain[other], rtol=0, atol=0)
+        mask = longformer_allowed(n, window, gidx, causal=causal)
+        want = _sdpa(Qg[0, 0, gidx], Kg[0, 0], Vg[0, 0], mask[gidx])
+        np.testing.assert_allclose(got[gidx], want, atol=1e-12, rtol=1e-10)
+    # the same tensors as both sets give the plain oracle
+    same = oracle_longformer(Q, K, V, window, gidx, Qg=Q, Kg=K, Vg=V)
+    np.testing.assert_allclose(same, oracle_longformer(Q, K, V, window, gidx), rtol=0, atol=0)
