@@ -77,12 +77,14 @@ def bigbird_attn_fwd(Q, K, V, b, g, w, r, rand_idx, key_mask=None, out=None, str
 
 
 def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, stream=None, dilation=None,
-                        causal=False):
+                        causal=False, Qg=None, Kg=None, Vg=None):
     """Longformer sliding-window + global attention forward; returns O.
 
     global_idx: int32 CUDA tensor of sorted unique positions (may be empty or None).
     dilation: int32 CUDA tensor [H] of per-head dilations, or None (all 0).
     causal: autoregressive mode (no key after the query).
+    Qg, Kg, Vg: the separate projections for global attention (all three or none):
+    global rows are computed from them, every other row from Q, K, V.
     """
     _check_qkv(Q, K, V)
     B, H, n, d = Q.shape
@@ -98,11 +100,18 @@ def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, st
     if dilation is not None and (not dilation.is_cuda or dilation.dtype != torch.int32
                                  or not dilation.is_contiguous() or dilation.numel() != H):
         raise ValueError("dilation must be a contiguous int32 CUDA tensor with one entry per head")
-    st = _lib.lib().longformer_attn_fwd_ex(
-        _ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, n, d, window, _ptr(dilation), 1 if causal else 0,
-        _ptr(global_idx if n_global else None), n_global, _ptr(key_mask), _DTYPE[Q.dtype],
-        _stream_handle(stream, Q.device))
-    _lib.check(st, "longformer_attn_fwd_ex")
+    sep = (Qg, Kg, Vg)
+    if any(t is not None for t in sep):
+        if any(t is None for t in sep):
+            raise ValueError("pass all of Qg, Kg, Vg or none")
+        _check_qkv(Qg, Kg, Vg)
+        if Qg.shape != Q.shape or Qg.dtype != Q.dtype or Qg.device != Q.device:
+            raise ValueError("Qg, Kg, Vg must match Q in shape, dtype and device")
+    st = _lib.lib().longformer_attn_fwd_gproj(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(Qg), _ptr(Kg), _ptr(Vg), _ptr(out), B, H, n, d, window,
+        _ptr(dilation), 1 if causal else 0, _ptr(global_idx if n_global else None), n_global, _ptr(key_mask),
+        _DTYPE[Q.dtype], _stream_handle(stream, Q.device))
+    _lib.check(st, "longformer_attn_fwd_gproj")
     return out
 
 

@@ -250,10 +250,24 @@ sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void 
 sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
                                  int window, const int32_t *dilation, int causal, const int32_t *global_idx,
                                  int n_global, const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream) {
+    return longformer_attn_fwd_gproj(Q, K, V, nullptr, nullptr, nullptr, O, B, H, n, d, window, dilation, causal,
+                                     global_idx, n_global, key_mask, dtype, stream);
+}
+
+sa_status longformer_attn_fwd_gproj(const void *Q, const void *K, const void *V, const void *Qg, const void *Kg,
+                                    const void *Vg, void *O, int B, int H, int n, int d, int window,
+                                    const int32_t *dilation, int causal, const int32_t *global_idx, int n_global,
+                                    const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream) {
     if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
     sa_status s = check_tensors(Q, K, V, O);
     if (s != SA_OK) return s;
+    // the separate set: all three or none, aligned, never aliasing O
+    const bool sep = Qg || Kg || Vg;
+    if (sep) {
+        s = check_tensors(Qg, Kg, Vg, O);
+        if (s != SA_OK) return s;
+    }
     s = longformer_args_ok(B, H, n, d, window, global_idx, n_global);
     if (s != SA_OK) return s;
     sa::Problem p = {};
@@ -266,6 +280,11 @@ sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, vo
     p.dilation = dilation;
     p.causal = causal;
     p.key_mask = key_mask;
+    if (sep) {
+        p.Qg = Qg;
+        p.Kg = Kg;
+        p.Vg = Vg;
+    }
     return run(p, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 

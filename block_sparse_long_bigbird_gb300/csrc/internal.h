@@ -34,6 +34,8 @@ struct Problem {
     int n_global;
     const int32_t *dilation;  // device [H] or NULL (dilated sliding window)
     int causal;               // autoregressive mode
+    // separate projections for global attention (NULL: global rows use Q, K, V)
+    const void *Qg, *Kg, *Vg;
     // both
     const uint8_t *key_mask;
     unsigned int *status;  // device status word

@@ -221,8 +221,11 @@ __global__ void __launch_bounds__(kThreads) bigbird_simt_kernel(Problem p) {
 // [i0 - reach, i0 + 63 + reach] plus those holding a global key, where
 // reach = (window / 2) (dilation + 1) ("Longformer", Sec. 3.1: dilated
 // window); the causal mode (App. B) drops everything after the query.
+// mode: 0 computes every row; with separate projections for global attention
+// (Sec. 3.1) the call runs twice, mode 1 (Q, K, V; global rows not stored)
+// and mode 2 (Qg, Kg, Vg; only global rows, tiles without one exit early).
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
+__global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p, int mode) {
     constexpr int BQ = 64;
     using L = Layout<D, BQ>;
     constexpr int R = BQ / kWarps;
@@ -243,9 +246,10 @@ __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
     const int reach = (int)min((long long)half * stride, (long long)n);
     const bool causal = p.causal != 0;
     const size_t head_off = (size_t)bh * n * D;
-    const T *Qh = static_cast<const T *>(p.Q) + head_off;
-    const T *Kh = static_cast<const T *>(p.K) + head_off;
-    const T *Vh = static_cast<const T *>(p.V) + head_off;
+    const bool gset = (mode == 2);
+    const T *Qh = static_cast<const T *>(gset ? p.Qg : p.Q) + head_off;
+    const T *Kh = static_cast<const T *>(gset ? p.Kg : p.K) + head_off;
+    const T *Vh = static_cast<const T *>(gset ? p.Vg : p.V) + head_off;
     T *Oh = static_cast<T *>(p.O) + head_off;
     const uint8_t *km = p.key_mask ? p.key_mask + (size_t)beta * n : nullptr;
     const int32_t *gidx = p.global_idx;
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
     }
     __syncthreads();
     const bool tile_has_global = (misc[0] | misc[1]) != 0u;
+    if (mode == 2 && !tile_has_global) return;  // block-uniform
     {
         const int lo = tile_has_global ? 0 : max(0, i0 - reach) / kChunk;
         const int hi = causal ? min(n - 1, i0 + BQ - 1) / kChunk
@@ -335,14 +340,28 @@ __global__ void __launch_bounds__(kThreads) longformer_simt_kernel(Problem p) {
             __syncthreads();
         }
     }
-    write_rows<T, D, R>(Oh, i0 + row0, n, l, acc);
+    if (mode == 0) {
+        write_rows<T, D, R>(Oh, i0 + row0, n, l, acc);
+    } else {
+        // mode 1 stores the non-global rows, mode 2 the global ones
+        constexpr int DL = D / 32;
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int i = i0 + row0 + rr;
+            if (i >= n || qglobal[rr] != (mode == 2)) continue;
+            const float inv = l[rr] > 0.f ? 1.f / l[rr] : 0.f;
+#pragma unroll
+            for (int j = 0; j < DL; ++j) store_val(Oh + (size_t)i * D + lane * DL + j, acc[rr][j] * inv);
+        }
+    }
 }
 
-template <class KernelFn>
-cudaError_t launch_with_smem(KernelFn kernel, dim3 grid, size_t smem, const Problem &p, cudaStream_t s) {
+template <class KernelFn, class... Args>
+cudaError_t launch_with_smem(KernelFn kernel, dim3 grid, size_t smem, cudaStream_t s, Args... args) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, smem, s>>>(p);
+    kernel<<<grid, kThreads, smem, s>>>(args...);
     return cudaGetLastError();
 }
 
@@ -359,27 +378,33 @@ cudaError_t launch_typed(const Problem &p, cudaStream_t s) {
         const int nb = p.n / p.b;
         dim3 grid(nb, BH);
         if (p.d == 64 && p.b == 64)
-            return launch_with_smem(bigbird_simt_kernel<T, 64, 64>, grid, smem_bytes<T, 64, 64>(nb), p, s);
+            return launch_with_smem(bigbird_simt_kernel<T, 64, 64>, grid, smem_bytes<T, 64, 64>(nb), s, p);
         if (p.d == 64 && p.b == 128)
-            return launch_with_smem(bigbird_simt_kernel<T, 64, 128>, grid, smem_bytes<T, 64, 128>(nb), p, s);
+            return launch_with_smem(bigbird_simt_kernel<T, 64, 128>, grid, smem_bytes<T, 64, 128>(nb), s, p);
         if (p.d == 128 && p.b == 64)
-            return launch_with_smem(bigbird_simt_kernel<T, 128, 64>, grid, smem_bytes<T, 128, 64>(nb), p, s);
+            return launch_with_smem(bigbird_simt_kernel<T, 128, 64>, grid, smem_bytes<T, 128, 64>(nb), s, p);
         if (p.d == 128 && p.b == 128)
-            return launch_with_smem(bigbird_simt_kernel<T, 128, 128>, grid, smem_bytes<T, 128, 128>(nb), p, s);
+            return launch_with_smem(bigbird_simt_kernel<T, 128, 128>, grid, smem_bytes<T, 128, 128>(nb), s, p);
         return cudaErrorInvalidValue;
     }
     const int tiles = (p.n + 63) / 64;
     const int nch = (p.n + kChunk - 1) / kChunk;
     dim3 grid(tiles, BH);
-    if (p.d == 64) return launch_with_smem(longformer_simt_kernel<T, 64>, grid, smem_bytes<T, 64, 64>(nch), p, s);
-    if (p.d == 128) return launch_with_smem(longformer_simt_kernel<T, 128>, grid, smem_bytes<T, 128, 64>(nch), p, s);
-    return cudaErrorInvalidValue;
+    const bool sep = p.Qg != nullptr && p.n_global > 0;
+    for (int mode = sep ? 1 : 0; mode <= (sep ? 2 : 0); ++mode) {
+        cudaError_t e = cudaErrorInvalidValue;
+        if (p.d == 64) e = launch_with_smem(longformer_simt_kernel<T, 64>, grid, smem_bytes<T, 64, 64>(nch), s, p, mode);
+        if (p.d == 128)
+            e = launch_with_smem(longformer_simt_kernel<T, 128>, grid, smem_bytes<T, 128, 64>(nch), s, p, mode);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_simt(const Problem &p, sa_dtype dtype, cudaStream_t stream, int *launches) {
-    *launches = 1;
+    *launches = (p.kind == kLongformer && p.Qg != nullptr && p.n_global > 0) ? 2 : 1;
     if (dtype == SA_FP32) return launch_typed<float>(p, stream);
     return launch_typed<__nv_bfloat16>(p, stream);
 }

@@ -22,10 +22,11 @@
 //     holds the tile's keys (the transposed pattern): X = K Q^T = S^T,
 //     Y = V dO^T = dP^T, P^T and dS^T (bf16) to TMEM, dV += P^T dO and
 //     dK += dS^T Q.
-// Roles (384 threads): warp 0 streams chunks (TMA) and writes per-step
-// records (chunk position, the tile halves it is allowed for, validity and
-// global bits, and in the key pass the chunk rows' lse and D); warp 1 lane 0
-// issues the MMAs; warpgroups 1 and 2 (warps 4-7, 8-11) take even and odd
+// Roles (384 threads): warp 0 writes per-step records (chunk position, the
+// tile halves it is allowed for, validity and global bits) and starts the
+// resident tile's copy; warp 1 issues the MMAs (one elected lane); warps 2 and
+// 3 stream the two chunk tensors (TMA), warp 3 also the key pass's per-row
+// lse and D; warpgroups 1 and 2 (warps 4-7, 8-11) take even and odd
 // steps, each thread owning one TMEM lane (one tile row). X and Y rotate
 // through NSL TMEM slots (three for d = 64, two for d = 128) and each step's
 // accumulate products are issued NSL - 1 steps late, so the MMA issuer runs
@@ -107,7 +108,7 @@ struct BwdParams {
     const int32_t *gidx;
     const int32_t *dilation;
     __nv_bfloat16 *dQ, *dK, *dV;
-    float *lse, *dl;  // [B*H*n] each
+    float *lse, *dl;  // [B*H*stats_stride(n)] each, stored negated (-lse, -D)
     unsigned *status;
 };
 
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         mbar_init(bar(C::B_TF), 1);
         for (int i = 0; i < C::NSTG; ++i) {
-            mbar_init(bar(C::B_F + i), 1);
+            mbar_init(bar(C::B_F + i), 2);  // the two chunk loaders
             mbar_init(bar(C::B_E + i), 1);
         }
         for (int i = 0; i < C::NSL; ++i) {
@@ -379,7 +380,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == 0) {
-        // ======================================================== producer
+        // ======================================================== step records
+        bool ok = true;
+        Walk wk{0, bmap[0]};
+        for (int g = 0; g < total && ok; ++g) {
+            if (g == nsteps) wk = Walk{0, bmap[0]};  // row pass: second sweep
+            const int c = walk_next(wk);
+            const uint32_t ii = g % kSI;
+            if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
+            if (lane == 0) {
+                BwdStep &rec = steps[ii];
+                rec.y = c * kCN;
+                rec.allow = hvt[c];
+                rec.vbits = vbt[c];
+                rec.gbits = LF ? gbt[c] : 0ull;
+                mbar_arrive(bar(C::B_IF + ii));
+            }
+            __syncwarp();
+        }
+        // the resident tile copy was issued at start-up; with no steps (or on
+        // abort) nothing else waits for it
+        if (total == 0 || !ok || *abort_flag) wait_drain(bar(C::B_TF), 0, p.wait_ns);
+    } else if (warp == 2 || warp == 3) {
+        // ======================================================== chunk loaders
+        // Warp 2 streams B1 (K or Q), warp 3 B2 (V or dO) and, in the key
+        // pass, the chunk rows' lse and D: copies issued by one warp complete
+        // one after another, so each tensor gets its own warp. Both arrive on
+        // the stage's full barrier with their own byte counts.
+        const bool second = (warp == 3);
         uint32_t arms[C::NSTG] = {};
         bool ok = true;
         Walk wk{0, bmap[0]};
@@ -389,42 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int y = c * kCN;
             const uint32_t st = g % C::NSTG;
             if (g >= C::NSTG && !(ok = wait_warp(bar(C::B_E + st), ((g / C::NSTG) - 1) & 1, ctl))) break;
-            const uint32_t tx = 2 * C::CH_BYTES + (PASS == kKeyPass ? 2 * kCN * 4 : 0);
+            const uint32_t tx = C::CH_BYTES + ((PASS == kKeyPass && second) ? 2 * kCN * 4 : 0);
             if (lane == 0) mbar_arrive_expect_tx(bar(C::B_F + st), tx);
             __syncwarp();
-            if (lane < 2 * (D / 64)) {
-                const int tsel = lane / (D / 64), dc = lane % (D / 64);
-                const uint32_t dst = sbase + (tsel ? C::B2_OFF : C::B1_OFF) + st * C::CH_BYTES + dc * C::REG_C;
-                tma_load_3d(dst, tsel ? &tmB2 : &tmB1, bar(C::B_F + st), dc * 64, y, bh);
-            } else if (PASS == kKeyPass && lane < 2 * (D / 64) + 2) {
-                // the chunk rows' lse and D (rows of the padded stride; rows at
-                // or past n hold lse = +inf, D = 0)
-                const int which = lane - 2 * (D / 64);
+            if (lane < D / 64) {
+                const uint32_t dst = sbase + (second ? C::B2_OFF : C::B1_OFF) + st * C::CH_BYTES + lane * C::REG_C;
+                tma_load_3d(dst, second ? &tmB2 : &tmB1, bar(C::B_F + st), lane * 64, y, bh);
+            } else if (PASS == kKeyPass && second && lane < D / 64 + 2) {
+                // the chunk rows' -lse and -D (rows of the padded stride; rows
+                // at or past n hold -lse = -inf, -D = 0)
+                const int which = lane - D / 64;
                 const float *src = (which ? p.dl : p.lse) + (size_t)bh * sst + y;
                 bulk_load(sbase + C::LS_OFF + st * (2 * kCN * 4) + which * kCN * 4, src, kCN * 4, bar(C::B_F + st));
             }
             ++arms[st];
-            // step record
-            const uint32_t ii = g % kSI;
-            if (g >= kSI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / kSI) - 1) & 1, ctl))) break;
-            if (lane == 0) {
-                BwdStep &rec = steps[ii];
-                rec.y = y;
-                rec.allow = hvt[c];
-                rec.vbits = vbt[c];
-                rec.gbits = LF ? gbt[c] : 0ull;
-                mbar_arrive(bar(C::B_IF + ii));
-            }
-            __syncwarp();
         }
         if (!ok || *abort_flag) {
             // drain our copies in flight before the CTA leaves
             for (int i = 0; i < C::NSTG; ++i)
                 if (arms[i]) wait_drain(bar(C::B_F + i), (arms[i] - 1) & 1, p.wait_ns);
         }
-        // the resident tile copy was issued at start-up; with no steps (or on
-        // abort) nothing else waits for it
-        if (total == 0 || !ok || *abort_flag) wait_drain(bar(C::B_TF), 0, p.wait_ns);
     } else if (warp == 1) {
         // ======================================================== MMA issuer
         // The whole warp runs the loop and the waits (so the descriptors and
@@ -552,26 +564,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(xa + 64 + 32 * hh, yv);
                 tmem_wait_ld();
                 const uint32_t mh = (uint32_t)(mk >> (32 * hh));
+                const bool full = (mh == 0xffffffffu);
                 if (stats) {
                     // scaled scores (masked: -inf), their maximum, then the
                     // rescaled sums l and u in packed fp32 pairs
                     const uint64_t c2 = f2_pack(sl2, sl2);
                     float mx = -CUDART_INF_F;
+                    if (full) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        float a, b;
-                        f2_unpack(f2_fma(f2_pack(xv[j], xv[j + 1]), c2, 0ull), a, b);
-                        xv[j] = ((mh >> j) & 1u) ? a : -CUDART_INF_F;
-                        xv[j + 1] = ((mh >> (j + 1)) & 1u) ? b : -CUDART_INF_F;
-                        mx = fmax3(mx, xv[j], xv[j + 1]);
+                        for (int j = 0; j < 32; j += 2) {
+                            f2_unpack(f2_fma(f2_pack(xv[j], xv[j + 1]), c2, 0ull), xv[j], xv[j + 1]);
+                            mx = fmax3(mx, xv[j], xv[j + 1]);
+                        }
+                    } else if (mh != 0u) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            float a, b;
+                            f2_unpack(f2_fma(f2_pack(xv[j], xv[j + 1]), c2, 0ull), a, b);
+                            xv[j] = ((mh >> j) & 1u) ? a : -CUDART_INF_F;
+                            xv[j + 1] = ((mh >> (j + 1)) & 1u) ? b : -CUDART_INF_F;
+                            mx = fmax3(mx, xv[j], xv[j + 1]);
+                        }
                     }
                     const float mn = fmaxf(m, mx);
-                    if (mn != -CUDART_INF_F) {
+                    if (mh != 0u && mn != -CUDART_INF_F) {
                         const float alpha = ex2(m - mn);
+                        const uint64_t nm2 = f2_pack(-mn, -mn);
                         uint64_t ls2 = 0ull, us2 = 0ull;
 #pragma unroll
                         for (int j = 0; j < 32; j += 2) {
-                            const uint64_t e2 = f2_pack(ex2(xv[j] - mn), ex2(xv[j + 1] - mn));
+                            float a, b;
+                            f2_unpack(f2_add(f2_pack(xv[j], xv[j + 1]), nm2), a, b);
+                            const uint64_t e2 = f2_pack(ex2(a), ex2(b));
                             ls2 = f2_add(ls2, e2);
                             us2 = f2_fma(e2, f2_pack(yv[j], yv[j + 1]), us2);
                         }
@@ -582,8 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         u = fmaf(u, alpha, ua + ub);
                         m = mn;
                     }
+                } else if (mh == 0u) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pw[16 * hh + j] = dw[16 * hh + j] = 0u;
                 } else {
-                    // P = 2^(s c - lse) on the allowed columns, dS = P (dP - D)
+                    // P = 2^(s c - lse) on the allowed columns, dS = P (dP - D);
+                    // the statistics arrive negated (-lse, -D) as packed pairs
                     const uint64_t c2 = f2_pack(sl2, sl2);
                     const uint64_t nl_row = f2_pack(-lse, -lse), nd_row = f2_pack(-dlv, -dlv);
 #pragma unroll
@@ -591,15 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int c = 32 * hh + j;
                         uint64_t nl = nl_row, nd = nd_row;
                         if (PASS == kKeyPass) {
-                            const float2 lv = *reinterpret_cast<const float2 *>(lsd + c);
-                            const float2 dv = *reinterpret_cast<const float2 *>(lsd + kCN + c);
-                            nl = f2_pack(-lv.x, -lv.y);
-                            nd = f2_pack(-dv.x, -dv.y);
+                            nl = *reinterpret_cast<const uint64_t *>(lsd + c);
+                            nd = *reinterpret_cast<const uint64_t *>(lsd + kCN + c);
                         }
                         float ta, tb;
                         f2_unpack(f2_fma(f2_pack(xv[j], xv[j + 1]), c2, nl), ta, tb);
-                        const float p0 = ((mh >> j) & 1u) ? ex2(ta) : 0.f;
-                        const float p1 = ((mh >> (j + 1)) & 1u) ? ex2(tb) : 0.f;
+                        float p0 = ex2(ta), p1 = ex2(tb);
+                        if (!full) {
+                            p0 = ((mh >> j) & 1u) ? p0 : 0.f;
+                            p1 = ((mh >> (j + 1)) & 1u) ? p1 : 0.f;
+                        }
                         const uint64_t p2 = f2_pack(p0, p1);
                         float da, db;
                         f2_unpack(f2_fma(p2, f2_add(f2_pack(yv[j], yv[j + 1]), nd), 0ull), da, db);
@@ -653,9 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dlv = lt > 0.f ? ut / lt : 0.f;
                     stat[row] = lse;
                     stat[kTM + row] = dlv;
-                    if (pos < sst) {
-                        p.lse[(size_t)bh * sst + pos] = lse;
-                        p.dl[(size_t)bh * sst + pos] = dlv;
+                    if (pos < sst) {  // stored negated: the key pass adds them
+                        p.lse[(size_t)bh * sst + pos] = -lse;
+                        p.dl[(size_t)bh * sst + pos] = -dlv;
                     }
                 }
                 named_bar_sync(1, 256);
@@ -708,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (PASS == kRowPass && nsteps == 0 && pos < sst && wg == 0) {
-            p.lse[(size_t)bh * sst + pos] = CUDART_INF_F;
+            p.lse[(size_t)bh * sst + pos] = -CUDART_INF_F;  // negated, as above
             p.dl[(size_t)bh * sst + pos] = 0.f;
         }
     }

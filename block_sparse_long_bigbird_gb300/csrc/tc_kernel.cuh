@@ -168,6 +168,7 @@ struct Params {
     // global key (gpre[kb], gpre[nkb] = total) and those blocks in order
     // (glist); all three written by longformer_prep before the main kernel.
     const __nv_bfloat16 *Q;
+    const __nv_bfloat16 *Qg;  // Longformer: queries of the global-row units (Q, or the separate Qg)
     const int32_t *dilation;  // Longformer: per-head dilation [H] or NULL
     const int32_t *gidx;
     const unsigned long long *gbits;
@@ -359,7 +360,8 @@ __device__ __forceinline__ UnitPtrs unit_ptrs(const Params &p, const UnitInfo &u
 template <int D, bool PADDED, bool LF>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     sparse_tc_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKg,
+                   const __grid_constant__ CUtensorMap tmVg, const Params p) {
     using C = Cfg<D>;
     static_assert(C::SI * 2 * 8 <= 2 * 32 * 4, "Longformer global-key masks fit the list area");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -413,6 +415,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
+        if (LF) {
+            prefetch_tmap(&tmKg);
+            prefetch_tmap(&tmVg);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     int pr[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) pr[k] = global_row(p.gidx, G.ng, G.n, cur.q0 + lane + 32 * k);
-                    const uint4 *qh = reinterpret_cast<const uint4 *>(p.Q + (size_t)cur.bh * G.n * D);
+                    const uint4 *qh = reinterpret_cast<const uint4 *>(p.Qg + (size_t)cur.bh * G.n * D);
                     uint8_t *qs = smem + x * C::BIG + C::Q_OFF;
 #pragma unroll 8
                     for (int it = 0; it < kBM * CPR / 32; ++it) {
@@ -770,7 +776,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                             const int bx = lane >> 1, s = bx / (D / 64), dc = bx % (D / 64);
                             const uint32_t dst = is_v ? tbase + C::V_OFF + sv * C::KV_BYTES
                                                       : tbase + C::K_OFF + sk * C::KV_BYTES;
-                            tma_load_3d(dst + dc * C::KV_REGION + s * 8192, is_v ? &tmV : &tmK,
+                            // global-row units read the global projections' keys and values
+                            const bool gsel = LF && cur.step0 >= 0;
+                            const CUtensorMap *tm = is_v ? (gsel ? &tmVg : &tmV) : (gsel ? &tmKg : &tmK);
+                            tma_load_3d(dst + dc * C::KV_REGION + s * 8192, tm,
                                         bar(is_v ? C::B_VF + sv : C::B_KF + sk), dc * 64, si.y[s], cur.bh);
                         }
                         ++k_arms[sk];
@@ -886,7 +895,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // ================================================================ V (3) / K (4) loader
         // Follows the unit ring and the step records; one box per lane.
         const bool is_k = (role == 4);
-        const CUtensorMap *tmap = is_k ? &tmK : &tmV;
         const uint32_t buf0 = tbase + (is_k ? C::K_OFF : C::V_OFF);
         const int bf = is_k ? C::B_KF : C::B_VF, be = is_k ? C::B_KE : C::B_VE;
         static_assert(C::KST == C::VST, "one stage count for both loaders");
@@ -897,6 +905,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             const uint32_t slot = ui_idx % kNU;
             if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
             const int kind = ring[slot].kind, n_steps = ring[slot].n_steps, bh = ring[slot].bh;
+            // global-row units read the global projections' keys and values
+            const bool gsel = LF && ring[slot].step0 >= 0;
+            const CUtensorMap *tmap = is_k ? (gsel ? &tmKg : &tmK) : (gsel ? &tmVg : &tmV);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_UE + slot));
             if (kind == kUnitEnd) break;

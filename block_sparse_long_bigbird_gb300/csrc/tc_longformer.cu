@@ -139,6 +139,10 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
     prm.O = static_cast<__nv_bfloat16 *>(p.O);
     prm.status = p.status;
     prm.Q = static_cast<const __nv_bfloat16 *>(p.Q);
+    // separate projections for global attention ("Longformer", Sec. 3.1): the
+    // global-row units take their queries, keys and values from Qg, Kg, Vg
+    const bool sep = p.Qg != nullptr;
+    prm.Qg = static_cast<const __nv_bfloat16 *>(sep ? p.Qg : p.Q);
     prm.gidx = p.global_idx;
     prm.dilation = p.dilation;
     unsigned long long *gbits = reinterpret_cast<unsigned long long *>(base + L.gbits);
@@ -148,9 +152,10 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
     prm.gpre = gpre;
     prm.glist = glist;
     const int BH = p.B * p.H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mkg, mvg;
     if (!make_qkv_map(&mq, p.Q, BH, p.n, D) || !make_qkv_map(&mk, p.K, BH, p.n, D) ||
-        !make_qkv_map(&mv, p.V, BH, p.n, D))
+        !make_qkv_map(&mv, p.V, BH, p.n, D) || !make_qkv_map(&mkg, sep ? p.Kg : p.K, BH, p.n, D) ||
+        !make_qkv_map(&mvg, sep ? p.Vg : p.V, BH, p.n, D))
         return cudaErrorInvalidValue;
     auto kern = p.key_mask ? sparse_tc_fwd<D, true, true> : sparse_tc_fwd<D, false, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::ALLOC_BYTES);
@@ -164,7 +169,7 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
     int grid = cfg.grid_ctas;
     if (grid > prm.geo.total_units) grid = prm.geo.total_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, prm);
+    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, mkg, mvg, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++*launches;
     return cudaSuccess;

@@ -161,6 +161,30 @@ sa_status longformer_attn_fwd_ex(const void *Q, const void *K, const void *V, vo
                                  const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
 
 /*
+ * longformer_attn_fwd_gproj - longformer_attn_fwd_ex with separate projections
+ * for global attention.
+ *
+ * Source: "Longformer", Sec. 3.1, "Linear Projections for Global Attention":
+ * one set of projections (Q, K, V) computes the sliding-window attention and a
+ * second set (Qg, Kg, Vg) the global attention. Reading taken here: the row of
+ * a global token is computed from Qg against Kg and Vg over every key it may
+ * see; every other row uses Q, K and V throughout, its scores against global
+ * keys included. With Qg = Q, Kg = K, Vg = V the result is that of
+ * longformer_attn_fwd_ex.
+ *
+ * Qg, Kg, Vg: DEVICE [B][H][n][d], same dtype and alignment as Q, K, V; all
+ *   three NULL (then this is longformer_attn_fwd_ex) or all three set; none may
+ *   alias O.
+ * Other arguments, layout, ownership and errors: as for longformer_attn_fwd_ex.
+ */
+sa_status longformer_attn_fwd_gproj(const void *Q, const void *K, const void *V,
+                                    const void *Qg, const void *Kg, const void *Vg, void *O,
+                                    int B, int H, int n, int d, int window,
+                                    const int32_t *dilation, int causal,
+                                    const int32_t *global_idx, int n_global,
+                                    const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
+
+/*
  * bigbird_attn_bwd - gradients of bigbird_attn_fwd.
  *
  * Source: the pages train through this attention ("Big Bird", App. E.1, MLM

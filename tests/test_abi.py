@@ -185,3 +185,19 @@ def test_bwd_workspace_bytes(lib):
     assert lib.sa_attn_bwd_workspace_bytes(8, 12, 4096, 64) == 2 * 4 * 8 * 12 * 4096
     assert lib.sa_attn_bwd_workspace_bytes(1, 2, 1000, 64) == 2 * 4 * 2 * 1024  # rows padded to 64
     assert lib.sa_attn_bwd_workspace_bytes(1, 1, 100, 96) == 0
+
+
+def _lfg(lib, **kw):
+    a = dict(Q=FAKE, K=FAKE + 0x100000, V=FAKE + 0x200000, Qg=FAKE + 0x500000, Kg=FAKE + 0x600000,
+             Vg=FAKE + 0x700000, O=FAKE + 0x300000, B=1, H=2, n=1024, d=64, window=64, dil=None, causal=0,
+             gidx=FAKE + 0x400000, ng=4, km=None, dtype=0)
+    a.update(kw)
+    return lib.longformer_attn_fwd_gproj(a["Q"], a["K"], a["V"], a["Qg"], a["Kg"], a["Vg"], a["O"], a["B"], a["H"],
+                                         a["n"], a["d"], a["window"], a["dil"], a["causal"], a["gidx"], a["ng"],
+                                         a["km"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("bad", [dict(Kg=None), dict(Qg=None, Kg=None), dict(Vg=FAKE + 8), dict(O=FAKE + 0x500000),
+                                 dict(causal=3), dict(window=5)])
+def test_longformer_gproj_invalid_args(lib, bad):
+    assert _lfg(lib, **bad) == 1

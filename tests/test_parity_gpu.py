@@ -337,3 +337,59 @@ def test_scratch_reuse_across_shapes():
     for (B, H, n, d, b) in shapes:
         rows = np.concatenate([np.arange(0, 2 * b), np.arange(n - b, n)])
         bigbird_case(B, H, n, d, b, 2, 3, 3, cfg_id=81, path="tc", rows=rows, heads=[(0, 0), (B - 1, H - 1)])
+
+
+# ------------------------------------------------------ Longformer: separate global projections
+
+def _gproj_case(B, H, n, d, window, gidx, path, key_mask=None, dilation=None, causal=False, rows=None, heads=None,
+                cfg_id=90):
+    from oracle import oracle_longformer
+    from parity_util import assert_close, set_path
+
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=cfg_id)
+    Qg, Kg, Vg = make_qkv(B, H, n, d, "bf16", cfg_id=cfg_id + 1)
+    dev = torch.device("cuda:0")
+    set_path(path)
+    try:
+        O = sa.longformer_attn_fwd(*(t.to(dev) for t in (Q, K, V)), window, gidx.to(dev),
+                                   None if key_mask is None else key_mask.to(dev),
+                                   dilation=None if dilation is None else torch.tensor(dilation, dtype=torch.int32,
+                                                                                       device=dev),
+                                   causal=causal, Qg=Qg.to(dev), Kg=Kg.to(dev), Vg=Vg.to(dev))
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    O = O.float().cpu()
+    heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
+    for beta, h in heads:
+        sl = (slice(beta, beta + 1), slice(h, h + 1))
+        km = None if key_mask is None else key_mask[beta:beta + 1].numpy()
+        ref = oracle_longformer(Q[sl], K[sl], V[sl], window, gidx.numpy(), key_mask=km, rows=rows,
+                                dilation=None if dilation is None else [dilation[h]], causal=causal,
+                                Qg=Qg[sl], Kg=Kg[sl], Vg=Vg[sl])[0, 0]
+        got = O[beta, h].numpy() if rows is None else O[beta, h].numpy()[np.asarray(rows)]
+        assert_close(got, ref, 2e-2, 2e-3, what=f"longformer gproj beta={beta} h={h}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("d,dilation,causal", [(64, None, False), (64, [0, 2], True), (128, None, False)])
+def test_longformer_global_projections_small(path, d, dilation, causal):
+    B, n = 2, 1000
+    _gproj_case(B, 2, n, d, 128, torch.tensor([0, 5, 500, 999], dtype=torch.int32), path,
+                key_mask=make_key_mask(B, n), dilation=dilation, causal=causal)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_global_projections_many_globals(path):
+    """200 scattered global tokens: two global-row units per head, rows spread over all band tiles."""
+    from block_sparse_long_bigbird_gb300.inputs import make_global_positions
+    _gproj_case(1, 2, 3000, 64, 64, make_global_positions(3000, 200), path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_global_projections_bench_shape_sampled(path):
+    """B=4 H=12 n=4096 window 512, globals 0..15: every global row and a band sample, two heads."""
+    rows = np.concatenate([np.arange(0, 160), np.arange(2000, 2100), np.arange(4000, 4096)])
+    _gproj_case(4, 12, 4096, 64, 512, torch.arange(16, dtype=torch.int32), path, rows=rows,
+                heads=[(0, 0), (3, 11)])
