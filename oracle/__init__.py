@@ -35,6 +35,9 @@ Every function pinned by a test that does not reuse this code; the pins are in
                            causal mode: enumeration of the window positions,
                            torch is_causal attention, per-residue-class full
                            attention, hand-derived pair counts)
+  bigbird_etc_allowed,     pinned (pure-Python enumeration of the ETC rules;
+  oracle_bigbird_etc       equals the ITC mask with g/b global blocks and r = 0
+                           when b divides g; padded prefix equivalence)
   oracle_longformer with   pinned (global rows = torch SDPA of Qg, Kg, Vg over
   separate global          their keys; other rows identical to the single-
   projections              projection oracle; same tensors give the same result)
@@ -55,10 +58,12 @@ Every function pinned by a test that does not reuse this code; the pins are in
 from .pattern import SplitMix64, splitmix64_stream, bigbird_random_table
 from .attention import (
     bigbird_allowed,
+    bigbird_etc_allowed,
     longformer_allowed,
     masked_attention,
     masked_softmax_probs,
     oracle_bigbird,
+    oracle_bigbird_etc,
     oracle_longformer,
     masked_attention_grads,
     masked_attention_grad_terms,
@@ -73,10 +78,12 @@ __all__ = [
     "splitmix64_stream",
     "bigbird_random_table",
     "bigbird_allowed",
+    "bigbird_etc_allowed",
     "longformer_allowed",
     "masked_attention",
     "masked_softmax_probs",
     "oracle_bigbird",
+    "oracle_bigbird_etc",
     "oracle_longformer",
     "masked_attention_grads",
     "masked_attention_grad_terms",

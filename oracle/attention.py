@@ -95,6 +95,41 @@ def longformer_allowed(n, window, global_idx, rows=None, dilation=0, causal=Fals
     return allowed
 
 
+def bigbird_etc_allowed(n, g_tokens, b, w, rows=None):
+    """BigBird-ETC mask, bool [len(rows), n] ("Big Bird", Sec. 2 global tokens,
+    extended construction; App. E Tab. 8 and the QA tables: g added global
+    tokens, window w blocks, no random blocks).
+
+    The sequence holds the g_tokens added global tokens first, then the regular
+    tokens. A global token sees every token and every token sees it. A regular
+    token at position p sees the regular tokens whose block (p - g_tokens) // b
+    is within w // 2 of its own, clipped at the ends.
+    """
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    cols = np.arange(n)
+    gi = rows < g_tokens
+    gj = cols < g_tokens
+    bi = (rows - g_tokens) // b
+    bj = (cols - g_tokens) // b
+    window = (np.abs(bi[:, None] - bj[None, :]) <= w // 2) & ~gi[:, None] & ~gj[None, :]
+    return window | gi[:, None] | gj[None, :]
+
+
+def oracle_bigbird_etc(Q, K, V, g_tokens, b, w, key_mask=None, rows=None):
+    """BigBird-ETC attention forward, float64 [B, H, len(rows), d]."""
+    Q, K, V = _as_f64(Q), _as_f64(K), _as_f64(V)
+    B, H, n, d = Q.shape
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    out = np.zeros((B, H, len(rows), d), dtype=np.float64)
+    mask0 = bigbird_etc_allowed(n, g_tokens, b, w, rows)
+    for beta in range(B):
+        kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+        mask = _apply_validity(mask0, rows, kv)
+        for h in range(H):
+            out[beta, h] = masked_attention(Q[beta, h, rows], K[beta, h], V[beta, h], mask)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Masked softmax attention
 # ---------------------------------------------------------------------------

@@ -579,3 +579,45 @@ def test_longformer_global_projections_split_rows():
     # the same tensors as both sets give the plain oracle
     same = oracle_longformer(Q, K, V, window, gidx, Qg=Q, Kg=K, Vg=V)
     np.testing.assert_allclose(same, oracle_longformer(Q, K, V, window, gidx), rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# BigBird-ETC (added global tokens, no random blocks)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,g,b,w", [(40, 5, 4, 3), (64, 8, 8, 1), (50, 0, 5, 3), (37, 3, 4, 5)])
+def test_etc_mask_matches_enumeration(n, g, b, w):
+    from oracle import bigbird_etc_allowed
+    got = bigbird_etc_allowed(n, g, b, w)
+    for i in range(n):
+        for j in range(n):
+            if i < g or j < g:
+                want = True
+            else:
+                want = abs((i - g) // b - (j - g) // b) <= w // 2
+            assert got[i, j] == want, (i, j)
+
+
+def test_etc_equals_itc_layout_with_block_aligned_globals():
+    """With b dividing g, ETC over n tokens is ITC with g/b global blocks and no random blocks."""
+    from oracle import bigbird_etc_allowed
+    n, g, b, w = 640, 128, 64, 3
+    itc = bigbird_allowed(n, b, g // b, w, np.full((n // b, 0), -1))
+    np.testing.assert_array_equal(bigbird_etc_allowed(n, g, b, w), itc)
+
+
+def test_etc_padded_prefix_equals_unpadded():
+    """g not a multiple of b: pad the global prefix to a whole block with tokens
+    that key padding removes; the real rows are unchanged."""
+    from oracle import oracle_bigbird_etc
+    g, b, w, nreg, d = 23, 16, 3, 96, 8
+    gp = -(-g // b) * b
+    Q, K, V = (_rand((1, 1, g + nreg, d), s) for s in (81, 82, 83))
+    ref = oracle_bigbird_etc(Q, K, V, g, b, w)
+    pad = lambda x: np.concatenate([x[:, :, :g], np.zeros((1, 1, gp - g, d)), x[:, :, g:]], axis=2)
+    km = np.ones((1, gp + nreg), dtype=np.uint8)
+    km[0, g:gp] = 0
+    got = oracle_bigbird_etc(pad(Q), pad(K), pad(V), gp, b, w, key_mask=km)
+    keep = np.concatenate([np.arange(g), np.arange(gp, gp + nreg)])
+    np.testing.assert_allclose(got[0, 0, keep], ref[0, 0], atol=1e-12, rtol=1e-12)
+    assert np.all(got[0, 0, g:gp] == 0)
