@@ -5,7 +5,9 @@ w = 3b, r = 3b tokens, i.e. 2 global, 3 window and 3 random blocks, n = 4096,
 12 heads) and Longformer's Sec. 3.1 (window 512, i.e. 256 tokens each side,
 global attention on a few chosen positions). The long and padded variants
 stretch the same pattern to n = 16384 and n = 65536. The two ``*_bwd_*``
-workloads time the backward (dQ, dK, dV) on the n = 4096 shapes.
+workloads time the backward (dQ, dK, dV) on the n = 4096 shapes. The ETC
+workload adds 256 global tokens in front of 4096 regular ones (App. E: g = 256,
+w = 3 blocks, r = 0), run as BigBird with 4 global blocks and no random blocks.
 """
 
 from dataclasses import dataclass, field
@@ -50,6 +52,8 @@ WORKLOADS = {
     "bigbird_bf16_n65536_d128": Workload(
         "bigbird_bf16_n65536_d128", "bigbird", B=1, H=16, n=65536, d=128, dtype="bf16",
         sigma=0.5, b=128, cfg_id=5),
+    "bigbird_etc_bf16_n4352": Workload(
+        "bigbird_etc_bf16_n4352", "bigbird", B=8, H=12, n=4352, d=64, dtype="bf16", g=4, w=3, r=0, cfg_id=6),
     "bigbird_bwd_bf16_n4096": Workload(
         "bigbird_bwd_bf16_n4096", "bigbird", B=8, H=12, n=4096, d=64, dtype="bf16", cfg_id=2, grad=True),
     "longformer_bwd_bf16_n4096": Workload(

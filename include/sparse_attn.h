@@ -92,6 +92,11 @@ sa_status build_bigbird_pattern(uint64_t seed, int H, int n, int b, int g, int w
  * |qb - kb| <= w / 2 (window of w blocks, clipped at the sequence ends), or kb
  * is listed in rand_idx[h][qb][:].
  *
+ * BigBird-ETC ("Big Bird", Sec. 2: g added global tokens such as CLS; App. E:
+ * r = 0) runs through this call: place the added tokens first, pad them to
+ * ceil(g_tokens / b) whole blocks with tokens that key_mask marks invalid, and
+ * pass g = ceil(g_tokens / b), r = 0. The padding rows come out zero.
+ *
  * Sizes: B, H >= 1; d in {64, 128}; b in {64, 128}; n a multiple of b;
  * 0 <= g <= n / b; w odd and >= 1; r >= 0.
  * rand_idx: DEVICE int32 [H][n/b][r] (e.g. from build_bigbird_pattern, copied

@@ -282,6 +282,22 @@ def test_bigbird_n65536_d128_workload(path):
                  path=path, rows=rows, heads=[(0, 0), (0, 13)])
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_etc_n4352_workload(path):
+    """ETC bench shape (256 added global tokens + 4096, window 3 blocks, r = 0) against the ETC oracle."""
+    from oracle import oracle_bigbird_etc
+    from parity_util import assert_close
+    wl = WORKLOADS["bigbird_etc_bf16_n4352"]
+    Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, "bf16", cfg_id=wl.cfg_id)
+    table = sa.build_bigbird_pattern(0, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+    O = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path=path).float().cpu()
+    rows = sampled_bigbird_rows(wl.n, wl.b, wl.g, seed=6)
+    for beta, h in [(0, 0), (7, 11)]:
+        sl = (slice(beta, beta + 1), slice(h, h + 1))
+        ref = oracle_bigbird_etc(Q[sl], K[sl], V[sl], wl.g * wl.b, wl.b, wl.w, rows=rows)[0, 0]
+        assert_close(O[beta, h].numpy()[rows], ref, 2e-2, 2e-3, what=f"etc workload beta={beta} h={h}")
+
+
 # ------------------------------------------------------------- properties
 
 @pytest.mark.parametrize("path", PATHS)
@@ -393,3 +409,33 @@ def test_longformer_global_projections_bench_shape_sampled(path):
     rows = np.concatenate([np.arange(0, 160), np.arange(2000, 2100), np.arange(4000, 4096)])
     _gproj_case(4, 12, 4096, 64, 512, torch.arange(16, dtype=torch.int32), path, rows=rows,
                 heads=[(0, 0), (3, 11)])
+
+
+# ------------------------------------------------------ BigBird-ETC through the ITC kernel
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("g_tokens,b,n_reg", [(256, 64, 1024), (230, 64, 1024), (100, 128, 1024)])
+def test_bigbird_etc_via_block_kernel(path, g_tokens, b, n_reg):
+    """ETC (g added global tokens, window 3 blocks, r = 0): the global prefix is
+    padded to whole blocks with tokens that key padding removes, then the
+    block kernel runs with ceil(g / b) global blocks and no random blocks."""
+    from oracle import oracle_bigbird_etc
+    from parity_util import assert_close, gpu_bigbird
+    B, H, d, w = 2, 2, 64, 3
+    n = g_tokens + n_reg
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=95)
+    gb = -(-g_tokens // b)
+    gp = gb * b
+    padn = gp + n_reg
+    pad = lambda x: torch.cat([x[:, :, :g_tokens], torch.zeros(B, H, gp - g_tokens, d, dtype=x.dtype),
+                               x[:, :, g_tokens:]], dim=2).contiguous()
+    km = torch.ones(B, padn, dtype=torch.uint8)
+    km[:, g_tokens:gp] = 0
+    table = sa.build_bigbird_pattern(0, H, padn, b, gb, w, 0)
+    O = gpu_bigbird(pad(Q), pad(K), pad(V), b, gb, w, 0, table, km, path).float().cpu()
+    keep = np.concatenate([np.arange(g_tokens), np.arange(gp, padn)])
+    ref = oracle_bigbird_etc(Q, K, V, g_tokens, b, w)
+    for beta in range(B):
+        for h in range(H):
+            assert_close(O[beta, h].numpy()[keep], ref[beta, h], 2e-2, 2e-3, what=f"etc beta={beta} h={h}")
+    assert np.all(O[:, :, g_tokens:gp].numpy() == 0)
