@@ -68,7 +68,7 @@ static_assert(sizeof(BwdStep) == 32, "BwdStep layout");
 
 template <int D>
 struct BwdCfg {
-    static constexpr int NSTG = (D == 64) ? 6 : 3;  // chunk stages (one K/Q + one V/dO chunk each)
+    static constexpr int NSTG = (D == 64) ? 6 : 4;  // chunk stages (one K/Q + one V/dO chunk each)
     static constexpr int NSL = (D == 64) ? 3 : 2;   // X/Y slots in TMEM (128 columns each)
     static constexpr int TILE_BYTES = kTM * D * 2;
     static constexpr int CH_BYTES = kCN * D * 2;

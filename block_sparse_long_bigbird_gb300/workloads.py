@@ -56,6 +56,9 @@ WORKLOADS = {
         "bigbird_etc_bf16_n4352", "bigbird", B=8, H=12, n=4352, d=64, dtype="bf16", g=4, w=3, r=0, cfg_id=6),
     "bigbird_bwd_bf16_n4096": Workload(
         "bigbird_bwd_bf16_n4096", "bigbird", B=8, H=12, n=4096, d=64, dtype="bf16", cfg_id=2, grad=True),
+    "bigbird_bwd_bf16_n65536_d128": Workload(
+        "bigbird_bwd_bf16_n65536_d128", "bigbird", B=1, H=16, n=65536, d=128, dtype="bf16",
+        sigma=0.5, b=128, cfg_id=5, grad=True),
     "longformer_bwd_bf16_n4096": Workload(
         "longformer_bwd_bf16_n4096", "longformer", B=4, H=12, n=4096, d=64, dtype="bf16",
         window=512, n_global=16, cfg_id=3, grad=True),
