@@ -115,6 +115,54 @@ def longformer_attn_fwd(Q, K, V, window, global_idx, key_mask=None, out=None, st
     return out
 
 
+def _check_host(*tensors):
+    for t in tensors:
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("host entry points take contiguous CPU tensors (page-locked for overlapped copies)")
+
+
+def bigbird_attn_fwd_host(Q, K, V, b, g, w, r, rand_idx, key_mask=None, out=None, stream=None, device=None):
+    """bigbird_attn_fwd on CPU tensors (pinned for overlap); returns O as a CPU tensor.
+
+    The copies are pipelined against the computation inside the library. The
+    result is complete once `stream` (default: the current stream of `device`)
+    has completed.
+    """
+    _check_host(Q, K, V, rand_idx, key_mask)
+    if Q.dtype not in _DTYPE or K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K, V must share shape and a supported dtype")
+    B, H, n, d = Q.shape
+    if out is None:
+        out = torch.empty(Q.shape, dtype=Q.dtype).pin_memory()
+    _check_host(out)
+    dev = device if device is not None else torch.cuda.current_device()
+    st = _lib.lib().bigbird_attn_fwd_host(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, n, d, b, g, w, r,
+        _ptr(rand_idx), _ptr(key_mask), _DTYPE[Q.dtype], _stream_handle(stream, dev))
+    _lib.check(st, "bigbird_attn_fwd_host")
+    return out
+
+
+def longformer_attn_fwd_host(Q, K, V, window, global_idx, key_mask=None, out=None, stream=None, dilation=None,
+                             causal=False, device=None):
+    """longformer_attn_fwd on CPU tensors (pinned for overlap); returns O as a CPU tensor."""
+    _check_host(Q, K, V, global_idx, key_mask, dilation)
+    if Q.dtype not in _DTYPE or K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K, V must share shape and a supported dtype")
+    B, H, n, d = Q.shape
+    if out is None:
+        out = torch.empty(Q.shape, dtype=Q.dtype).pin_memory()
+    _check_host(out)
+    n_global = 0 if global_idx is None else int(global_idx.numel())
+    dev = device if device is not None else torch.cuda.current_device()
+    st = _lib.lib().longformer_attn_fwd_host(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(out), B, H, n, d, window, _ptr(dilation), 1 if causal else 0,
+        _ptr(global_idx if n_global else None), n_global, _ptr(key_mask), _DTYPE[Q.dtype],
+        _stream_handle(stream, dev))
+    _lib.check(st, "longformer_attn_fwd_host")
+    return out
+
+
 def _check_bwd(Q, K, V, dO):
     _check_qkv(Q, K, V)
     if not dO.is_cuda or not dO.is_contiguous() or dO.dtype != Q.dtype or dO.shape != Q.shape \

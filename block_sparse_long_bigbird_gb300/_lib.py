@@ -41,6 +41,8 @@ SIGNATURES = {
     "longformer_attn_fwd_ex": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I, _VP]),
     "longformer_attn_fwd_gproj": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP,
                                        _I, _VP]),
+    "bigbird_attn_fwd_host": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _I, _VP]),
+    "longformer_attn_fwd_host": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I, _VP]),
     "bigbird_attn_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _I,
                               _VP]),
     "longformer_attn_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I,

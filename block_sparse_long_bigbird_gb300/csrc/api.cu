@@ -2,6 +2,7 @@
 // status word, scratch (workspace) management and options.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -25,6 +26,13 @@ struct DeviceState {
     void *user_ws = nullptr;  // caller-owned scratch (sa_set_workspace)
     size_t user_ws_bytes = 0;
     size_t user_ws_clean = 0;
+    // host-buffer path: copy streams, events and device staging buffers
+    bool host_ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_last = nullptr;
+    cudaEvent_t ev_in[2] = {}, ev_done[2] = {}, ev_out[2] = {};
+    void *stage = nullptr;
+    size_t stage_bytes = 0;
 };
 
 std::mutex g_mutex;
@@ -217,6 +225,150 @@ sa_status check_bwd_tensors(const void *Q, const void *K, const void *V, const v
     return SA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Host-buffer path: the forward on HOST tensors, pipelined over chunks of heads.
+// Chunk k's inputs are copied in on one library stream while chunk k - 1
+// computes on the caller's stream and chunk k - 2's output is copied out on a
+// second library stream; two device staging sets alternate. Every chunk is an
+// ordinary device-side call of the library on a slice of heads of one batch
+// entry, so the numerics are those of the device entry points.
+constexpr int kHostChunks = 4;  // target number of chunks per call
+
+sa_status host_path_init(DeviceState &st) {
+    if (st.host_ready) return SA_OK;
+    if (cudaStreamCreateWithFlags(&st.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&st.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st.ev_start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st.ev_last, cudaEventDisableTiming) != cudaSuccess)
+        return SA_ERR_CUDA;
+    for (int i = 0; i < 2; ++i)
+        if (cudaEventCreateWithFlags(&st.ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&st.ev_done[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&st.ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+            return SA_ERR_CUDA;
+    // the first call waits on ev_last: give it a completed state
+    if (cudaEventRecord(st.ev_last, st.d2h) != cudaSuccess) return SA_ERR_CUDA;
+    st.host_ready = true;
+    return SA_OK;
+}
+
+// `hp` carries HOST pointers in Q, K, V, O, rand_idx / global_idx, dilation
+// and key_mask. A chunk is `bc` whole batch entries, or (when one batch entry
+// is more than a chunk) `hc` consecutive heads of one batch entry; either way
+// its rows are one contiguous stretch of the [B][H][n][d] arrays.
+sa_status run_host(const sa::Problem &hp, sa_dtype dtype, cudaStream_t s) {
+    const size_t elem = dtype == SA_FP32 ? 4 : 2;
+    const int B = hp.B, H = hp.H, n = hp.n, d = hp.d;
+    const size_t head_bytes = (size_t)n * d * elem;
+    const int per_chunk = std::max(1, (B * H + kHostChunks - 1) / kHostChunks);  // (batch, head) pairs
+    const int bc = per_chunk >= H ? per_chunk / H : 1;   // batch entries per chunk
+    const int hc = per_chunk >= H ? H : per_chunk;       // heads per chunk (within one batch entry)
+    const size_t set_bytes = 4 * (size_t)bc * hc * head_bytes;  // Q, K, V, O of one chunk
+    // small tables, copied once per call
+    const bool bb = hp.kind == sa::kBigBird;
+    const size_t rand_bytes = bb && hp.rand_idx ? (size_t)H * (n / hp.b) * hp.r * 4 : 0;
+    const size_t gidx_bytes = !bb && hp.global_idx ? (size_t)hp.n_global * 4 : 0;
+    const size_t dil_bytes = !bb && hp.dilation ? (size_t)H * 4 : 0;
+    const size_t km_bytes = hp.key_mask ? (size_t)B * n : 0;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t need = 2 * up(set_bytes) + up(rand_bytes) + up(gidx_bytes) + up(dil_bytes) + up(km_bytes);
+
+    int dev = 0;
+    DeviceState *st = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        sa_status e = current_device(&dev, &st);
+        if (e != SA_OK) return e;
+        if (st->cc_major != 10 || st->cc_minor != 3) return SA_ERR_UNSUPPORTED;
+        if ((e = host_path_init(*st)) != SA_OK) return e;
+        if (st->stage_bytes < need) {
+            if (st->stage) {
+                if (cudaDeviceSynchronize() != cudaSuccess) return SA_ERR_CUDA;
+                cudaFree(st->stage);
+                st->stage = nullptr;
+                st->stage_bytes = 0;
+            }
+            if (cudaMalloc(&st->stage, need) != cudaSuccess) return SA_ERR_CUDA;
+            st->stage_bytes = need;
+        }
+    }
+    uint8_t *base = static_cast<uint8_t *>(st->stage);
+    uint8_t *sets[2] = {base, base + up(set_bytes)};
+    uint8_t *tab = base + 2 * up(set_bytes);
+    int32_t *d_rand = rand_bytes ? reinterpret_cast<int32_t *>(tab) : nullptr;
+    tab += up(rand_bytes);
+    int32_t *d_gidx = gidx_bytes ? reinterpret_cast<int32_t *>(tab) : nullptr;
+    tab += up(gidx_bytes);
+    int32_t *d_dil = dil_bytes ? reinterpret_cast<int32_t *>(tab) : nullptr;
+    tab += up(dil_bytes);
+    uint8_t *d_km = km_bytes ? tab : nullptr;
+
+    // order: after earlier work on the caller's stream and the previous host call
+    if (cudaEventRecord(st->ev_start, s) != cudaSuccess || cudaStreamWaitEvent(st->h2d, st->ev_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(st->h2d, st->ev_last, 0) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (rand_bytes && cudaMemcpyAsync(d_rand, hp.rand_idx, rand_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (gidx_bytes && cudaMemcpyAsync(d_gidx, hp.global_idx, gidx_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (dil_bytes && cudaMemcpyAsync(d_dil, hp.dilation, dil_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (km_bytes && cudaMemcpyAsync(d_km, hp.key_mask, km_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
+        return SA_ERR_CUDA;
+
+    int launches = 0, k = 0;
+    const size_t chunk_cap = (size_t)bc * hc * head_bytes;
+    for (int beta = 0; beta < B; beta += bc) {
+        const int nb_here = std::min(bc, B - beta);
+        for (int h0 = 0; h0 < H; h0 += hc, ++k) {
+            const int cnt = std::min(hc, H - h0);
+            const int set = k & 1;
+            const size_t off = ((size_t)beta * H + h0) * head_bytes;  // byte offset of the slice in [B][H][n][d]
+            const size_t bytes = (size_t)nb_here * cnt * head_bytes;
+            uint8_t *dq = sets[set], *dk = dq + chunk_cap, *dv = dk + chunk_cap, *dout = dv + chunk_cap;
+            // the staging set is free once chunk k - 2's output has been copied out
+            if (k >= 2 && cudaStreamWaitEvent(st->h2d, st->ev_out[set], 0) != cudaSuccess) return SA_ERR_CUDA;
+            if (cudaMemcpyAsync(dq, static_cast<const uint8_t *>(hp.Q) + off, bytes, cudaMemcpyHostToDevice, st->h2d) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(dk, static_cast<const uint8_t *>(hp.K) + off, bytes, cudaMemcpyHostToDevice, st->h2d) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(dv, static_cast<const uint8_t *>(hp.V) + off, bytes, cudaMemcpyHostToDevice, st->h2d) !=
+                    cudaSuccess ||
+                cudaEventRecord(st->ev_in[set], st->h2d) != cudaSuccess || cudaStreamWaitEvent(s, st->ev_in[set], 0) != cudaSuccess)
+                return SA_ERR_CUDA;
+            sa::Problem p = hp;
+            p.Q = dq;
+            p.K = dk;
+            p.V = dv;
+            p.O = dout;
+            p.B = nb_here;  // whole batch entries (cnt == H), or one entry's heads [h0, h0 + cnt)
+            p.H = cnt;
+            p.key_mask = d_km ? d_km + (size_t)beta * n : nullptr;
+            if (bb) {
+                p.rand_idx = d_rand ? d_rand + (size_t)h0 * (n / hp.b) * hp.r : nullptr;
+            } else {
+                p.global_idx = d_gidx;
+                p.dilation = d_dil ? d_dil + h0 : nullptr;
+            }
+            const sa_status e = run(p, dtype, s);
+            if (e != SA_OK) return e;
+            launches += g_last_launches;
+            if (cudaEventRecord(st->ev_done[set], s) != cudaSuccess ||
+                cudaStreamWaitEvent(st->d2h, st->ev_done[set], 0) != cudaSuccess ||
+                cudaMemcpyAsync(static_cast<uint8_t *>(hp.O) + off, dout, bytes, cudaMemcpyDeviceToHost, st->d2h) !=
+                    cudaSuccess ||
+                cudaEventRecord(st->ev_out[set], st->d2h) != cudaSuccess)
+                return SA_ERR_CUDA;
+        }
+    }
+    // the caller's stream completes once the last output copy has (the copies
+    // of one stream run in order)
+    if (cudaEventRecord(st->ev_last, st->d2h) != cudaSuccess || cudaStreamWaitEvent(s, st->ev_last, 0) != cudaSuccess)
+        return SA_ERR_CUDA;
+    g_last_launches = launches;
+    return SA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -335,6 +487,44 @@ sa_status longformer_attn_bwd(const void *Q, const void *K, const void *V, const
 size_t sa_attn_bwd_workspace_bytes(int B, int H, int n, int d) {
     if (!size_ok(B, H, n, d)) return 0;
     return bwd_stats_bytes(B, H, n);
+}
+
+sa_status bigbird_attn_fwd_host(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
+                                int b, int g, int w, int r, const int32_t *rand_idx, const uint8_t *key_mask,
+                                sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !O || O == Q || O == K || O == V) return SA_ERR_INVALID_ARG;
+    sa_status s = bigbird_args_ok(B, H, n, d, b, g, w, r, rand_idx);
+    if (s != SA_OK) return s;
+    sa::Problem p = {};
+    p.kind = sa::kBigBird;
+    p.Q = Q; p.K = K; p.V = V; p.O = O;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.b = b; p.g = g; p.w = w; p.r = r;
+    p.rand_idx = r > 0 ? rand_idx : nullptr;
+    p.key_mask = key_mask;
+    return run_host(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sa_status longformer_attn_fwd_host(const void *Q, const void *K, const void *V, void *O, int B, int H, int n, int d,
+                                   int window, const int32_t *dilation, int causal, const int32_t *global_idx,
+                                   int n_global, const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+    if (!Q || !K || !V || !O || O == Q || O == K || O == V) return SA_ERR_INVALID_ARG;
+    sa_status s = longformer_args_ok(B, H, n, d, window, global_idx, n_global);
+    if (s != SA_OK) return s;
+    sa::Problem p = {};
+    p.kind = sa::kLongformer;
+    p.Q = Q; p.K = K; p.V = V; p.O = O;
+    p.B = B; p.H = H; p.n = n; p.d = d;
+    p.window = window;
+    p.global_idx = n_global > 0 ? global_idx : nullptr;
+    p.n_global = n_global;
+    p.dilation = dilation;
+    p.causal = causal;
+    p.key_mask = key_mask;
+    return run_host(p, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g) {

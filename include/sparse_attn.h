@@ -190,6 +190,45 @@ sa_status longformer_attn_fwd_gproj(const void *Q, const void *K, const void *V,
                                     const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
 
 /*
+ * bigbird_attn_fwd_host / longformer_attn_fwd_host - the forward on HOST
+ * buffers, with the host<->device copies pipelined against the computation.
+ * (The pages have no counterpart: this is a deployment variant of the same
+ * computation for inputs that live in host memory.)
+ *
+ * The (batch, head) pairs are processed in about four chunks per call: whole
+ * batch entries, or consecutive heads of one batch entry when an entry is
+ * more than a chunk. Chunk k's Q, K, V are copied to the device on a
+ * library-owned stream while chunk k - 1 computes on `stream` and chunk k - 2's
+ * O is copied back on a second library-owned stream; two device staging sets
+ * alternate. Each chunk is an ordinary device-side call
+ * (bigbird_attn_fwd / longformer_attn_fwd_ex) on a slice, so results are
+ * bitwise those of the device entry points.
+ *
+ * Q, K, V, O: HOST [B][H][n][d] arrays of the dtype. Page-locked memory
+ *   (cudaHostAlloc, cudaHostRegister) is needed for the copies to overlap;
+ *   pageable memory works but the copies then run one after another.
+ * rand_idx, global_idx, dilation, key_mask: HOST arrays with the layouts of
+ *   the device entry points (copied once per call).
+ * Completion: asynchronous on `stream`; O is complete once `stream` has
+ *   completed the work issued by this call. The caller must not modify Q, K,
+ *   V or read O before then.
+ * Scratch: device staging of 2 x 4 x (heads per chunk) x n x d elements plus
+ *   the tables, allocated by the library on first use and grown on demand;
+ *   plus the device entry points' own workspace.
+ * Errors: as for bigbird_attn_fwd / longformer_attn_fwd_ex (NULL or aliasing
+ *   tensors are SA_ERR_INVALID_ARG).
+ */
+sa_status bigbird_attn_fwd_host(const void *Q, const void *K, const void *V, void *O,
+                                int B, int H, int n, int d, int b, int g, int w, int r,
+                                const int32_t *rand_idx, const uint8_t *key_mask,
+                                sa_dtype dtype, sa_stream_t stream);
+sa_status longformer_attn_fwd_host(const void *Q, const void *K, const void *V, void *O,
+                                   int B, int H, int n, int d, int window,
+                                   const int32_t *dilation, int causal,
+                                   const int32_t *global_idx, int n_global,
+                                   const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
+
+/*
  * bigbird_attn_bwd - gradients of bigbird_attn_fwd.
  *
  * Source: the pages train through this attention ("Big Bird", App. E.1, MLM
