@@ -358,9 +358,19 @@ def oracle_bigbird_bwd(Q, K, V, dO, b, g, w, rand_table, key_mask=None, row_chun
 
 
 def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilation=None,
-                          causal=False, row_chunk=1024, terms=False):
+                          causal=False, row_chunk=1024, terms=False, Qg=None, Kg=None, Vg=None):
     """Gradients (dQ, dK, dV), float64 [B, H, n, d], of ``oracle_longformer``
-    (``terms``: as for ``oracle_bigbird_bwd``)."""
+    (``terms``: as for ``oracle_bigbird_bwd``).
+
+    With the separate projections for global attention (``Qg``, ``Kg``,
+    ``Vg``), the global rows depend only on the g set and the other rows only
+    on Q, K, V, so the gradients split by rows: returns (dQ, dK, dV, dQg, dKg,
+    dVg), each set summed over its own rows (``terms`` is not supported then).
+    """
+    if Qg is not None:
+        assert not terms
+        return _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, causal,
+                                     row_chunk, Qg, Kg, Vg)
     Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
     B, H, n, d = Q.shape
     dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
@@ -383,6 +393,32 @@ def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilati
                         T[which][kind][beta, h] = tt[which][kind]
             dQ[beta, h], dK[beta, h], dV[beta, h] = res
     return ((dQ, dK, dV), T) if terms else (dQ, dK, dV)
+
+
+def _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, causal, row_chunk, Qg, Kg, Vg):
+    """Separate projections: rows of global tokens against (Qg, Kg, Vg), the
+    other rows against (Q, K, V); each row set's mask is the row's usual mask."""
+    Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
+    Qg, Kg, Vg = _as_f64(Qg), _as_f64(Kg), _as_f64(Vg)
+    B, H, n, d = Q.shape
+    dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
+    is_global = np.zeros(n, dtype=bool)
+    is_global[np.asarray(global_idx, dtype=np.int64)] = True
+    out = [np.zeros_like(Q) for _ in range(6)]
+    for h in range(H):
+        for beta in range(B):
+            kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
+            for sel, (q, k, v), base in ((~is_global, (Q, K, V), 0), (is_global, (Qg, Kg, Vg), 3)):
+                rows = np.nonzero(sel)[0]
+                for c0 in range(0, len(rows), row_chunk):
+                    rr = rows[c0:c0 + row_chunk]
+                    mask = _apply_validity(longformer_allowed(n, window, global_idx, rr, dilation=dil[h],
+                                                              causal=causal), rr, kv)
+                    dq, dk, dv = masked_attention_grads(q[beta, h, rr], k[beta, h], v[beta, h], mask, dO[beta, h, rr])
+                    out[base][beta, h, rr] = dq
+                    out[base + 1][beta, h] += dk
+                    out[base + 2][beta, h] += dv
+    return tuple(out)
 
 
 # ---------------------------------------------------------------------------

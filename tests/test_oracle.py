@@ -621,3 +621,32 @@ def test_etc_padded_prefix_equals_unpadded():
     keep = np.concatenate([np.arange(g), np.arange(gp, gp + nreg)])
     np.testing.assert_allclose(got[0, 0, keep], ref[0, 0], atol=1e-12, rtol=1e-12)
     assert np.all(got[0, 0, g:gp] == 0)
+
+
+def test_longformer_global_projection_grads_match_finite_differences():
+    """The six gradients of the separate-projection forward, by central differences."""
+    from oracle import oracle_longformer_bwd
+    n, window, d = 12, 4, 3
+    gidx = np.array([2, 9])
+    X = [_rand((1, 1, n, d), s) for s in (101, 102, 103, 104, 105, 106)]
+    dO = _rand((1, 1, n, d), 107)
+    km = np.ones((1, n), dtype=np.uint8)
+    km[0, 11] = 0
+    for causal in (False, True):
+        fwd = lambda q, k, v, qg, kg, vg: oracle_longformer(q, k, v, window, gidx, key_mask=km, causal=causal,
+                                                           Qg=qg, Kg=kg, Vg=vg)
+        got = oracle_longformer_bwd(*X[:3], dO, window, gidx, key_mask=km, causal=causal,
+                                    Qg=X[3], Kg=X[4], Vg=X[5])
+        eps = 1e-5
+        for which in range(6):
+            x = X[which]
+            want = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                old = x[idx]
+                x[idx] = old + eps
+                lp = float((fwd(*X) * dO).sum())
+                x[idx] = old - eps
+                lm = float((fwd(*X) * dO).sum())
+                x[idx] = old
+                want[idx] = (lp - lm) / (2 * eps)
+            np.testing.assert_allclose(got[which], want, atol=1e-8, rtol=1e-6, err_msg=f"grad {which} causal={causal}")
