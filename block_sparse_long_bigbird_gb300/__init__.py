@@ -213,6 +213,24 @@ def longformer_attn_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilation
     return dQ, dK, dV
 
 
+def longformer_attn_bwd_gproj(Q, K, V, Qg, Kg, Vg, dO, window, global_idx, key_mask=None, dilation=None,
+                              causal=False, out=None, stream=None):
+    """Gradients (dQ, dK, dV, dQg, dKg, dVg) of longformer_attn_fwd with separate global projections."""
+    _check_bwd(Q, K, V, dO)
+    _check_qkv(Qg, Kg, Vg)
+    if Qg.shape != Q.shape or Qg.dtype != Q.dtype:
+        raise ValueError("Qg, Kg, Vg must match Q in shape and dtype")
+    B, H, n, d = Q.shape
+    grads = out if out is not None else tuple(torch.empty_like(Q) for _ in range(6))
+    n_global = 0 if global_idx is None else int(global_idx.numel())
+    st = _lib.lib().longformer_attn_bwd_gproj(
+        *(_ptr(t) for t in (Q, K, V, Qg, Kg, Vg, dO)), *(_ptr(t) for t in grads), B, H, n, d, window,
+        _ptr(dilation), 1 if causal else 0, _ptr(global_idx if n_global else None), n_global, _ptr(key_mask),
+        _DTYPE[Q.dtype], _stream_handle(stream, Q.device))
+    _lib.check(st, "longformer_attn_bwd_gproj")
+    return grads
+
+
 def attn_bwd_workspace_bytes(B, H, n, d):
     return int(_lib.lib().sa_attn_bwd_workspace_bytes(B, H, n, d))
 

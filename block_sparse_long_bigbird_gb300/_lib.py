@@ -47,6 +47,7 @@ SIGNATURES = {
                               _VP]),
     "longformer_attn_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I,
                                  _VP]),
+    "longformer_attn_bwd_gproj": (_I, [_VP] * 13 + [_I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _I, _VP]),
     "sa_attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "sa_bigbird_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "sa_longformer_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),

@@ -484,6 +484,51 @@ sa_status longformer_attn_bwd(const void *Q, const void *K, const void *V, const
     return run_bwd(p, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+sa_status longformer_attn_bwd_gproj(const void *Q, const void *K, const void *V, const void *Qg, const void *Kg,
+                                    const void *Vg, const void *dO, void *dQ, void *dK, void *dV, void *dQg, void *dKg,
+                                    void *dVg, int B, int H, int n, int d, int window, const int32_t *dilation,
+                                    int causal, const int32_t *global_idx, int n_global, const uint8_t *key_mask,
+                                    sa_dtype dtype, sa_stream_t stream) {
+    if (dtype != SA_BF16 && dtype != SA_FP32) return SA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SA_ERR_INVALID_ARG;
+    const void *in[7] = {Q, K, V, Qg, Kg, Vg, dO};
+    void *out[6] = {dQ, dK, dV, dQg, dKg, dVg};
+    for (const void *t : in)
+        if (!t || !aligned16(t)) return SA_ERR_INVALID_ARG;
+    for (int a = 0; a < 6; ++a) {
+        if (!out[a] || !aligned16(out[a])) return SA_ERR_INVALID_ARG;
+        for (const void *t : in)
+            if (out[a] == t) return SA_ERR_INVALID_ARG;
+        for (int b = 0; b < a; ++b)
+            if (out[a] == out[b]) return SA_ERR_INVALID_ARG;
+    }
+    sa_status s = longformer_args_ok(B, H, n, d, window, global_idx, n_global);
+    if (s != SA_OK) return s;
+    // the non-global rows against Q, K, V, then the global rows against Qg, Kg, Vg
+    for (int set = 1; set <= 2; ++set) {
+        sa::Problem p = {};
+        p.kind = sa::kLongformer;
+        p.Q = set == 1 ? Q : Qg;
+        p.K = set == 1 ? K : Kg;
+        p.V = set == 1 ? V : Vg;
+        p.dO = dO;
+        p.dQ = set == 1 ? dQ : dQg;
+        p.dK = set == 1 ? dK : dKg;
+        p.dV = set == 1 ? dV : dVg;
+        p.B = B; p.H = H; p.n = n; p.d = d;
+        p.window = window;
+        p.global_idx = n_global > 0 ? global_idx : nullptr;
+        p.n_global = n_global;
+        p.dilation = dilation;
+        p.causal = causal;
+        p.key_mask = key_mask;
+        p.row_set = set;
+        s = run_bwd(p, dtype, reinterpret_cast<cudaStream_t>(stream));
+        if (s != SA_OK) return s;
+    }
+    return SA_OK;
+}
+
 size_t sa_attn_bwd_workspace_bytes(int B, int H, int n, int d) {
     if (!size_ok(B, H, n, d)) return 0;
     return bwd_stats_bytes(B, H, n);

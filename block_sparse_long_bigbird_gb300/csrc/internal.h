@@ -46,6 +46,9 @@ struct Problem {
     const void *dO;
     void *dQ, *dK, *dV;
     float *row_stats;
+    // Longformer backward with separate global projections: which query rows
+    // take part (0 all, 1 the non-global rows, 2 the global rows only)
+    int row_set;
 };
 
 // Row stride of the backward's per-row statistics: n rounded up to 64, so that

@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(Problem p) {
         const int il = row0 + rr, i = i0 + il;
         qvalid[rr] = (i < n) && (km ? (km[i] != 0) : true);
         qglob[rr] = LF ? (((misc[il >> 5] >> (il & 31)) & 1u) != 0u) : false;
+        if (LF && p.row_set != 0 && qglob[rr] != (p.row_set == 2)) qvalid[rr] = false;  // row outside the set
         m[rr] = -CUDART_INF_F;
         l[rr] = 0.f;
         u[rr] = 0.f;
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kThreads) bwd_cols_kernel(Problem p) {
                     for (int rr = 0; rr < R; ++rr) {
                         const int j = j0 + key0 + rr;
                         bool ok = rvalid[il] && kvalid[rr];
+                        if (LF && p.row_set != 0 && iglob != (p.row_set == 2)) ok = false;  // row outside the set
                         if (LF && ok) ok = lf_allowed(geo, i, j, iglob, kglob[rr]);
                         float pr = 0.f, ds = 0.f;
                         if (ok) {

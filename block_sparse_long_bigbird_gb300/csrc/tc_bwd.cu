@@ -100,6 +100,7 @@ struct BwdParams {
     int kind;                // kBigBird / kLongformer
     int nb, b, g, w, r, half;  // BigBird
     int window, ng, causal;  // Longformer
+    int row_set;             // Longformer: 0 all rows, 1 non-global rows, 2 global rows only
     int nch;                 // 64-row chunks per head, ceil(n / 64)
     float scale_log2, scale;
     unsigned long long wait_ns;
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(&hvt[c], halves);
     };
     int lstride = 1, lreach = 0;
+    bool tile_global = false;  // Longformer: a global position among the tile's rows or keys
     if (LF) {
         lf_geometry(p, h, lstride, lreach);
         if (tile == 0 && threadIdx.x == 0 && p.dilation) {
@@ -274,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (dil < 0 || dil > kMaxDilation) atomicOr(p.status, kDevBadIndex);
         }
         // chunks holding a global position (validated here once per head)
-        bool tile_global = false;
         for (int t = threadIdx.x; t < p.ng; t += kThreads) {
             const int gp = __ldg(p.gidx + t);
             if (gp < 0 || gp >= n || (t > 0 && __ldg(p.gidx + t - 1) >= gp)) {
@@ -348,6 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < kCN && y + e < n; ++e) vb |= (uint64_t)(km[y + e] != 0) << e;
         }
         vbt[c] = vb;
+        // global rows only: row pass tiles and key pass chunks without a global row have no work
+        if (LF && p.row_set == 2 && (PASS == kRowPass ? !tile_global : gbt[c] == 0ull)) vb = 0ull;
         if (vb != 0ull) atomicOr(&bmap[c >> 5], 1u << (c & 31));
     }
     __syncthreads();
@@ -520,8 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const int pos = t0 + row;                // this thread's query row (row pass) or key (key pass)
         const int hf = row >> 6;                 // tile half
-        const bool own_valid = pos_valid(km, pos, n);
         const bool own_global = LF && p.ng > 0 && pos < n && lf_is_global(p, pos);
+        // row pass: a query row outside the row set takes no part
+        const bool own_valid = pos_valid(km, pos, n) &&
+                               !(PASS == kRowPass && LF && p.row_set != 0 && own_global != (p.row_set == 2));
         const float sl2 = p.scale_log2;
         float m = -CUDART_INF_F, l = 0.f, u = 0.f;  // row pass statistics
         float lse = CUDART_INF_F, dlv = 0.f;
@@ -538,6 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 mk = ((rec.allow >> hf) & 1u) ? ~0ull : 0ull;
             }
+            // key pass: only the rows of the row set (the columns are query rows)
+            if (PASS == kKeyPass && LF && p.row_set != 0) mk &= (p.row_set == 2) ? rec.gbits : ~rec.gbits;
             return mk & rec.vbits;
         };
 
@@ -829,6 +836,7 @@ cudaError_t launch_tc_bwd(const Problem &pr, const TcConfig &cfg, cudaStream_t s
         bp.dilation = pr.dilation;
     }
     bp.nch = (pr.n + kCN - 1) / kCN;
+    bp.row_set = pr.row_set;
     bp.scale_log2 = kLog2e / sqrtf((float)pr.d);
     bp.scale = 1.f / sqrtf((float)pr.d);
     bp.wait_ns = (unsigned long long)cfg.wait_limit * 1000ull;

@@ -281,6 +281,26 @@ sa_status longformer_attn_bwd(const void *Q, const void *K, const void *V, const
                               const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
 
 /*
+ * longformer_attn_bwd_gproj - gradients of longformer_attn_fwd_gproj.
+ *
+ * With separate projections for global attention the rows of global tokens
+ * depend only on Qg, Kg, Vg and the other rows only on Q, K, V, so the six
+ * gradients split by rows: dQ, dK, dV sum over the non-global rows (dQ is 0
+ * on global rows), dQg, dKg, dVg over the global rows (dQg is 0 elsewhere).
+ * Formulas, layouts, numerics and scratch as for longformer_attn_bwd; two
+ * backward runs (four launches).
+ * Errors: as for longformer_attn_bwd; every pointer is required, and no output
+ *   may alias an input or another output.
+ */
+sa_status longformer_attn_bwd_gproj(const void *Q, const void *K, const void *V,
+                                    const void *Qg, const void *Kg, const void *Vg, const void *dO,
+                                    void *dQ, void *dK, void *dV, void *dQg, void *dKg, void *dVg,
+                                    int B, int H, int n, int d, int window,
+                                    const int32_t *dilation, int causal,
+                                    const int32_t *global_idx, int n_global,
+                                    const uint8_t *key_mask, sa_dtype dtype, sa_stream_t stream);
+
+/*
  * Scratch (workspace) sizing. The split-KV partials of the global rows and the
  * kernel's work counters need device scratch. By default the library allocates
  * it once per device (cudaMalloc, zeroed) and grows it on demand; a caller that

@@ -365,12 +365,12 @@ def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilati
     With the separate projections for global attention (``Qg``, ``Kg``,
     ``Vg``), the global rows depend only on the g set and the other rows only
     on Q, K, V, so the gradients split by rows: returns (dQ, dK, dV, dQg, dKg,
-    dVg), each set summed over its own rows (``terms`` is not supported then).
+    dVg), each set summed over its own rows; with ``terms``, ((six gradients),
+    six (sum |term|, sqrt(sum term^2)) pairs).
     """
     if Qg is not None:
-        assert not terms
         return _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, causal,
-                                     row_chunk, Qg, Kg, Vg)
+                                     row_chunk, Qg, Kg, Vg, terms)
     Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
     B, H, n, d = Q.shape
     dil = np.zeros(H, dtype=np.int64) if dilation is None else np.asarray(dilation, dtype=np.int64)
@@ -395,7 +395,8 @@ def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilati
     return ((dQ, dK, dV), T) if terms else (dQ, dK, dV)
 
 
-def _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, causal, row_chunk, Qg, Kg, Vg):
+def _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, causal, row_chunk, Qg, Kg, Vg,
+                          terms=False):
     """Separate projections: rows of global tokens against (Qg, Kg, Vg), the
     other rows against (Q, K, V); each row set's mask is the row's usual mask."""
     Q, K, V, dO = _as_f64(Q), _as_f64(K), _as_f64(V), _as_f64(dO)
@@ -405,6 +406,8 @@ def _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, c
     is_global = np.zeros(n, dtype=bool)
     is_global[np.asarray(global_idx, dtype=np.int64)] = True
     out = [np.zeros_like(Q) for _ in range(6)]
+    ta = [np.zeros_like(Q) for _ in range(6)]  # sum |term|
+    t2 = [np.zeros_like(Q) for _ in range(6)]  # sum term^2
     for h in range(H):
         for beta in range(B):
             kv = None if key_mask is None else np.asarray(key_mask[beta]) != 0
@@ -414,11 +417,21 @@ def _longformer_bwd_split(Q, K, V, dO, window, global_idx, key_mask, dilation, c
                     rr = rows[c0:c0 + row_chunk]
                     mask = _apply_validity(longformer_allowed(n, window, global_idx, rr, dilation=dil[h],
                                                               causal=causal), rr, kv)
-                    dq, dk, dv = masked_attention_grads(q[beta, h, rr], k[beta, h], v[beta, h], mask, dO[beta, h, rr])
+                    args = (q[beta, h, rr], k[beta, h], v[beta, h], mask, dO[beta, h, rr])
+                    dq, dk, dv = masked_attention_grads(*args)
                     out[base][beta, h, rr] = dq
                     out[base + 1][beta, h] += dk
                     out[base + 2][beta, h] += dv
-    return tuple(out)
+                    if terms:
+                        (qa, qr), (ka, kr), (va, vr) = masked_attention_grad_terms(*args)
+                        ta[base][beta, h, rr], t2[base][beta, h, rr] = qa, qr * qr
+                        ta[base + 1][beta, h] += ka
+                        t2[base + 1][beta, h] += kr * kr
+                        ta[base + 2][beta, h] += va
+                        t2[base + 2][beta, h] += vr * vr
+    if not terms:
+        return tuple(out)
+    return tuple(out), tuple((ta[i], np.sqrt(t2[i])) for i in range(6))
 
 
 # ---------------------------------------------------------------------------

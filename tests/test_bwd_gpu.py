@@ -123,3 +123,39 @@ def test_bwd_bad_random_entry_latches_status():
     sa.bigbird_attn_bwd(Q, K, V, dO, 64, 2, 3, 3, table.to(dev))
     assert sa.get_last_device_status() == sa._lib.SA_ERR_BAD_INDEX
     assert sa.get_last_device_status() == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("causal,dilation", [(False, None), (True, [0, 2])])
+def test_longformer_gproj_bwd(path, causal, dilation):
+    """Six gradients of the separate-projection forward: non-global rows into
+    Q, K, V, global rows into Qg, Kg, Vg."""
+    from oracle import oracle_longformer_bwd
+    from parity_util import assert_close_grad, set_path
+    dev = torch.device("cuda:0")
+    B, H, n, d, window = 2, 2, 1000, 64, 128
+    gidx = torch.tensor([0, 5, 500, 999], dtype=torch.int32)
+    km = make_key_mask(B, n)
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=110)
+    Qg, Kg, Vg = make_qkv(B, H, n, d, "bf16", cfg_id=111)
+    dO = make_grad_out(B, H, n, d, "bf16", cfg_id=110)
+    set_path(path)
+    try:
+        dil = None if dilation is None else torch.tensor(dilation, dtype=torch.int32, device=dev)
+        grads = sa.longformer_attn_bwd_gproj(*(t.to(dev) for t in (Q, K, V, Qg, Kg, Vg, dO)), window,
+                                             gidx.to(dev), km.to(dev), dilation=dil, causal=causal)
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    grads = [t.float().cpu().numpy() for t in grads]
+    for beta in range(B):
+        for h in range(H):
+            sl = (slice(beta, beta + 1), slice(h, h + 1))
+            refs, terms = oracle_longformer_bwd(Q[sl], K[sl], V[sl], dO[sl], window, gidx.numpy(),
+                                                key_mask=km[beta:beta + 1].numpy(),
+                                                dilation=None if dilation is None else [dilation[h]], causal=causal,
+                                                Qg=Qg[sl], Kg=Kg[sl], Vg=Vg[sl], terms=True)
+            for i, name in enumerate(("dQ", "dK", "dV", "dQg", "dKg", "dVg")):
+                assert_close_grad(grads[i][beta, h], refs[i][0, 0], "bf16",
+                                  terms=(terms[i][0][0, 0], terms[i][1][0, 0]), what=f"gproj {name} b={beta} h={h}")
