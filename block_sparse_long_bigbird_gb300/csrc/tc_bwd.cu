@@ -114,17 +114,18 @@ struct BwdParams {
 };
 
 // Per-chunk tables after the chunk bitmap (byte offsets from the bitmap):
-// validity bits [nch] (uint64), Longformer global bits [nch] (uint64), and
-// the tile halves each chunk is marked for [nch] (uint32; bit h: half h).
+// validity bits [nch] (uint64; only with key padding, else computed from n),
+// Longformer global bits [nch] (uint64; Longformer only), and the tile halves
+// each chunk is marked for [nch] (uint32; bit h: half h).
 struct ChunkTables {
     int vb_off, gb_off, hv_off, bytes;
 };
-__host__ __device__ inline ChunkTables chunk_tables(int nch) {
+__host__ __device__ inline ChunkTables chunk_tables(int nch, bool padded, bool lf) {
     ChunkTables t;
     const int words = (nch + 31) / 32;
     t.vb_off = ((words * 4) + 7) & ~7;
-    t.gb_off = t.vb_off + 8 * nch;
-    t.hv_off = t.gb_off + 8 * nch;
+    t.gb_off = t.vb_off + (padded ? 8 * nch : 0);
+    t.hv_off = t.gb_off + (lf ? 8 * nch : 0);
     t.bytes = t.hv_off + 4 * nch;
     return t;
 }
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *nsteps_s = reinterpret_cast<int *>(smem + C::MISC_OFF + 8);
     unsigned *bmap = reinterpret_cast<unsigned *>(smem + C::MAP_OFF);
     const int words = (p.nch + 31) / 32;
-    const ChunkTables ct = chunk_tables(p.nch);
+    const ChunkTables ct = chunk_tables(p.nch, km != nullptr, LF);
     unsigned long long *vbt = reinterpret_cast<unsigned long long *>(smem + C::MAP_OFF + ct.vb_off);
     unsigned long long *gbt = reinterpret_cast<unsigned long long *>(smem + C::MAP_OFF + ct.gb_off);
     unsigned *hvt = reinterpret_cast<unsigned *>(smem + C::MAP_OFF + ct.hv_off);
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             vb = 0ull;
             for (int e = 0; e < kCN && y + e < n; ++e) vb |= (uint64_t)(km[y + e] != 0) << e;
         }
-        vbt[c] = vb;
+        if (km) vbt[c] = vb;
         // global rows only: row pass tiles and key pass chunks without a global row have no work
         if (LF && p.row_set == 2 && (PASS == kRowPass ? !tile_global : gbt[c] == 0ull)) vb = 0ull;
         if (vb != 0ull) atomicOr(&bmap[c >> 5], 1u << (c & 31));
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 BwdStep &rec = steps[ii];
                 rec.y = c * kCN;
                 rec.allow = hvt[c];
-                rec.vbits = vbt[c];
+                rec.vbits = km ? vbt[c] : bits_below64(n - c * kCN);
                 rec.gbits = LF ? gbt[c] : 0ull;
                 mbar_arrive(bar(C::B_IF + ii));
             }
@@ -786,8 +787,8 @@ bool make_map(CUtensorMap *m, const void *base, int BH, int n, int d) {
 }
 
 template <int D>
-size_t bwd_smem_bytes(int nch) {
-    return (size_t)BwdCfg<D>::MAP_OFF + (size_t)chunk_tables(nch).bytes + 1024;  // + alignment slack
+size_t bwd_smem_bytes(int nch, bool padded, bool lf) {
+    return (size_t)BwdCfg<D>::MAP_OFF + (size_t)chunk_tables(nch, padded, lf).bytes + 1024;  // + alignment slack
 }
 
 template <int D>
@@ -797,7 +798,7 @@ cudaError_t launch_d(const Problem &pr, const BwdParams &bp, cudaStream_t s) {
     if (!make_map(&mQ, pr.Q, BH, pr.n, D) || !make_map(&mK, pr.K, BH, pr.n, D) || !make_map(&mV, pr.V, BH, pr.n, D) ||
         !make_map(&mdO, pr.dO, BH, pr.n, D))
         return cudaErrorInvalidValue;
-    const size_t smem = bwd_smem_bytes<D>(bp.nch);
+    const size_t smem = bwd_smem_bytes<D>(bp.nch, bp.key_mask != nullptr, bp.kind == kLongformer);
     if (smem > 232448) return cudaErrorNotSupported;
     const dim3 grid((pr.n + kTM - 1) / kTM, BH);
     auto rows = sparse_tc_bwd<D, kRowPass>;

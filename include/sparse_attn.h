@@ -255,6 +255,12 @@ sa_status longformer_attn_fwd_host(const void *Q, const void *K, const void *V, 
  *   Deterministic: no atomics; every sum runs in a fixed order.
  * Scratch: 2 * B * H * n64 floats of per-row statistics in the workspace,
  *   n64 = n rounded up to a multiple of 64 (sa_attn_bwd_workspace_bytes).
+ * Limits: the bf16 tensor-core kernels keep per-64-row tables in shared
+ *   memory, which bounds n (d = 64: about 1.4M tokens, 500K with key padding;
+ *   d = 128: about 470K, 160K with key padding; the Longformer call with
+ *   padding about 300K / 97K). Beyond that the call returns
+ *   SA_ERR_UNSUPPORTED before any work is queued; SA_OPT_FORCE_SIMT runs the
+ *   SIMT backward, which has no such bound.
  * Errors: as for bigbird_attn_fwd, plus SA_ERR_INVALID_ARG when an output
  *   aliases an input or another output.
  */
