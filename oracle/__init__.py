@@ -50,6 +50,8 @@ Every function pinned by a test that does not reuse this code; the pins are in
                            scaled_dot_product_attention with the same mask;
                            shift invariance sum_j dK_j = 0 and sum_j dV_j =
                            sum of dO over rows with an allowed key)
+  oracle_bigbird_bwd_      pinned (equals the full oracle_bigbird_bwd at the
+  sampled                  sampled rows and key blocks, with padding)
   masked_attention_grad_   pinned (brute-force sums of |term| and term^2 on
   terms                    a tiny case; the exact gradient lies inside the
                            rounding bound it yields for bf16-rounded P and dS)
@@ -68,6 +70,7 @@ from .attention import (
     masked_attention_grads,
     masked_attention_grad_terms,
     oracle_bigbird_bwd,
+    oracle_bigbird_bwd_sampled,
     oracle_longformer_bwd,
     bigbird_attended_pairs,
     longformer_attended_pairs,
@@ -88,6 +91,7 @@ __all__ = [
     "masked_attention_grads",
     "masked_attention_grad_terms",
     "oracle_bigbird_bwd",
+    "oracle_bigbird_bwd_sampled",
     "oracle_longformer_bwd",
     "bigbird_attended_pairs",
     "longformer_attended_pairs",

@@ -266,7 +266,7 @@ def masked_attention_grads(q, k, v, mask, dout):
 
     q, dout: [m, d]; k, v: [n, d]; mask: bool [m, n].
     """
-    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    q, k, v, dout = (_as_f64(x) for x in (q, k, v, dout))
     scale = 1.0 / math.sqrt(q.shape[1])
     p = masked_softmax_probs(q, k, mask)
     dv = p.T @ dout
@@ -286,7 +286,7 @@ def masked_attention_grad_terms(q, k, v, mask, dout):
     factor P or dS by a relative e (at most e * sum |t|), the second is the
     scale of that effect when the roundings are independent.
     """
-    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    q, k, v, dout = (_as_f64(x) for x in (q, k, v, dout))
     scale = 1.0 / math.sqrt(q.shape[1])
     p = masked_softmax_probs(q, k, mask)
     dp = dout @ v.T
@@ -355,6 +355,59 @@ def oracle_bigbird_bwd(Q, K, V, dO, b, g, w, rand_table, key_mask=None, row_chun
                         T[which][kind][beta, h] = tt[which][kind]
             dQ[beta, h], dK[beta, h], dV[beta, h] = res
     return ((dQ, dK, dV), T) if terms else (dQ, dK, dV)
+
+
+def oracle_bigbird_bwd_sampled(Qh, Kh, Vh, dOh, b, g, w, rand_row, rows, key_blocks, key_valid=None,
+                               row_chunk=512):
+    """Exact gradients of one head at sampled places, for sequences too long for
+    ``oracle_bigbird_bwd``: dQ on ``rows``, and dK, dV on the keys of
+    ``key_blocks``, with the term sizes of ``masked_attention_grad_terms``.
+
+    dQ_i needs only row i's own neighbourhood. dK_j and dV_j sum over the rows
+    that see key j; for the sampled key blocks those rows are found from the
+    block mask (its transpose), so every contribution is included.
+    Returns ((dq, (A, R)), (dk, (A, R)), (dv, (A, R))): dq [len(rows), d],
+    dk and dv [len(keys), d] in the order of the sampled blocks' keys.
+    """
+    Qh, Kh, Vh, dOh = (_as_f64(x) for x in (Qh, Kh, Vh, dOh))
+    n, d = Qh.shape
+    nb = n // b
+    blk = bigbird_block_allowed(nb, g, w, rand_row)
+    kv = None if key_valid is None else np.asarray(key_valid, dtype=bool)
+    cols = np.arange(n)
+
+    def mask_of(rr):
+        return _apply_validity(blk[rr[:, None] // b, cols[None, :] // b], rr, kv)
+
+    rows = np.asarray(rows)
+    dq = np.zeros((len(rows), d))
+    qa = np.zeros((len(rows), d))
+    qr = np.zeros((len(rows), d))
+    for c0 in range(0, len(rows), row_chunk):
+        rr = rows[c0:c0 + row_chunk]
+        args = (Qh[rr], Kh, Vh, mask_of(rr), dOh[rr])
+        dq[c0:c0 + len(rr)] = masked_attention_grads(*args)[0]
+        (a, r2), _, _ = masked_attention_grad_terms(*args)
+        qa[c0:c0 + len(rr)], qr[c0:c0 + len(rr)] = a, r2
+    keys = np.concatenate([np.arange(kb * b, (kb + 1) * b) for kb in key_blocks])
+    seeing = np.nonzero(blk[:, np.asarray(key_blocks)].any(axis=1))[0]  # query blocks that see a sampled block
+    srows = np.concatenate([np.arange(qb * b, (qb + 1) * b) for qb in seeing])
+    dk = np.zeros((n, d))
+    dv = np.zeros((n, d))
+    ka, kr2, va, vr2 = (np.zeros((n, d)) for _ in range(4))
+    for c0 in range(0, len(srows), row_chunk):
+        rr = srows[c0:c0 + row_chunk]
+        args = (Qh[rr], Kh, Vh, mask_of(rr), dOh[rr])
+        _, k1, v1 = masked_attention_grads(*args)
+        _, (a1, r1), (a2, r2) = masked_attention_grad_terms(*args)
+        dk += k1
+        dv += v1
+        ka += a1
+        kr2 += r1 * r1
+        va += a2
+        vr2 += r2 * r2
+    return ((dq, (qa, qr)), (dk[keys], (ka[keys], np.sqrt(kr2[keys]))),
+            (dv[keys], (va[keys], np.sqrt(vr2[keys]))))
 
 
 def oracle_longformer_bwd(Q, K, V, dO, window, global_idx, key_mask=None, dilation=None,

@@ -159,3 +159,49 @@ def test_longformer_gproj_bwd(path, causal, dilation):
             for i, name in enumerate(("dQ", "dK", "dV", "dQg", "dKg", "dVg")):
                 assert_close_grad(grads[i][beta, h], refs[i][0, 0], "bf16",
                                   terms=(terms[i][0][0, 0], terms[i][1][0, 0]), what=f"gproj {name} b={beta} h={h}")
+
+
+def _sampled_bwd_check(wl_name, path, heads, kblocks, seed):
+    """Full-size backward in the bench's configuration: dQ on sampled query
+    blocks, dK and dV on sampled non-global key blocks, against the exact
+    sampled oracle, within the bf16 rounding bound."""
+    from block_sparse_long_bigbird_gb300.workloads import WORKLOADS
+    from oracle import oracle_bigbird_bwd_sampled
+    from parity_util import assert_close_grad, sampled_bigbird_rows, set_path
+    wl = WORKLOADS[wl_name]
+    dev = torch.device("cuda:0")
+    Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, "bf16", sigma=wl.sigma, cfg_id=wl.cfg_id)
+    dO = make_grad_out(wl.B, wl.H, wl.n, wl.d, "bf16", cfg_id=wl.cfg_id)
+    table = sa.build_bigbird_pattern(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+    km = make_key_mask(wl.B, wl.n) if wl.padded else None
+    set_path(path)
+    try:
+        grads = sa.bigbird_attn_bwd(*(t.to(dev) for t in (Q, K, V, dO)), wl.b, wl.g, wl.w, wl.r, table.to(dev),
+                                    None if km is None else km.to(dev))
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        set_path("tc")
+    grads = [t.float().cpu().numpy() for t in grads]
+    rows = sampled_bigbird_rows(wl.n, wl.b, wl.g, n_random_blocks=3, seed=seed)
+    keys = np.concatenate([np.arange(k * wl.b, (k + 1) * wl.b) for k in kblocks])
+    for beta, h in heads:
+        (dq, tq), (dk, tk), (dv, tv) = oracle_bigbird_bwd_sampled(
+            Q[beta, h], K[beta, h], V[beta, h], dO[beta, h], wl.b, wl.g, wl.w, table.numpy()[h], rows, kblocks,
+            key_valid=None if km is None else km[beta].numpy())
+        assert_close_grad(grads[0][beta, h][rows], dq, "bf16", terms=tq, what=f"{wl_name} dQ {beta},{h}")
+        assert_close_grad(grads[1][beta, h][keys], dk, "bf16", terms=tk, what=f"{wl_name} dK {beta},{h}")
+        assert_close_grad(grads[2][beta, h][keys], dv, "bf16", terms=tv, what=f"{wl_name} dV {beta},{h}")
+
+
+def test_bigbird_bwd_n65536_d128_sampled():
+    _sampled_bwd_check("bigbird_bwd_bf16_n65536_d128", "tc", [(0, 0), (0, 13)], [5, 200, 511], seed=7)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bigbird_bwd_n16384_padded_sampled(path):
+    from block_sparse_long_bigbird_gb300.workloads import WORKLOADS, Workload
+    import dataclasses
+    base = WORKLOADS["bigbird_bf16_n16384_padded"]
+    WORKLOADS.setdefault("_bwd_n16384_padded", dataclasses.replace(base, name="_bwd_n16384_padded", grad=True))
+    _sampled_bwd_check("_bwd_n16384_padded", path, [(0, 0), (1, 15)], [3, 100, 255], seed=8)

@@ -650,3 +650,26 @@ def test_longformer_global_projection_grads_match_finite_differences():
                 x[idx] = old
                 want[idx] = (lp - lm) / (2 * eps)
             np.testing.assert_allclose(got[which], want, atol=1e-8, rtol=1e-6, err_msg=f"grad {which} causal={causal}")
+
+
+def test_sampled_backward_equals_full_backward():
+    """The sampled backward (for long sequences) reproduces the full backward's
+    dQ rows and dK, dV key blocks, term sizes included."""
+    from oracle import oracle_bigbird_bwd, oracle_bigbird_bwd_sampled
+    n, b, g, w, r, d = 512, 32, 2, 3, 2, 8
+    table = bigbird_random_table(4, 1, n, b, g, w, r)
+    Q, K, V, dO = (_rand((1, 1, n, d), s) for s in (121, 122, 123, 124))
+    km = np.ones((1, n), dtype=np.uint8)
+    km[0, 470:] = 0
+    full, terms = oracle_bigbird_bwd(Q, K, V, dO, b, g, w, table, key_mask=km, terms=True)
+    rows = np.array([0, 5, 100, 101, 300, 511])
+    kblocks = [3, 7, 15]
+    keys = np.concatenate([np.arange(k * b, (k + 1) * b) for k in kblocks])
+    (dq, tq), (dk, tk), (dv, tv) = oracle_bigbird_bwd_sampled(Q[0, 0], K[0, 0], V[0, 0], dO[0, 0], b, g, w,
+                                                              table[0], rows, kblocks, key_valid=km[0], row_chunk=50)
+    np.testing.assert_allclose(dq, full[0][0, 0, rows], atol=1e-12)
+    np.testing.assert_allclose(dk, full[1][0, 0, keys], atol=1e-12)
+    np.testing.assert_allclose(dv, full[2][0, 0, keys], atol=1e-12)
+    for got, want, idx in ((tq, terms[0], rows), (tk, terms[1], keys), (tv, terms[2], keys)):
+        np.testing.assert_allclose(got[0], want[0][0, 0, idx], atol=1e-12)
+        np.testing.assert_allclose(got[1], want[1][0, 0, idx], atol=1e-12)
