@@ -36,6 +36,9 @@ struct DeviceState {
 };
 
 std::mutex g_mutex;
+// Held while a host-buffer call enqueues its work: calls share the staging
+// sets, and the event chain between them is built in enqueue order.
+std::mutex g_host_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<int> g_force_simt{0};
 std::atomic<long long> g_wait_limit{2000000};  // microseconds
@@ -257,6 +260,7 @@ sa_status host_path_init(DeviceState &st) {
 // is more than a chunk) `hc` consecutive heads of one batch entry; either way
 // its rows are one contiguous stretch of the [B][H][n][d] arrays.
 sa_status run_host(const sa::Problem &hp, sa_dtype dtype, cudaStream_t s) {
+    std::lock_guard<std::mutex> host_lock(g_host_mutex);
     const size_t elem = dtype == SA_FP32 ? 4 : 2;
     const int B = hp.B, H = hp.H, n = hp.n, d = hp.d;
     const size_t head_bytes = (size_t)n * d * elem;

@@ -215,6 +215,9 @@ sa_status longformer_attn_fwd_gproj(const void *Q, const void *K, const void *V,
  * Scratch: device staging of 2 x 4 x (heads per chunk) x n x d elements plus
  *   the tables, allocated by the library on first use and grown on demand;
  *   plus the device entry points' own workspace.
+ * Concurrency: calls from several host threads are serialised while they
+ *   enqueue (they share the staging sets); on the device each call's copies
+ *   wait for the previous call's last output copy.
  * Errors: as for bigbird_attn_fwd / longformer_attn_fwd_ex (NULL or aliasing
  *   tensors are SA_ERR_INVALID_ARG).
  */
