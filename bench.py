@@ -178,6 +178,11 @@ def make_problem(wl, rank=0):
     prob = {"Q": Q, "K": K, "V": V, "key_mask": km}
     if wl.grad:
         prob["dO"] = make_grad_out(wl.B, wl.H, wl.n, wl.d, wl.dtype, cfg_id=wl.cfg_id + 100 * rank)
+    if wl.gproj:
+        prob["Qg"], prob["Kg"], prob["Vg"] = make_qkv(wl.B, wl.H, wl.n, wl.d, wl.dtype, sigma=wl.sigma,
+                                                      cfg_id=wl.cfg_id + 100 * rank + 1)
+    if wl.dilation:
+        prob["dilation"] = torch.tensor(wl.dilation, dtype=torch.int32)
     if wl.kind == "bigbird":
         table = sa.build_bigbird_pattern(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
         prob["table"] = table
@@ -188,8 +193,9 @@ def make_problem(wl, rank=0):
     else:
         gidx = torch.arange(wl.n_global, dtype=torch.int32)
         prob["gidx"] = gidx
-        pairs = accounting.longformer_pairs(wl.n, wl.window, gidx.numpy(),
-                                            None if km is None else km.numpy()) * wl.H
+        dil = wl.dilation or (0,) * wl.H
+        pairs = sum(accounting.longformer_pairs(wl.n, wl.window, gidx.numpy(), None if km is None else km.numpy(),
+                                                dilation=dh, causal=wl.causal) for dh in dil)
         if km is None:
             pairs *= wl.B
     tokens = wl.B * wl.n if km is None else int(km.sum())
@@ -216,38 +222,75 @@ def call(wl, dev_t, out, stream=None):
                             dev_t.get("key_mask"), out=out, stream=stream)
     else:
         sa.longformer_attn_fwd(dev_t["Q"], dev_t["K"], dev_t["V"], wl.window, dev_t["gidx"],
-                               dev_t.get("key_mask"), out=out, stream=stream)
+                               dev_t.get("key_mask"), out=out, stream=stream, dilation=dev_t.get("dilation"),
+                               causal=wl.causal, Qg=dev_t.get("Qg"), Kg=dev_t.get("Kg"), Vg=dev_t.get("Vg"))
+
+
+LONG_SEQ = 8192  # beyond this the CPU baseline samples rows instead of whole heads
 
 
 def cpu_oracle_sample(wl, prob, budget_s):
-    """Time the float64 oracle on whole heads of the workload until `budget_s` is used."""
+    """Time the float64 oracle on the workload until `budget_s` is used: whole
+    (batch, head) pairs, or for sequences longer than LONG_SEQ blocks of rows
+    of successive heads (credited with the exact pair count of those rows)."""
     import numpy as np
 
     from block_sparse_long_bigbird_gb300 import accounting
-    from oracle import oracle_bigbird, oracle_bigbird_bwd, oracle_longformer, oracle_longformer_bwd
+    from oracle import (bigbird_allowed, longformer_allowed, masked_attention_grads, oracle_bigbird,
+                        oracle_bigbird_bwd, oracle_longformer, oracle_longformer_bwd)
 
     Q, K, V, km = prob["Q"], prob["K"], prob["V"], prob["key_mask"]
     per_pair = float(accounting.BWD_FLOPS_PER_PAIR_PER_D if wl.grad else accounting.FWD_FLOPS_PER_PAIR_PER_D)
     heads = [(beta, h) for beta in range(wl.B) for h in range(wl.H)]
+    long_seq = wl.n > LONG_SEQ
+    nrows = max(64, min(1024, (1 << 24) // wl.n))  # the dense masked oracle costs n per row
+    rows = np.arange(wl.n // 2, wl.n // 2 + nrows) if long_seq else None  # a block of rows mid-sequence
     done, flops = 0, 0.0
     t0 = time.perf_counter()
     for beta, h in heads:
         sl = (slice(beta, beta + 1), slice(h, h + 1))
         kmb = None if km is None else km[beta:beta + 1].numpy()
+        kv = None if kmb is None else kmb[0] != 0
         if wl.kind == "bigbird":
             tab = prob["table"].numpy()[h:h + 1]
-            if wl.grad:
+            if long_seq:
+                mask = bigbird_allowed(wl.n, wl.b, wl.g, wl.w, tab[0], rows)
+                if kv is not None:
+                    mask = mask & kv[None, :] & kv[rows][:, None]
+                if wl.grad:
+                    # every backward product for the row block's pairs: its dQ rows and
+                    # its contributions to dK and dV
+                    masked_attention_grads(Q[beta, h, rows], K[beta, h], V[beta, h], mask, prob["dO"][beta, h, rows])
+                else:
+                    oracle_bigbird(Q[sl], K[sl], V[sl], wl.b, wl.g, wl.w, tab, key_mask=kmb, rows=rows)
+            elif wl.grad:
                 oracle_bigbird_bwd(Q[sl], K[sl], V[sl], prob["dO"][sl], wl.b, wl.g, wl.w, tab, key_mask=kmb)
             else:
                 oracle_bigbird(Q[sl], K[sl], V[sl], wl.b, wl.g, wl.w, tab, key_mask=kmb)
-            flops += per_pair * wl.d * accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, tab, kmb)
+            if long_seq:
+                flops += per_pair * wl.d * int(mask.sum())
+            else:
+                flops += per_pair * wl.d * accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, tab, kmb)
         else:
             gi = prob["gidx"].numpy()
+            dh = wl.dilation[h] if wl.dilation else 0
+            gsl = {k: prob[k][sl] for k in ("Qg", "Kg", "Vg")} if wl.gproj else {}
             if wl.grad:
-                oracle_longformer_bwd(Q[sl], K[sl], V[sl], prob["dO"][sl], wl.window, gi, key_mask=kmb)
+                oracle_longformer_bwd(Q[sl], K[sl], V[sl], prob["dO"][sl], wl.window, gi, key_mask=kmb,
+                                      dilation=[dh], causal=wl.causal, **gsl)
+                flops += per_pair * wl.d * accounting.longformer_pairs(wl.n, wl.window, gi, kmb, dilation=dh,
+                                                                       causal=wl.causal)
             else:
-                oracle_longformer(Q[sl], K[sl], V[sl], wl.window, gi, key_mask=kmb)
-            flops += per_pair * wl.d * accounting.longformer_pairs(wl.n, wl.window, gi, kmb)
+                oracle_longformer(Q[sl], K[sl], V[sl], wl.window, gi, key_mask=kmb, rows=rows, dilation=[dh],
+                                  causal=wl.causal, **gsl)
+                if long_seq:
+                    mask = longformer_allowed(wl.n, wl.window, gi, rows, dilation=dh, causal=wl.causal)
+                    if kv is not None:
+                        mask = mask & kv[None, :] & kv[rows][:, None]
+                    flops += per_pair * wl.d * int(mask.sum())
+                else:
+                    flops += per_pair * wl.d * accounting.longformer_pairs(wl.n, wl.window, gi, kmb, dilation=dh,
+                                                                           causal=wl.causal)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -258,8 +301,10 @@ def cpu_oracle_sample(wl, prob, budget_s):
         cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
     except Exception:
         cores = len(os.sched_getaffinity(0))
+    what = (f"rows [n/2, n/2 + {nrows}) (dense masked float64, all n keys per row; backward: every product "
+            f"of those rows' pairs) of") if long_seq else "all rows of"
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {len(heads)} (batch, head) pairs, all rows, float64 numpy, {dt:.1f} s"}
+            "sample": f"{what} {done} of {len(heads)} (batch, head) pairs, float64 numpy, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -299,6 +344,12 @@ def workload_config(wl):
         cfg.update({"b": wl.b, "g": wl.g, "w": wl.w, "r": wl.r, "pattern_seed": wl.seed})
     else:
         cfg.update({"window": wl.window, "n_global": wl.n_global})
+        if wl.dilation:
+            cfg["dilation"] = list(wl.dilation)
+        if wl.causal:
+            cfg["causal"] = True
+        if wl.gproj:
+            cfg["separate_global_projections"] = True
     if wl.padded:
         cfg["key_padding"] = "lengths ~ U[n/2, n] (seed 2000)"
     return cfg
@@ -397,10 +448,13 @@ def main(argv=None):
 
     e2e = None
     if not args.no_e2e:
-        if wl.grad:
-            # backward: host->device copies of Q, K, V, dO, the device call,
-            # device->host copies of dQ, dK, dV, all on the launching stream
-            ins, outs = ("Q", "K", "V", "dO"), out
+        if wl.grad or wl.gproj:
+            # backward (and the separate-projection forward, which has no
+            # host-buffer entry point): host->device copies of the inputs, the
+            # device call, device->host copies of the outputs, all on the
+            # launching stream
+            ins = ("Q", "K", "V", "dO") if wl.grad else ("Q", "K", "V", "Qg", "Kg", "Vg")
+            outs = out if wl.grad else (out,)
             host = {k: prob[k].pin_memory() for k in ins}
             out_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
 
@@ -417,7 +471,7 @@ def main(argv=None):
             # forward: the host-buffer entry point, which pipelines the copies
             # against the computation chunk by chunk
             host = {k: prob[k].pin_memory() for k in ("Q", "K", "V")}
-            tabs = {k: prob[k] for k in ("table", "gidx", "key_mask") if prob.get(k) is not None}
+            tabs = {k: prob[k] for k in ("table", "gidx", "key_mask", "dilation") if prob.get(k) is not None}
             out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
             def e2e_step():
@@ -426,7 +480,8 @@ def main(argv=None):
                                              tabs.get("table"), tabs.get("key_mask"), out=out_h, stream=stream)
                 else:
                     sa.longformer_attn_fwd_host(host["Q"], host["K"], host["V"], wl.window, tabs.get("gidx"),
-                                                tabs.get("key_mask"), out=out_h, stream=stream)
+                                                tabs.get("key_mask"), out=out_h, stream=stream,
+                                                dilation=tabs.get("dilation"), causal=wl.causal)
 
             h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(tabs.values()))
             d2h = out_h.numel() * out_h.element_size()
@@ -449,7 +504,7 @@ def main(argv=None):
             e_t = float(t.item())
         e2e = {"value": world * prob["flops"] / (e_t * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_t, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "api": "backward: device call with stream-ordered copies" if wl.grad
+               "api": "device call with stream-ordered copies" if (wl.grad or wl.gproj)
                else f"{wl.kind}_attn_fwd_host (host buffers, copies pipelined in the library)"}
 
     cpu = None

@@ -52,26 +52,43 @@ def bigbird_pairs(n, b, g, w, table, key_mask=None):
     return total
 
 
-def longformer_pairs(n, window, global_idx, key_mask=None):
-    """Attended pairs of one head summed over batch entries (B = 1 if no mask)."""
+def longformer_pairs(n, window, global_idx, key_mask=None, dilation=0, causal=False):
+    """Attended pairs of one head summed over batch entries (B = 1 if no mask).
+
+    ``dilation``: the head's window gaps (stride dilation + 1); ``causal``: no
+    key after the query ("Longformer", Sec. 3.1 and App. B). Counted per row
+    with prefix sums over each residue class of the stride.
+    """
     half = window // 2
+    s = int(dilation) + 1
+    reach = half * s
     G = np.unique(np.asarray(global_idx, dtype=np.int64))
     is_g = np.zeros(n, dtype=bool)
     is_g[G] = True
     masks = [np.ones(n, dtype=bool)] if key_mask is None else [np.asarray(m) != 0 for m in key_mask]
+    i = np.arange(n)
+    m = -(-n // s)  # positions per residue class (the last classes may hold one fewer)
     total = 0
     for valid in masks:
-        cum = np.concatenate([[0], np.cumsum(valid)])
-        gv = np.cumsum(np.concatenate([[0], (is_g & valid).astype(np.int64)]))
-        n_valid = int(cum[-1])
-        for i in range(n):
-            if not valid[i]:
-                continue
-            if is_g[i]:
-                total += n_valid
-                continue
-            lo, hi = max(0, i - half), min(n - 1, i + half)
-            band = int(cum[hi + 1] - cum[lo])
-            outside = int(gv[n] - (gv[hi + 1] - gv[lo]))  # valid globals outside the band
-            total += band + outside
+        # per residue class c: prefix counts of valid keys and of valid global keys
+        vc = np.zeros((s, m + 1), dtype=np.int64)
+        gc = np.zeros((s, m + 1), dtype=np.int64)
+        for c in range(s):
+            pos = np.arange(c, n, s)
+            vc[c, 1:len(pos) + 1] = np.cumsum(valid[pos])
+            vc[c, len(pos) + 1:] = vc[c, len(pos)]
+            gc[c, 1:len(pos) + 1] = np.cumsum(valid[pos] & is_g[pos])
+            gc[c, len(pos) + 1:] = gc[c, len(pos)]
+        c = i % s
+        lo = i - np.minimum(reach, (i // s) * s)          # first band position of the class
+        hi_full = i + np.minimum(reach, ((n - 1 - i) // s) * s)
+        hi = i if causal else hi_full
+        band = vc[c, hi // s + 1] - vc[c, lo // s]
+        band_g = gc[c, hi // s + 1] - gc[c, lo // s]
+        cum_v = np.concatenate([[0], np.cumsum(valid)])
+        cum_g = np.concatenate([[0], np.cumsum(valid & is_g)])
+        upto = (i + 1) if causal else np.full(n, n)
+        glob_keys = cum_g[upto]                       # valid global keys the row may see
+        row_counts = np.where(is_g, cum_v[upto], band + glob_keys - band_g)
+        total += int(row_counts[valid].sum())
     return total

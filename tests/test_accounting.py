@@ -26,3 +26,16 @@ def test_longformer_pairs(n, window, G):
     km[0, : n // 2 + 3] = 1
     km[1, 1::2] = 1
     assert accounting.longformer_pairs(n, window, G, km) == longformer_attended_pairs(n, window, G, km, B=2)
+
+
+@pytest.mark.parametrize("n,window,G,dil,causal", [(1000, 64, [0, 5, 500, 999], 1, False),
+                                                   (777, 96, [3], 2, True), (512, 128, [], 3, True),
+                                                   (300, 1000, [7, 8], 5, False), (640, 32, [0, 1, 2], 0, True)])
+def test_longformer_pairs_dilated_causal(n, window, G, dil, causal):
+    assert accounting.longformer_pairs(n, window, G, dilation=dil, causal=causal) == \
+        longformer_attended_pairs(n, window, G, dilation=[dil], causal=causal)
+    km = np.zeros((2, n), dtype=np.uint8)
+    km[0, : n // 2 + 3] = 1
+    km[1, 1::3] = 1
+    assert accounting.longformer_pairs(n, window, G, km, dilation=dil, causal=causal) == \
+        longformer_attended_pairs(n, window, G, km, B=2, dilation=[dil], causal=causal)

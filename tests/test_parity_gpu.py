@@ -439,3 +439,23 @@ def test_bigbird_etc_via_block_kernel(path, g_tokens, b, n_reg):
         for h in range(H):
             assert_close(O[beta, h].numpy()[keep], ref[beta, h], 2e-2, 2e-3, what=f"etc beta={beta} h={h}")
     assert np.all(O[:, :, g_tokens:gp].numpy() == 0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_charlm_n23040_workload(path):
+    """Autoregressive char-LM shape (B=16 H=8 n=23040, window 512, dilation 3 on
+    the last two heads, causal, no global tokens): sampled rows of a plain and a
+    dilated head, first and last batch entry."""
+    wl = WORKLOADS["longformer_charlm_bf16_n23040"]
+    rows = np.concatenate([np.arange(0, 300), np.arange(11000, 11500), np.arange(wl.n - 300, wl.n)])
+    longformer_case(wl.B, wl.H, wl.n, wl.d, wl.window, None, cfg_id=wl.cfg_id, path=path, rows=rows,
+                    heads=[(0, 0), (15, 7)], dilation=list(wl.dilation), causal=True)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_longformer_gproj_n4096_workload(path):
+    """Bench shape with separate global projections (generated as the bench does)."""
+    wl = WORKLOADS["longformer_gproj_bf16_n4096"]
+    rows = np.concatenate([np.arange(0, 200), np.arange(2000, 2100), np.arange(wl.n - 100, wl.n)])
+    _gproj_case(wl.B, wl.H, wl.n, wl.d, wl.window, torch.arange(wl.n_global, dtype=torch.int32), path,
+                rows=rows, heads=[(0, 0), (3, 11)], cfg_id=wl.cfg_id)
