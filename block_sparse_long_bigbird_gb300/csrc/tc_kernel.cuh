@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // Units are decoded (and their key/value blocks prefetched into L2)
         // one unit ahead of the TMA loads that consume them.
         uint32_t g = 0, qcnt = 0;
-        uint32_t k_arms[C::KST] = {}, v_arms[C::VST] = {};
+        uint32_t issued = 0;  // steps whose K and V copies are out (drained on abort)
         bool q_tma_last = false;  // the latest Q fill was a TMA copy (drained on abort)
         uint64_t *gmk = reinterpret_cast<uint64_t *>(list);  // Longformer: global-key bits per step
         bool ok = true;
@@ -751,7 +751,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     }
                     // step info -> softmax
                     const uint32_t ii = g % C::SI;
-                    if (g >= C::SI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / C::SI) - 1) & 1, ctl))) break;
+                    const uint32_t sk = g % C::KST;
+                    if constexpr (!C::LOADERS) {
+                        // One wait per step. Stage sk is released once PV of step
+                        // g - KST has completed. PV of a step is issued only after
+                        // every softmax thread published its P, and each softmax
+                        // warp releases its step record before that, so the
+                        // record slot of step g - SI (<= g - KST) is free as well.
+                        static_assert(C::SI >= C::KST && C::KST == C::VST, "record ring covers the stage ring");
+                        if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
+                    } else {
+                        if (g >= C::SI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / C::SI) - 1) & 1, ctl))) break;
+                    }
                     if (lane == 0) {
                         steps[ii] = si;
                         if (LF) {
@@ -764,9 +775,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         // K and V of the step in one copy instruction, one box per
                         // lane: a thread's bulk copies complete one after another,
                         // different lanes' copies overlap
-                        const uint32_t sk = g % C::KST, sv = g % C::VST;
-                        if (g >= C::KST && !(ok = wait_warp(bar(C::B_KE + sk), ((g / C::KST) - 1) & 1, ctl))) break;
-                        if (g >= C::VST && !(ok = wait_warp(bar(C::B_VE + sv), ((g / C::VST) - 1) & 1, ctl))) break;
+                        const uint32_t sv = sk;
                         if (lane == 0) mbar_arrive_expect_tx(bar(C::B_KF + sk), C::KV_BYTES);
                         if (lane == 1) mbar_arrive_expect_tx(bar(C::B_VF + sv), C::KV_BYTES);
                         __syncwarp();
@@ -782,8 +791,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                             tma_load_3d(dst + dc * C::KV_REGION + s * 8192, tm,
                                         bar(is_v ? C::B_VF + sv : C::B_KF + sk), dc * 64, si.y[s], cur.bh);
                         }
-                        ++k_arms[sk];
-                        ++v_arms[sv];
+                        ++issued;
                     }
                     if (t == 1) {
                         decode_ahead();
@@ -798,10 +806,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             slow_cur = slow_nxt;
         }
         if (!ok && lane == 0) {  // abort: wait for the copies this tile still has in flight
-            for (int i = 0; i < C::KST; ++i)
-                if (k_arms[i]) wait_drain(bar(C::B_KF + i), (k_arms[i] - 1) & 1, G.wait_ns);
-            for (int i = 0; i < C::VST; ++i)
-                if (v_arms[i]) wait_drain(bar(C::B_VF + i), (v_arms[i] - 1) & 1, G.wait_ns);
+            for (uint32_t i = 0; i < (uint32_t)C::KST && i < issued; ++i) {
+                const uint32_t arms = (issued - 1 - i) / C::KST + 1;  // copies into stage i
+                wait_drain(bar(C::B_KF + i), (arms - 1) & 1, G.wait_ns);
+                wait_drain(bar(C::B_VF + i), (arms - 1) & 1, G.wait_ns);
+            }
             if (qcnt && q_tma_last) wait_drain(bar(C::B_QF), (qcnt - 1) & 1, G.wait_ns);
         }
     } else if (role == 1) {
@@ -1141,10 +1150,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 // has read the P that S_g's slot held and its V stage is free.
                 // The stage releases go out from here rather than as tensor-core
                 // commits, each of which costs the shared MMA front end about as
-                // much as an MMA.
+                // much as an MMA. With separate K and V loaders K_g and V_{g-2} are
+                // released on their own barriers; with one producer both halves of
+                // stage g-2 are released at once, so the producer waits once.
                 if (tid == 0) {
-                    mbar_arrive(bar(C::B_KE + g % C::KST));
-                    if (g >= 2) mbar_arrive(bar(C::B_VE + (g - 2) % C::VST));
+                    if constexpr (C::LOADERS) {
+                        mbar_arrive(bar(C::B_KE + g % C::KST));
+                        if (g >= 2) mbar_arrive(bar(C::B_VE + (g - 2) % C::VST));
+                    } else {
+                        if (g >= 2) mbar_arrive(bar(C::B_KE + (g - 2) % C::KST));
+                    }
                 }
                 const uint32_t sa = tmem + lane_base + sb * C::KB;
                 // Stream the step's 64-key sub-blocks ("halves"; one for d = 64):
