@@ -48,6 +48,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
+// Predicated forms: only lanes with `act` set perform the operation, and the
+// warp does not branch (no reconvergence around a one-lane operation).
+__device__ __forceinline__ void mbar_arrive_if(uint32_t bar, bool act) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+                 "r"((uint32_t)act)
+                 : "memory");
+}
+// arrive.expect_tx of `bytes` on `bar`, then the tiled copy completing on it
+__device__ __forceinline__ void tma_load_3d_if(bool act, uint32_t dst, const void *tmap, uint32_t bar, int x, int y, int z,
+                                               uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %7, 0;\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%5], %6;\n\t"
+        "@p cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "r"(bytes), "r"((uint32_t)act)
+        : "memory");
+}
 // Contiguous global -> shared copy of `bytes` (multiple of 16; both addresses
 // 16-byte aligned), completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

@@ -10,9 +10,10 @@
 // tensor is materialised and no score matrix leaves the SM.
 //
 // Work unit = one 128-row query tile of one (batch, head):
-//   * BigBird, b = 64: query blocks (2t, 2t+1); the unit walks the sorted
-//     union of their key-block lists, two 64-key blocks per 128-key step, and
-//     each 64-row half masks the blocks outside its own list.
+//   * BigBird, b = 64: query blocks (2t, 2t+1); the unit walks the union of
+//     their key-block lists (blocks both see first, then one-half blocks
+//     alternating halves), one 64-key block per step for d = 64 and two for
+//     d = 128, and each 64-row half masks the blocks outside its own list.
 //   * BigBird, b = 128: query block t; one key block per step.
 //   * Tiles that contain a global query block (attends all n keys) are split
 //     into `splits` chunks of steps (split-KV); each chunk writes an fp32
@@ -100,6 +101,8 @@ struct Cfg {
     static constexpr int SUB = KB / 64;             // 64-key sub-blocks per step
     static constexpr int NS = 2;                    // S slots per tile (QK^T of step g+1 overlaps softmax g)
     static constexpr int KST = (KB == 64) ? 5 : 3;  // K / V stages per tile
+    // Q buffers per tile pipeline (two let the next unit's Q load while the
+    // current unit runs; measured no faster for d = 64 than a fifth K/V stage)
     static constexpr int VST = KST, NQ = 1;
     static constexpr int SI = (KB == 64) ? 8 : 6;   // step-info ring depth
     static constexpr int Q_BYTES = kBM * D * 2;     // Q tile
@@ -111,7 +114,7 @@ struct Cfg {
     static constexpr int V_OFF = K_OFF + KST * KV_BYTES;
     static constexpr int BIG = V_OFF + VST * KV_BYTES;
     // barrier slots within a tile's small area
-    static constexpr int B_QF = 0, B_QE = 1, B_KF = 2, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
+    static constexpr int B_QF = 0, B_QE = B_QF + NQ, B_KF = B_QE + NQ, B_KE = B_KF + KST, B_VF = B_KE + KST, B_VE = B_VF + VST,
                          B_IF = B_VE + VST, B_IE = B_IF + SI, B_SF = B_IE + SI, B_PF = B_SF + NS, B_PV = B_PF + NS,
                          B_UF = B_PV + NS, B_UE = B_UF + kNU, B_DRAIN = B_UE + kNU, B_COUNT = B_DRAIN + 1;
     static constexpr int BAR_OFF = 0;
@@ -294,24 +297,25 @@ __device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1,
     const bool a0 = valid && (j0 < G.g || v < G.g || abs(v - j0) <= G.half || in_r0);
     const bool a1 = valid && j1 >= 0 && (j1 < G.g || v < G.g || abs(v - j1) <= G.half || in_r1);
     const unsigned vm = __ballot_sync(kFull, valid);
-    // Rank among the survivors = survivors holding a smaller block, found by
-    // comparing block indices bit by bit from the top (one ballot per bit;
-    // far cheaper than a shuffle per lane beside busy softmax warps): `eq`
-    // keeps the survivors equal to v on the bits seen so far, `less` collects
-    // those found smaller. Valid indices are < nb <= 2^nbits.
-    unsigned eq = vm, less = 0u;
-    const int nbits = 32 - __clz(max(G.nb - 1, 1));
-    for (int bb = nbits - 1; bb >= 0; --bb) {
-        const bool one = (v >> bb) & 1;
-        const unsigned ones = __ballot_sync(kFull, one);
-        if (one) {
-            less |= eq & ~ones;
-            eq &= ones;
-        } else {
-            eq &= ~ones;
-        }
+    // Order for steps of two 64-key sub-slots: blocks both query halves see
+    // first, then blocks of one half only, alternating half 0 / half 1, so a
+    // step's two sub-slots give both halves' warps work where possible (a
+    // sub-slot masked for a half costs that half's warps nothing). The rest of
+    // the longer one-half run follows. Within a class, lane order.
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned m_both = __ballot_sync(kFull, valid && a0 && a1);
+    const unsigned m_0 = __ballot_sync(kFull, valid && a0 && !a1);
+    const unsigned m_1 = __ballot_sync(kFull, valid && a1 && !a0);
+    const int nboth = __popc(m_both), n0 = __popc(m_0), n1 = __popc(m_1), k = min(n0, n1);
+    int pos;
+    if (a0 && a1) {
+        pos = __popc(m_both & below);
+    } else {
+        const int i = __popc((a0 ? m_0 : m_1) & below);
+        pos = nboth + (i < k ? 2 * i + (a0 ? 0 : 1) : 2 * k + (i - k));
     }
-    const int pos = __popc(less);
+    // survivors that no query half sees (possible only with a key mask) go last
+    if (!a0 && !a1) pos = nboth + n0 + n1 + __popc(vm & ~(m_both | m_0 | m_1) & below);
     if (valid) list[pos] = (uint32_t)v | (a0 ? (1u << 30) : 0u) | (a1 ? (1u << 31) : 0u);
     __syncwarp();
     return __popc(vm);
@@ -380,8 +384,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (int x = 0; x < C::NT; ++x) {
             const uint32_t bb = sbase + C::SMALL_OFF + x * C::SMALL + C::BAR_OFF;
             auto bar = [&](int i) { return bb + 8u * (uint32_t)i; };
-            mbar_init(bar(C::B_QF), 1);
-            mbar_init(bar(C::B_QE), 1);
+            for (int i = 0; i < C::NQ; ++i) {
+                mbar_init(bar(C::B_QF + i), 1);
+                mbar_init(bar(C::B_QE + i), 1);
+            }
             for (int i = 0; i < C::KST; ++i) {
                 mbar_init(bar(C::B_KF + i), 1);
                 mbar_init(bar(C::B_KE + i), 1);
@@ -615,7 +621,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 const UnitPtrs up = unit_ptrs(p, cur);
                 const int nlist = cur.pad0;
                 // ---- Q tile
-                if (qcnt >= 1 && !(ok = wait_warp(bar(C::B_QE), (qcnt - 1) & 1, ctl))) break;
+                const uint32_t qs = qcnt % C::NQ;  // Q buffer of this unit
+                if (qcnt >= (uint32_t)C::NQ && !(ok = wait_warp(bar(C::B_QE + qs), ((qcnt / C::NQ) - 1) & 1, ctl)))
+                    break;
                 if (LF && cur.step0 >= 0) {
                     // Longformer global rows: gather them with plain loads into
                     // the 128-B swizzled K-major layout the TMA would produce
@@ -625,7 +633,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) pr[k] = global_row(p.gidx, G.ng, G.n, cur.q0 + lane + 32 * k);
                     const uint4 *qh = reinterpret_cast<const uint4 *>(p.Qg + (size_t)cur.bh * G.n * D);
-                    uint8_t *qs = smem + x * C::BIG + C::Q_OFF;
+                    uint8_t *qsm = smem + x * C::BIG + C::Q_OFF + qs * C::Q_BYTES;
 #pragma unroll 8
                     for (int it = 0; it < kBM * CPR / 32; ++it) {
                         const int idx = it * 32 + lane;
@@ -634,20 +642,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         const int src = grp == 0 ? pr[0] : grp == 1 ? pr[1] : grp == 2 ? pr[2] : pr[3];
                         const int pos = __shfl_sync(kFull, src, r & 31);
                         const uint4 v = pos < G.n ? __ldg(qh + (size_t)pos * CPR + cq) : make_uint4(0u, 0u, 0u, 0u);
-                        *reinterpret_cast<uint4 *>(qs + (cq >> 3) * kRegionBytes + r * 128 +
+                        *reinterpret_cast<uint4 *>(qsm + (cq >> 3) * kRegionBytes + r * 128 +
                                                    (((cq & 7) ^ (r & 7)) << 4)) = v;
                     }
                     fence_proxy_async_smem();  // generic-proxy writes -> tcgen05 operand reads
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::B_QF));
+                    if (lane == 0) mbar_arrive(bar(C::B_QF + qs));
                     q_tma_last = false;
                 } else {
                     if (lane == 0) {
-                        const uint32_t dst = tbase + C::Q_OFF;
-                        mbar_arrive_expect_tx(bar(C::B_QF), C::Q_BYTES);
+                        const uint32_t dst = tbase + C::Q_OFF + qs * C::Q_BYTES;
+                        mbar_arrive_expect_tx(bar(C::B_QF + qs), C::Q_BYTES);
                         for (int dc = 0; dc < D / 64; ++dc)
                             for (int rh = 0; rh < 2; ++rh)
-                                tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF), dc * 64,
+                                tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF + qs), dc * 64,
                                             cur.q0 + rh * 64, cur.bh);
                     }
                     q_tma_last = true;
@@ -763,35 +771,34 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     } else {
                         if (g >= C::SI && !(ok = wait_warp(bar(C::B_IE + ii), ((g / C::SI) - 1) & 1, ctl))) break;
                     }
-                    if (lane == 0) {
+                    if constexpr (!C::LOADERS) {
+                        // Branch-free: every lane stores the same record, lane 0
+                        // publishes it, and two lanes arm the K and V stages and
+                        // issue their copies (one box each). A thread's bulk copies
+                        // complete one after another, so the issuing pair moves on
+                        // by two lanes every step: consecutive steps' copies overlap.
+                        static_assert(D == 64 && C::SUB == 1, "one 64-key box per K or V step");
+                        steps[ii] = si;
+                        if (LF) {
+                            gmk[2 * ii] = gm2[0];
+                            gmk[2 * ii + 1] = gm2[1];
+                        }
+                        mbar_arrive_if(bar(C::B_IF + ii), lane == 0);
+                        const int kl = (int)((2u * g) & 31u);  // this step's K lane; V: the next one
+                        const bool is_v = lane == kl + 1;
+                        // global-row units read the global projections' keys and values
+                        const bool gsel = LF && cur.step0 >= 0;
+                        const CUtensorMap *tm = is_v ? (gsel ? &tmVg : &tmV) : (gsel ? &tmKg : &tmK);
+                        tma_load_3d_if(lane == kl || is_v, tbase + (is_v ? C::V_OFF : C::K_OFF) + sk * C::KV_BYTES, tm,
+                                       bar((is_v ? C::B_VF : C::B_KF) + sk), 0, si.y[0], cur.bh, C::KV_BYTES);
+                        ++issued;
+                    } else if (lane == 0) {
                         steps[ii] = si;
                         if (LF) {
                             gmk[2 * ii] = gm2[0];
                             gmk[2 * ii + 1] = gm2[1];
                         }
                         mbar_arrive(bar(C::B_IF + ii));
-                    }
-                    if constexpr (!C::LOADERS) {
-                        // K and V of the step in one copy instruction, one box per
-                        // lane: a thread's bulk copies complete one after another,
-                        // different lanes' copies overlap
-                        const uint32_t sv = sk;
-                        if (lane == 0) mbar_arrive_expect_tx(bar(C::B_KF + sk), C::KV_BYTES);
-                        if (lane == 1) mbar_arrive_expect_tx(bar(C::B_VF + sv), C::KV_BYTES);
-                        __syncwarp();
-                        constexpr int BOXES = C::SUB * (D / 64);  // boxes per K (or V) stage
-                        if (lane < 2 * BOXES) {
-                            const bool is_v = lane & 1;
-                            const int bx = lane >> 1, s = bx / (D / 64), dc = bx % (D / 64);
-                            const uint32_t dst = is_v ? tbase + C::V_OFF + sv * C::KV_BYTES
-                                                      : tbase + C::K_OFF + sk * C::KV_BYTES;
-                            // global-row units read the global projections' keys and values
-                            const bool gsel = LF && cur.step0 >= 0;
-                            const CUtensorMap *tm = is_v ? (gsel ? &tmVg : &tmV) : (gsel ? &tmKg : &tmK);
-                            tma_load_3d(dst + dc * C::KV_REGION + s * 8192, tm,
-                                        bar(is_v ? C::B_VF + sv : C::B_KF + sk), dc * 64, si.y[s], cur.bh);
-                        }
-                        ++issued;
                     }
                     if (t == 1) {
                         decode_ahead();
@@ -811,7 +818,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 wait_drain(bar(C::B_KF + i), (arms - 1) & 1, G.wait_ns);
                 wait_drain(bar(C::B_VF + i), (arms - 1) & 1, G.wait_ns);
             }
-            if (qcnt && q_tma_last) wait_drain(bar(C::B_QF), (qcnt - 1) & 1, G.wait_ns);
+            if (qcnt && q_tma_last) wait_drain(bar(C::B_QF + (qcnt - 1) % C::NQ), ((qcnt - 1) / C::NQ) & 1, G.wait_ns);
         }
     } else if (role == 1) {
         // ================================================================ MMA issuer (tile x)
@@ -867,8 +874,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     pend = -1;
                     continue;
                 }
-                const uint32_t ob = qcnt & 1;
-                if (!(ok = wait_warp(bar(C::B_QF), qcnt & 1, ctl))) break;
+                const uint32_t ob = qcnt & 1, qs = qcnt % C::NQ;
+                if (!(ok = wait_warp(bar(C::B_QF + qs), (qcnt / C::NQ) & 1, ctl))) break;
+                const uint64_t dQ = dQ0 + (uint64_t)((qs * C::Q_BYTES) >> 4);
                 tc_fence_after();
                 for (int t = 0; t < n_steps; ++t, ++g) {
                     const uint32_t sk = g % C::KST, sb = g % C::NS;
@@ -880,10 +888,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint64_t qoff = (uint64_t)(((kk >> 2) * kRegionBytes + (kk & 3) * 32) >> 4);
                             const uint64_t koff = ko + (uint64_t)(((kk >> 2) * C::KV_REGION + (kk & 3) * 32) >> 4);
-                            mma_bf16_ss(tmem + sb * C::KB, dQ0 + qoff, dK0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                            mma_bf16_ss(tmem + sb * C::KB, dQ + qoff, dK0 + koff, idesc_qk, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(bar(C::B_SF + sb));
-                        if (t == n_steps - 1) mma_commit(bar(C::B_QE));
+                        if (t == n_steps - 1) mma_commit(bar(C::B_QE + qs));
                     }
                     __syncwarp();
                     // two S slots: S_g overlaps the softmax of step g-1, then PV_{g-1}
