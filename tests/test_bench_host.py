@@ -1,0 +1,75 @@
+"""Host-side logic of bench.py (no GPU): clock-sample parsing, the stored
+DRAM-traffic records and the workload descriptions in the JSON line."""
+
+import json
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from block_sparse_long_bigbird_gb300.workloads import WORKLOADS  # noqa: E402
+
+
+def _sampler(lines):
+    s = bench.ClockSampler(0)
+    s.lines = lines
+    return s.summary()
+
+
+def test_clock_summary_median_and_reasons():
+    # index, sm, max sm, power, active mask, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
+    lines = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1395.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    s = _sampler(lines)
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_flags_thermal_and_skips_garbage():
+    lines = [
+        "garbage line",
+        "0, 1500, 2070, 700.0, 0x40, Not Active, Active, Not Active, Not Active",
+        "0, N/A, 2070, 700.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    s = _sampler(lines)
+    assert s["samples"] == 1 and s["sm_mhz"] == 1500.0
+    assert s["reasons"] == ["hw_thermal_slowdown"]
+
+
+def test_clock_summary_without_samples():
+    s = _sampler([])
+    assert s["samples"] == 0 and s["reasons"] == ["unavailable"]
+
+
+def test_traffic_records_match_kernel_sources():
+    # The DRAM traffic the bench reports comes from an ncu capture of the
+    # committed kernel source; a record whose source hash no longer matches
+    # is ignored by the bench (traffic: null). The headline and Longformer
+    # forward records must be current.
+    assert bench.read_traffic("sparse_tc_fwd<64,dense,bigbird>", "bigbird_bf16_n4096") is not None
+    assert bench.read_traffic("sparse_tc_fwd<64,dense,longformer>", "longformer_bf16_n4096") is not None
+
+
+def test_traffic_records_are_well_formed():
+    with open(bench.TRAFFIC_FILE) as f:
+        entries = json.load(f)
+    for e in entries:
+        assert set(e) >= {"kernel", "workload", "source_sha", "dram_bytes_per_launch", "source"}
+        assert e["workload"] in WORKLOADS
+        assert isinstance(e["dram_bytes_per_launch"], int) and e["dram_bytes_per_launch"] > 0
+        assert len(e["source_sha"]) == 16
+
+
+def test_workload_configs_name_the_workload_and_no_model():
+    for name, wl in WORKLOADS.items():
+        cfg = bench.workload_config(wl)
+        assert cfg["workload"].startswith(name)
+        assert "model" not in cfg
+        for key in ("B", "H", "n", "d", "dtype", "l2"):
+            assert key in cfg, (name, key)
