@@ -17,7 +17,8 @@ flushed (256 MiB write) between timed steps, outside the timed events.
 every host->device copy of Q, K, V (and the tables) and the device->host copy
 of O is inside the timed region; the library pipelines them against the
 computation chunk by chunk. `--impl reference` times the float64 CPU oracle instead.
-Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
+Multi-GPU (torchrun): every rank runs its own batch of B sequences drawn
+from its own seeds, so the global batch is world x B (weak scaling, no
 collective on the data path); the step time is the max over ranks.
 """
 
@@ -39,6 +40,10 @@ from block_sparse_long_bigbird_gb300.workloads import HEADLINE, WORKLOADS  # noq
 METRIC = "useful TFLOP/s and tokens/s of sparse attn fwd at n=4096, % of bf16 tensor peak"
 METRIC_BWD = "useful TFLOP/s and tokens/s of sparse attn bwd (dQ, dK, dV) at n=4096, % of bf16 tensor peak"
 UNIT = "TFLOP/s"
+# useful FLOPs per attended pair, in units of d: the score (2d) and the P.V
+# accumulation (2d) forward; five such products backward
+FWD_FLOPS_PER_PAIR_PER_D = 4
+BWD_FLOPS_PER_PAIR_PER_D = 10
 L2_FLUSH_BYTES = 256 << 20
 TC_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_kernel.cuh")
 TC_BWD_SOURCE = os.path.join(ROOT, "block_sparse_long_bigbird_gb300", "csrc", "tc_bwd.cu")
@@ -76,11 +81,11 @@ def aggregate(per_rank_ms, flops_per_rank_step, tokens_per_rank_step):
     }
 
 
-def shard_units(n_units, world, rank):
-    """Contiguous share of `n_units` independent (batch, head) units for `rank`."""
-    base, extra = divmod(n_units, world)
-    start = rank * base + min(rank, extra)
-    return start, start + base + (1 if rank < extra else 0)
+def rank_seed_offset(rank):
+    """Seed offset of a rank's own batch: under torchrun the global batch is
+    world x B sequences and rank k draws sequences [k B, (k + 1) B) from its
+    own seeds (cfg_id + 100 k), so no rank needs another rank's data."""
+    return 100 * rank
 
 
 def read_peaks():
@@ -165,24 +170,37 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def make_problem(wl, rank=0):
-    """Seeded synthetic inputs on the CPU, plus the useful-work count of one step."""
+def make_inputs(wl, rank=0):
+    """Seeded synthetic inputs on the CPU (the shared generators only: no
+    pattern table and no work count, which each side makes for itself)."""
     import torch
 
-    import block_sparse_long_bigbird_gb300 as sa
-    from block_sparse_long_bigbird_gb300 import accounting
     from block_sparse_long_bigbird_gb300.inputs import make_grad_out, make_key_mask, make_qkv
 
-    Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, wl.dtype, sigma=wl.sigma, cfg_id=wl.cfg_id + 100 * rank)
+    Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, wl.dtype, sigma=wl.sigma, cfg_id=wl.cfg_id + rank_seed_offset(rank))
     km = make_key_mask(wl.B, wl.n) if wl.padded else None
     prob = {"Q": Q, "K": K, "V": V, "key_mask": km}
     if wl.grad:
-        prob["dO"] = make_grad_out(wl.B, wl.H, wl.n, wl.d, wl.dtype, cfg_id=wl.cfg_id + 100 * rank)
+        prob["dO"] = make_grad_out(wl.B, wl.H, wl.n, wl.d, wl.dtype, cfg_id=wl.cfg_id + rank_seed_offset(rank))
     if wl.gproj:
         prob["Qg"], prob["Kg"], prob["Vg"] = make_qkv(wl.B, wl.H, wl.n, wl.d, wl.dtype, sigma=wl.sigma,
-                                                      cfg_id=wl.cfg_id + 100 * rank + 1)
+                                                      cfg_id=wl.cfg_id + rank_seed_offset(rank) + 1)
     if wl.dilation:
         prob["dilation"] = torch.tensor(wl.dilation, dtype=torch.int32)
+    if wl.kind != "bigbird":
+        prob["gidx"] = torch.arange(wl.n_global, dtype=torch.int32)
+    prob["tokens"] = wl.B * wl.n if km is None else int(km.sum())
+    return prob
+
+
+def make_problem(wl, rank=0):
+    """The product side of one step: inputs, the library's pattern table and
+    the useful-work count of one step (the library's host accounting)."""
+    import block_sparse_long_bigbird_gb300 as sa
+    from block_sparse_long_bigbird_gb300 import accounting
+
+    prob = make_inputs(wl, rank)
+    km = prob["key_mask"]
     if wl.kind == "bigbird":
         table = sa.build_bigbird_pattern(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
         prob["table"] = table
@@ -191,18 +209,15 @@ def make_problem(wl, rank=0):
         else:
             pairs = accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, table.numpy(), km.numpy())
     else:
-        gidx = torch.arange(wl.n_global, dtype=torch.int32)
-        prob["gidx"] = gidx
         dil = wl.dilation or (0,) * wl.H
-        pairs = sum(accounting.longformer_pairs(wl.n, wl.window, gidx.numpy(), None if km is None else km.numpy(),
-                                                dilation=dh, causal=wl.causal) for dh in dil)
+        pairs = sum(accounting.longformer_pairs(wl.n, wl.window, prob["gidx"].numpy(),
+                                                None if km is None else km.numpy(), dilation=dh, causal=wl.causal)
+                    for dh in dil)
         if km is None:
             pairs *= wl.B
-    tokens = wl.B * wl.n if km is None else int(km.sum())
     prob["pairs"] = pairs
     per_pair = accounting.BWD_FLOPS_PER_PAIR_PER_D if wl.grad else accounting.FWD_FLOPS_PER_PAIR_PER_D
     prob["flops"] = float(per_pair) * wl.d * pairs
-    prob["tokens"] = tokens
     return prob
 
 
@@ -235,12 +250,15 @@ def cpu_oracle_sample(wl, prob, budget_s):
     of successive heads (credited with the exact pair count of those rows)."""
     import numpy as np
 
-    from block_sparse_long_bigbird_gb300 import accounting
-    from oracle import (bigbird_allowed, longformer_allowed, masked_attention_grads, oracle_bigbird,
-                        oracle_bigbird_bwd, oracle_longformer, oracle_longformer_bwd)
+    from oracle import (bigbird_allowed, bigbird_attended_pairs, bigbird_random_table, longformer_allowed,
+                        longformer_attended_pairs, masked_attention_grads, oracle_bigbird, oracle_bigbird_bwd,
+                        oracle_longformer, oracle_longformer_bwd)
 
     Q, K, V, km = prob["Q"], prob["K"], prob["V"], prob["key_mask"]
-    per_pair = float(accounting.BWD_FLOPS_PER_PAIR_PER_D if wl.grad else accounting.FWD_FLOPS_PER_PAIR_PER_D)
+    # The oracle side draws its own pattern table and counts its own work; it
+    # takes only the seeded inputs from the shared generators.
+    per_pair = float(BWD_FLOPS_PER_PAIR_PER_D if wl.grad else FWD_FLOPS_PER_PAIR_PER_D)
+    table = bigbird_random_table(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r) if wl.kind == "bigbird" else None
     heads = [(beta, h) for beta in range(wl.B) for h in range(wl.H)]
     long_seq = wl.n > LONG_SEQ
     nrows = max(64, min(1024, (1 << 24) // wl.n))  # the dense masked oracle costs n per row
@@ -252,7 +270,7 @@ def cpu_oracle_sample(wl, prob, budget_s):
         kmb = None if km is None else km[beta:beta + 1].numpy()
         kv = None if kmb is None else kmb[0] != 0
         if wl.kind == "bigbird":
-            tab = prob["table"].numpy()[h:h + 1]
+            tab = table[h:h + 1]
             if long_seq:
                 mask = bigbird_allowed(wl.n, wl.b, wl.g, wl.w, tab[0], rows)
                 if kv is not None:
@@ -270,7 +288,7 @@ def cpu_oracle_sample(wl, prob, budget_s):
             if long_seq:
                 flops += per_pair * wl.d * int(mask.sum())
             else:
-                flops += per_pair * wl.d * accounting.bigbird_pairs(wl.n, wl.b, wl.g, wl.w, tab, kmb)
+                flops += per_pair * wl.d * bigbird_attended_pairs(wl.n, wl.b, wl.g, wl.w, tab, key_mask=kmb)
         else:
             gi = prob["gidx"].numpy()
             dh = wl.dilation[h] if wl.dilation else 0
@@ -278,8 +296,8 @@ def cpu_oracle_sample(wl, prob, budget_s):
             if wl.grad:
                 oracle_longformer_bwd(Q[sl], K[sl], V[sl], prob["dO"][sl], wl.window, gi, key_mask=kmb,
                                       dilation=[dh], causal=wl.causal, **gsl)
-                flops += per_pair * wl.d * accounting.longformer_pairs(wl.n, wl.window, gi, kmb, dilation=dh,
-                                                                       causal=wl.causal)
+                flops += per_pair * wl.d * longformer_attended_pairs(wl.n, wl.window, gi, key_mask=kmb,
+                                                                     dilation=[dh], causal=wl.causal)
             else:
                 oracle_longformer(Q[sl], K[sl], V[sl], wl.window, gi, key_mask=kmb, rows=rows, dilation=[dh],
                                   causal=wl.causal, **gsl)
@@ -289,8 +307,8 @@ def cpu_oracle_sample(wl, prob, budget_s):
                         mask = mask & kv[None, :] & kv[rows][:, None]
                     flops += per_pair * wl.d * int(mask.sum())
                 else:
-                    flops += per_pair * wl.d * accounting.longformer_pairs(wl.n, wl.window, gi, kmb, dilation=dh,
-                                                                           causal=wl.causal)
+                    flops += per_pair * wl.d * longformer_attended_pairs(wl.n, wl.window, gi, key_mask=kmb,
+                                                                         dilation=[dh], causal=wl.causal)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -312,7 +330,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     wl = WORKLOADS[args.workload]
-    prob = make_problem(wl)
+    prob = make_inputs(wl)  # the oracle arm loads no product code
     budget = max(0.5, min(args.cpu_seconds, 120.0) / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_oracle_sample(wl, prob, 0.0)

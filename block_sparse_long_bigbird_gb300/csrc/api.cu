@@ -311,14 +311,26 @@ sa_status run_host(const sa::Problem &hp, sa_dtype dtype, cudaStream_t s) {
     if (cudaEventRecord(st->ev_start, s) != cudaSuccess || cudaStreamWaitEvent(st->h2d, st->ev_start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(st->h2d, st->ev_last, 0) != cudaSuccess)
         return SA_ERR_CUDA;
+    // From here on copies may be queued on the library streams. An error exit
+    // still closes the chain: the output copies already queued end with
+    // ev_last on the output stream (which the copy-in stream also follows), and
+    // the caller's stream waits on it, so the caller may free or reuse its host
+    // buffers once its stream has drained, even after an error.
+    auto fail = [&](sa_status e) {
+        cudaEventRecord(st->ev_start, st->h2d);  // everything queued for copy-in so far
+        cudaStreamWaitEvent(st->d2h, st->ev_start, 0);
+        cudaEventRecord(st->ev_last, st->d2h);
+        cudaStreamWaitEvent(s, st->ev_last, 0);
+        return e;
+    };
     if (rand_bytes && cudaMemcpyAsync(d_rand, hp.rand_idx, rand_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
-        return SA_ERR_CUDA;
+        return fail(SA_ERR_CUDA);
     if (gidx_bytes && cudaMemcpyAsync(d_gidx, hp.global_idx, gidx_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
-        return SA_ERR_CUDA;
+        return fail(SA_ERR_CUDA);
     if (dil_bytes && cudaMemcpyAsync(d_dil, hp.dilation, dil_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
-        return SA_ERR_CUDA;
+        return fail(SA_ERR_CUDA);
     if (km_bytes && cudaMemcpyAsync(d_km, hp.key_mask, km_bytes, cudaMemcpyHostToDevice, st->h2d) != cudaSuccess)
-        return SA_ERR_CUDA;
+        return fail(SA_ERR_CUDA);
 
     int launches = 0, k = 0;
     const size_t chunk_cap = (size_t)bc * hc * head_bytes;
@@ -331,7 +343,7 @@ sa_status run_host(const sa::Problem &hp, sa_dtype dtype, cudaStream_t s) {
             const size_t bytes = (size_t)nb_here * cnt * head_bytes;
             uint8_t *dq = sets[set], *dk = dq + chunk_cap, *dv = dk + chunk_cap, *dout = dv + chunk_cap;
             // the staging set is free once chunk k - 2's output has been copied out
-            if (k >= 2 && cudaStreamWaitEvent(st->h2d, st->ev_out[set], 0) != cudaSuccess) return SA_ERR_CUDA;
+            if (k >= 2 && cudaStreamWaitEvent(st->h2d, st->ev_out[set], 0) != cudaSuccess) return fail(SA_ERR_CUDA);
             if (cudaMemcpyAsync(dq, static_cast<const uint8_t *>(hp.Q) + off, bytes, cudaMemcpyHostToDevice, st->h2d) !=
                     cudaSuccess ||
                 cudaMemcpyAsync(dk, static_cast<const uint8_t *>(hp.K) + off, bytes, cudaMemcpyHostToDevice, st->h2d) !=
@@ -339,7 +351,7 @@ sa_status run_host(const sa::Problem &hp, sa_dtype dtype, cudaStream_t s) {
                 cudaMemcpyAsync(dv, static_cast<const uint8_t *>(hp.V) + off, bytes, cudaMemcpyHostToDevice, st->h2d) !=
                     cudaSuccess ||
                 cudaEventRecord(st->ev_in[set], st->h2d) != cudaSuccess || cudaStreamWaitEvent(s, st->ev_in[set], 0) != cudaSuccess)
-                return SA_ERR_CUDA;
+                return fail(SA_ERR_CUDA);
             sa::Problem p = hp;
             p.Q = dq;
             p.K = dk;
@@ -355,14 +367,14 @@ sa_status run_host(const sa::Problem &hp, sa_dtype dtype, cudaStream_t s) {
                 p.dilation = d_dil ? d_dil + h0 : nullptr;
             }
             const sa_status e = run(p, dtype, s);
-            if (e != SA_OK) return e;
+            if (e != SA_OK) return fail(e);
             launches += g_last_launches;
             if (cudaEventRecord(st->ev_done[set], s) != cudaSuccess ||
                 cudaStreamWaitEvent(st->d2h, st->ev_done[set], 0) != cudaSuccess ||
                 cudaMemcpyAsync(static_cast<uint8_t *>(hp.O) + off, dout, bytes, cudaMemcpyDeviceToHost, st->d2h) !=
                     cudaSuccess ||
                 cudaEventRecord(st->ev_out[set], st->d2h) != cudaSuccess)
-                return SA_ERR_CUDA;
+                return fail(SA_ERR_CUDA);
         }
     }
     // the caller's stream completes once the last output copy has (the copies
@@ -702,10 +714,12 @@ extern "C" sa_status bigbird_attn_fwd_noalloc(const void *Q, const void *K, cons
     p.b = b; p.g = g; p.w = w; p.r = r;
     p.rand_idx = r > 0 ? rand_idx : nullptr;
     p.key_mask = key_mask;
-    // The scratch need depends only on the sizes and the split option: reject
-    // oversize calls before touching the device.
-    const sa::TcConfig size_cfg = tc_config(nullptr);
-    const size_t need = sa::tc_workspace_bytes(p, size_cfg);
+    // One configuration for the size check, the counter clear and the launch
+    // (the split option is read once). The scratch need depends only on the
+    // sizes and the split option, not on the grid size: reject oversize calls
+    // before touching the device.
+    sa::TcConfig cfg = tc_config(nullptr);
+    const size_t need = sa::tc_workspace_bytes(p, cfg);
     if (need > SA_NOALLOC_SCRATCH_BYTES) return SA_ERR_UNSUPPORTED;
 
     int dev = 0;
@@ -718,7 +732,7 @@ extern "C" sa_status bigbird_attn_fwd_noalloc(const void *Q, const void *K, cons
     s = noalloc_scratch(dev, &scratch);
     if (s != SA_OK) return s;
     p.status = st->status;
-    const sa::TcConfig cfg = tc_config(st);
+    if (g_grid_ctas.load() <= 0) cfg.grid_ctas = st->num_sms;  // grid size only: the scratch need is unchanged
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const size_t zero_bytes = sa::tc_workspace_counter_bytes(p, cfg);
     if (cudaMemsetAsync(scratch, 0, zero_bytes, cs) != cudaSuccess) return SA_ERR_CUDA;

@@ -65,6 +65,7 @@ cudaError_t launch_bigbird(const Problem &p, const TcConfig &cfg, void *ws, size
     uint8_t *base = static_cast<uint8_t *>(ws);
     prm.ws.counters = reinterpret_cast<unsigned *>(base);
     prm.ws.row_cnt = reinterpret_cast<unsigned *>(base + L.row_cnt);
+    prm.ws.n_row_cnt = (size_t)prm.geo.B * prm.geo.H * prm.geo.gtiles * kBM;
     prm.ws.part_o = L.part_o ? reinterpret_cast<float *>(base + L.part_o) : nullptr;
     prm.ws.part_ml = L.part_ml ? reinterpret_cast<float2 *>(base + L.part_ml) : nullptr;
     prm.rand_idx = p.rand_idx;

@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the resident tile copy was issued at start-up; with no steps (or on
         // abort) nothing else waits for it
-        if (total == 0 || !ok || *abort_flag) wait_drain(bar(C::B_TF), 0, p.wait_ns);
+        if (total == 0 || !ok || *abort_flag) wait_drain(bar(C::B_TF), 0);
     } else if (warp == 2 || warp == 3) {
         // ======================================================== chunk loaders
         // Warp 2 streams B1 (K or Q), warp 3 B2 (V or dO) and, in the key
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok || *abort_flag) {
             // drain our copies in flight before the CTA leaves
             for (int i = 0; i < C::NSTG; ++i)
-                if (arms[i]) wait_drain(bar(C::B_F + i), (arms[i] - 1) & 1, p.wait_ns);
+                if (arms[i]) wait_drain(bar(C::B_F + i), (arms[i] - 1) & 1);
         }
     } else if (warp == 1) {
         // ======================================================== MMA issuer
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(bar(C::B_DRAIN));
             }
             __syncwarp();
-            wait_drain(bar(C::B_DRAIN), 0, p.wait_ns);
+            wait_drain(bar(C::B_DRAIN), 0);
         }
         __syncwarp();
     } else if (warp >= 4) {

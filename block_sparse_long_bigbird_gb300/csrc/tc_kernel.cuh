@@ -123,7 +123,7 @@ struct Cfg {
     static constexpr int LIST_OFF = STEP_OFF + SI * 32;  // two lists: the next unit is decoded early
     static constexpr int SMALL = LIST_OFF + 2 * 32 * 4;
     static constexpr int SMALL_OFF = NT * BIG;
-    static constexpr int MISC_OFF = SMALL_OFF + NT * SMALL;  // TMEM address, abort flag
+    static constexpr int MISC_OFF = SMALL_OFF + NT * SMALL;  // TMEM address, abort flag, last-CTA flag
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
     static constexpr int ALLOC_BYTES = SMEM_BYTES + 1024;  // slack for 1024-B alignment
     // TMEM: each tile owns TILE_COLS columns: NS S slots of KB, then two O buffers of D
@@ -157,6 +157,7 @@ struct Geometry {
 struct Workspace {
     unsigned *counters;   // [0] next unit, [1] finished CTAs
     unsigned *row_cnt;    // [B*H*gtiles][128] arrivals per split row
+    size_t n_row_cnt;     // entries of row_cnt
     float *part_o;        // [B*H*gtiles][splits][128][D]
     float2 *part_ml;      // [B*H*gtiles][splits][128] (m, l)
 };
@@ -815,10 +816,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!ok && lane == 0) {  // abort: wait for the copies this tile still has in flight
             for (uint32_t i = 0; i < (uint32_t)C::KST && i < issued; ++i) {
                 const uint32_t arms = (issued - 1 - i) / C::KST + 1;  // copies into stage i
-                wait_drain(bar(C::B_KF + i), (arms - 1) & 1, G.wait_ns);
-                wait_drain(bar(C::B_VF + i), (arms - 1) & 1, G.wait_ns);
+                wait_drain(bar(C::B_KF + i), (arms - 1) & 1);
+                wait_drain(bar(C::B_VF + i), (arms - 1) & 1);
             }
-            if (qcnt && q_tma_last) wait_drain(bar(C::B_QF + (qcnt - 1) % C::NQ), ((qcnt - 1) / C::NQ) & 1, G.wait_ns);
+            if (qcnt && q_tma_last) wait_drain(bar(C::B_QF + (qcnt - 1) % C::NQ), ((qcnt - 1) / C::NQ) & 1);
         }
     } else if (role == 1) {
         // ================================================================ MMA issuer (tile x)
@@ -906,7 +907,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             // drain: every MMA issued by the leader has completed once this arrives
             if (leader) mma_commit(bar(C::B_DRAIN));
             __syncwarp();
-            wait_drain(bar(C::B_DRAIN), 0, G.wait_ns);
+            wait_drain(bar(C::B_DRAIN), 0);
         }
     } else if (role == 3 || role == 4) {
         // ================================================================ V (3) / K (4) loader
@@ -948,7 +949,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
         if (!ok && lane == 0)  // abort: wait for the copies still in flight
             for (int i = 0; i < C::KST; ++i)
-                if (arms[i]) wait_drain(bar(bf + i), (arms[i] - 1) & 1, G.wait_ns);
+                if (arms[i]) wait_drain(bar(bf + i), (arms[i] - 1) & 1);
     } else if (role == 2) {
         // ================================================================ softmax / epilogue (tile x)
         const int tid = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
@@ -1327,13 +1328,29 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(*tmem_holder, C::TMEM_COLS);
+    // The last CTA to finish resets the scheduler for the next call. Every
+    // other CTA has finished all its work (merges included) by then. After a
+    // timeout some split rows may not have been merged and their arrival
+    // counters are left non-zero: the last CTA zeroes them as well, so the
+    // next call starts from a clean scratch whether or not the caller has
+    // read the status word in between.
+    volatile int *last_flag = abort_flag + 1;
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned done = atomicAdd(p.ws.counters + 1, 1u);
-        if (done == gridDim.x - 1) {  // last CTA: reset the scheduler for the next call
-            atomicExch(p.ws.counters, 0u);
-            atomicExch(p.ws.counters + 1, 0u);
-        }
+        const bool last = done == gridDim.x - 1;
+        *last_flag = last ? 1 + ((atomicOr(p.status, 0u) & kDevTimeout) ? 1 : 0) : 0;
+    }
+    __syncthreads();
+    const int last = *last_flag;
+    if (last == 2) {
+        for (size_t i = threadIdx.x; i < p.ws.n_row_cnt; i += blockDim.x) p.ws.row_cnt[i] = 0u;
+        __threadfence();
+        __syncthreads();
+    }
+    if (last && threadIdx.x == 0) {
+        atomicExch(p.ws.counters, 0u);
+        atomicExch(p.ws.counters + 1, 0u);
     }
 }
 

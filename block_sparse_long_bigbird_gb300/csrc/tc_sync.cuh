@@ -26,13 +26,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-__device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -40,12 +40,14 @@ __device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity) {
 // Per-thread wait, bounded in time: returns false (and leaves) once the CTA
 // aborts. The first probe has no suspend hint (cheapest when the phase is
 // already complete); later probes sleep in the hardware until the phase
-// completes or the hint expires. No warp-collective operation inside, so
-// lanes of one warp may call it independently.
+// completes or the hint expires (the hint never exceeds the limit, so a short
+// limit takes effect within about one limit). No warp-collective operation
+// inside, so lanes of one warp may call it independently.
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Ctl &c) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = c.limit_ns < kSuspendNs ? (uint32_t)c.limit_ns : kSuspendNs;
     unsigned long long t0 = 0;
-    while (!try_wait_hint(bar, parity)) {
+    while (!try_wait_hint(bar, parity, hint)) {
         if (*c.abort) return false;
         const unsigned long long now = global_ns();
         if (t0 == 0) {
@@ -65,11 +67,16 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const C
     const bool ok = wait_one(bar, parity, c);
     return __all_sync(0xffffffffu, ok);
 }
-// Drain wait used on the abort path (ignores the abort flag, still bounded).
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+// Drain wait: before a CTA frees its TMEM and exits, it waits for its own
+// TMA copies and MMAs still in flight. It ignores the abort flag and has its
+// own limit, independent of the pipeline waits' limit (SA_OPT_WAIT_LIMIT may
+// be set very short): an asynchronous copy or MMA that was issued lands in
+// microseconds, so one second only ends a drain whose phase never completes.
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = global_ns();
     while (!ptx::mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > limit_ns) return;
+        if (global_ns() - t0 > kDrainLimitNs) return;
 }
 
 }  // namespace tcsync

@@ -13,7 +13,9 @@ Longformer paper Sec. 3 train on text that is out of scope here):
     generator seeded ``5000 + 10 * cfg``, cast like Q, K, V.
   * Key padding: per-sequence valid lengths ``L ~ U{n/2, ..., n}`` from a CPU
     generator seeded 2000; ``key_mask[beta, t] = t < L[beta]``.
-  * BigBird random table: drawn by ``build_bigbird_pattern`` from seed 0.
+  * BigBird random table: seed 0. The product draws it with
+    ``build_bigbird_pattern``; the oracle side draws its own from the same
+    spec, and the tests check that the two are bitwise equal.
 """
 
 import torch

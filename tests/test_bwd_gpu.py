@@ -11,7 +11,7 @@ import torch
 
 import block_sparse_long_bigbird_gb300 as sa
 from block_sparse_long_bigbird_gb300.inputs import make_grad_out, make_key_mask, make_qkv, make_random_key_mask
-from parity_util import PATHS, bigbird_bwd_case, gpu_bigbird_bwd, longformer_bwd_case
+from parity_util import PATHS, bigbird_bwd_case, gpu_bigbird_bwd, longformer_bwd_case, pattern_table
 
 pytestmark = pytest.mark.gpu
 
@@ -103,7 +103,7 @@ def test_bwd_is_deterministic(path):
     B, H, n, d = 2, 2, 1024, 64
     Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=72)
     dO = make_grad_out(B, H, n, d, "bf16", cfg_id=72)
-    table = sa.build_bigbird_pattern(0, H, n, 64, 2, 3, 3)
+    table = pattern_table(0, H, n, 64, 2, 3, 3)
     first = gpu_bigbird_bwd(Q, K, V, dO, 64, 2, 3, 3, table, path=path)
     second = gpu_bigbird_bwd(Q, K, V, dO, 64, 2, 3, 3, table, path=path)
     for a, b in zip(first, second):
@@ -115,7 +115,7 @@ def test_bwd_bad_random_entry_latches_status():
     B, H, n, d = 1, 1, 512, 64
     Q, K, V = (t.to(dev) for t in make_qkv(B, H, n, d, "bf16", cfg_id=73))
     dO = make_grad_out(B, H, n, d, "bf16", cfg_id=73).to(dev)
-    table = sa.build_bigbird_pattern(0, H, n, 64, 2, 3, 3)
+    table = pattern_table(0, H, n, 64, 2, 3, 3)
     O = sa.bigbird_attn_fwd(Q, K, V, 64, 2, 3, 3, table.to(dev))
     torch.cuda.synchronize()
     assert sa.get_last_device_status() == 0
@@ -172,7 +172,7 @@ def _sampled_bwd_check(wl_name, path, heads, kblocks, seed):
     dev = torch.device("cuda:0")
     Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, "bf16", sigma=wl.sigma, cfg_id=wl.cfg_id)
     dO = make_grad_out(wl.B, wl.H, wl.n, wl.d, "bf16", cfg_id=wl.cfg_id)
-    table = sa.build_bigbird_pattern(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+    table = pattern_table(wl.seed, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
     km = make_key_mask(wl.B, wl.n) if wl.padded else None
     set_path(path)
     try:

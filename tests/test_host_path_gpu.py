@@ -7,6 +7,7 @@ import torch
 
 import block_sparse_long_bigbird_gb300 as sa
 from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv
+from parity_util import pattern_table
 
 pytestmark = pytest.mark.gpu
 
@@ -17,7 +18,7 @@ def test_bigbird_host_path_matches_device_path(B, H, n, d, b, padded):
     dev = torch.device("cuda:0")
     g, w, r = 2, 3, 3
     Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=96)
-    table = sa.build_bigbird_pattern(0, H, n, b, g, w, r)
+    table = pattern_table(0, H, n, b, g, w, r)
     km = make_key_mask(B, n) if padded else None
     ref = sa.bigbird_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), b, g, w, r, table.to(dev),
                               None if km is None else km.to(dev)).cpu()
@@ -49,7 +50,7 @@ def test_host_path_fp32():
     dev = torch.device("cuda:0")
     B, H, n, d, b, g, w, r = 1, 2, 1024, 64, 64, 2, 3, 3
     Q, K, V = make_qkv(B, H, n, d, "fp32", cfg_id=98)
-    table = sa.build_bigbird_pattern(0, H, n, b, g, w, r)
+    table = pattern_table(0, H, n, b, g, w, r)
     ref = sa.bigbird_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), b, g, w, r, table.to(dev)).cpu()
     out = sa.bigbird_attn_fwd_host(Q.pin_memory(), K.pin_memory(), V.pin_memory(), b, g, w, r, table)
     torch.cuda.synchronize()

@@ -12,7 +12,7 @@ import torch
 import block_sparse_long_bigbird_gb300 as sa
 from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv, make_random_key_mask
 from block_sparse_long_bigbird_gb300.workloads import WORKLOADS
-from parity_util import (PATHS, bigbird_case, gpu_bigbird, longformer_case, sampled_bigbird_rows)
+from parity_util import (PATHS, bigbird_case, gpu_bigbird, longformer_case, pattern_table, sampled_bigbird_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -289,7 +289,7 @@ def test_bigbird_etc_n4352_workload(path):
     from parity_util import assert_close
     wl = WORKLOADS["bigbird_etc_bf16_n4352"]
     Q, K, V = make_qkv(wl.B, wl.H, wl.n, wl.d, "bf16", cfg_id=wl.cfg_id)
-    table = sa.build_bigbird_pattern(0, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+    table = pattern_table(0, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
     O = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path=path).float().cpu()
     rows = sampled_bigbird_rows(wl.n, wl.b, wl.g, seed=6)
     for beta, h in [(0, 0), (7, 11)]:
@@ -304,7 +304,7 @@ def test_bigbird_etc_n4352_workload(path):
 def test_bigbird_deterministic(path):
     wl = WORKLOADS["bigbird_bf16_n4096"]
     Q, K, V = make_qkv(2, wl.H, wl.n, wl.d, "bf16", cfg_id=wl.cfg_id)
-    table = sa.build_bigbird_pattern(0, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
+    table = pattern_table(0, wl.H, wl.n, wl.b, wl.g, wl.w, wl.r)
     O1 = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path=path)
     O2 = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path=path)
     assert torch.equal(O1, O2)
@@ -314,7 +314,7 @@ def test_bigbird_deterministic(path):
 def test_bad_random_index_latches_status(path):
     B, H, n, d, b, g, w, r = 1, 1, 512, 64, 64, 2, 3, 3
     Q, K, V = (t.cuda() for t in make_qkv(B, H, n, d, "bf16", cfg_id=70))
-    table = sa.build_bigbird_pattern(0, H, n, b, g, w, r)
+    table = pattern_table(0, H, n, b, g, w, r)
     table[0, 5, 1] = 1000  # out of [-1, nb): skipped by the kernel, latched as SA_ERR_BAD_INDEX
     sa.set_option(sa.SA_OPT_FORCE_SIMT, 1 if path == "simt" else 0)
     try:
@@ -340,7 +340,7 @@ def test_unsorted_global_index_latches_status(path):
 def test_tc_and_simt_agree_closely():
     wl = WORKLOADS["bigbird_bf16_n4096"]
     Q, K, V = make_qkv(1, 4, wl.n, wl.d, "bf16", cfg_id=72)
-    table = sa.build_bigbird_pattern(0, 4, wl.n, wl.b, wl.g, wl.w, wl.r)
+    table = pattern_table(0, 4, wl.n, wl.b, wl.g, wl.w, wl.r)
     a = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path="tc").float()
     b = gpu_bigbird(Q, K, V, wl.b, wl.g, wl.w, wl.r, table, path="simt").float()
     assert (a - b).abs().max().item() <= 2e-2
@@ -431,7 +431,7 @@ def test_bigbird_etc_via_block_kernel(path, g_tokens, b, n_reg):
                                x[:, :, g_tokens:]], dim=2).contiguous()
     km = torch.ones(B, padn, dtype=torch.uint8)
     km[:, g_tokens:gp] = 0
-    table = sa.build_bigbird_pattern(0, H, padn, b, gb, w, 0)
+    table = pattern_table(0, H, padn, b, gb, w, 0)
     O = gpu_bigbird(pad(Q), pad(K), pad(V), b, gb, w, 0, table, km, path).float().cpu()
     keep = np.concatenate([np.arange(g_tokens), np.arange(gp, padn)])
     ref = oracle_bigbird_etc(Q, K, V, g_tokens, b, w)

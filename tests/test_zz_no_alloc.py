@@ -8,7 +8,9 @@ tensor-core kernel with its scratch in a fixed array compiled into the
 library. These tests call it through the C ABI and compare it with
 bigbird_attn_fwd on the same inputs, twice in a row (the array keeps the
 previous call's contents, so the second call checks that the counters are
-cleared and reused correctly).
+cleared and reused correctly). Both entry points run the same deterministic
+kernel on the same inputs, so their outputs must be bitwise equal, which is
+stricter than the 2e-2 / 2e-3 tolerance against the oracle.
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test.
@@ -23,8 +25,7 @@ import torch
 import block_sparse_long_bigbird_gb300 as sa
 from block_sparse_long_bigbird_gb300 import _lib
 from block_sparse_long_bigbird_gb300.inputs import make_key_mask, make_qkv
-
-TOL_MAX, TOL_MEAN = 2e-2, 2e-3
+from parity_util import pattern_table
 
 
 def _noalloc(Q, K, V, O, b, g, w, r, table, key_mask):
@@ -51,7 +52,7 @@ def test_noalloc_matches_bigbird_attn_fwd(case):
     dev = torch.device("cuda:0")
     Qc, Kc, Vc = make_qkv(B, H, n, d, "bf16", cfg_id=80)
     Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
-    table = sa.build_bigbird_pattern(0, H, n, b, g, w, r).to(dev)
+    table = pattern_table(0, H, n, b, g, w, r).to(dev)
     km = make_key_mask(B, n, seed=11).to(dev) if padded else None
     need = sa.bigbird_workspace_bytes(B, H, n, d, b, g)
     assert 0 < need <= _lib.NOALLOC_SCRATCH_BYTES
@@ -59,17 +60,17 @@ def test_noalloc_matches_bigbird_attn_fwd(case):
     ref = sa.bigbird_attn_fwd(Q, K, V, b, g, w, r, table, km)
     torch.cuda.synchronize()
     assert sa.get_last_device_status() == 0
-    ref = ref.float()
     for call in range(2):
         O = torch.full_like(Q, float("nan"))
         st = _noalloc(Q, K, V, O, b, g, w, r, table, km)
         assert st == _lib.SA_OK, _lib.STATUS_NAMES.get(st, st)
         torch.cuda.synchronize()
         assert sa.get_last_device_status() == 0
-        err = (O.float() - ref).abs()
         assert torch.isfinite(O.float()).all(), f"call {call}: non-finite output"
-        assert err.max().item() <= TOL_MAX and err.mean().item() <= TOL_MEAN, \
-            f"call {call}: max {err.max().item():.3e} mean {err.mean().item():.3e}"
+        if not torch.equal(O, ref):
+            err = (O.float() - ref.float()).abs()
+            raise AssertionError(f"call {call}: differs from bigbird_attn_fwd "
+                                 f"(max {err.max().item():.3e}, mean {err.mean().item():.3e})")
         if km is not None:
             pad = (km == 0)[:, None, :, None].expand_as(O)
             assert (O[pad] == 0).all(), "padded query rows must be exactly 0"
