@@ -241,6 +241,14 @@ def get_last_device_status(stream=None, device=None):
     return _lib.lib().sa_get_last_device_status(_stream_handle(stream, dev))
 
 
+def check_wait_expiry(limit_us, stream=None, device=None):
+    """Launch the failure-detection self-check: a bounded wait on a barrier that
+    nothing arrives at, which must latch SA_ERR_TIMEOUT (read it with
+    get_last_device_status)."""
+    dev = device if device is not None else torch.cuda.current_device()
+    _lib.check(_lib.lib().sa_check_wait_expiry(int(limit_us), _stream_handle(stream, dev)), "sa_check_wait_expiry")
+
+
 def set_option(option, value):
     _lib.check(_lib.lib().sa_set_option(option, int(value)), "sa_set_option")
 

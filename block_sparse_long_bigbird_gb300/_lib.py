@@ -57,6 +57,7 @@ SIGNATURES = {
     "sa_set_option": (_I, [_I, ctypes.c_int64]),
     "sa_last_launch_count": (_I, []),
     "bigbird_attn_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP]),
+    "sa_check_wait_expiry": (_I, [ctypes.c_int64, _VP]),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
 

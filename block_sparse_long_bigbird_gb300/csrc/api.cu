@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "tc_sync.cuh"
 
 namespace {
 
@@ -741,5 +742,46 @@ extern "C" sa_status bigbird_attn_fwd_noalloc(const void *Q, const void *K, cons
     if (e == cudaErrorNotSupported) return SA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return SA_ERR_CUDA;
     g_last_launches = launches;
+    return SA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// sa_check_wait_expiry: the bounded-wait machinery of the tensor-core kernels,
+// exercised without a fault. One warp waits, through the kernels' own wait
+// helper, on an mbarrier that nothing ever arrives at; the wait gives up after
+// the limit, raises the CTA's abort flag and latches SA_ERR_TIMEOUT in the
+// device status word, and the kernel returns.
+namespace {
+
+__global__ void __launch_bounds__(32, 1) wait_expiry_kernel(unsigned *status, unsigned long long limit_ns) {
+    using namespace sa::tcsync;
+    __shared__ __align__(8) uint64_t never;  // phase 0 never completes: its one arrival never comes
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        sa::ptx::mbar_init(sa::ptx::smem_u32(&never), 1);
+        abort_flag = 0;
+        sa::ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    const Ctl ctl{&abort_flag, status, limit_ns};
+    wait_warp(sa::ptx::smem_u32(&never), 0, ctl);
+}
+
+}  // namespace
+
+extern "C" sa_status sa_check_wait_expiry(int64_t limit_us, sa_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return SA_ERR_INVALID_ARG;
+    int dev = 0;
+    DeviceState *st = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        const sa_status s = current_device(&dev, &st);
+        if (s != SA_OK) return s;
+        if (st->cc_major != 10 || st->cc_minor != 3) return SA_ERR_UNSUPPORTED;
+    }
+    wait_expiry_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        st->status, (unsigned long long)limit_us * 1000ull);
+    if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
+    g_last_launches = 1;
     return SA_OK;
 }

@@ -45,8 +45,11 @@ __device__ __forceinline__ bool try_wait_hint(uint32_t bar, uint32_t parity, uin
 // inside, so lanes of one warp may call it independently.
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Ctl &c) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint32_t hint = c.limit_ns < kSuspendNs ? (uint32_t)c.limit_ns : kSuspendNs;
-    unsigned long long t0 = 0;
+    const bool short_limit = c.limit_ns < kSuspendNs;
+    const uint32_t hint = short_limit ? (uint32_t)c.limit_ns : kSuspendNs;
+    // With the default limit the clock starts at the first hinted miss (no
+    // timer read on the common path); a short limit starts it now.
+    unsigned long long t0 = short_limit ? global_ns() : 0;
     while (!try_wait_hint(bar, parity, hint)) {
         if (*c.abort) return false;
         const unsigned long long now = global_ns();

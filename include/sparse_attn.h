@@ -379,6 +379,21 @@ sa_status sa_set_option(int option, int64_t value);
 int sa_last_launch_count(void);
 
 /*
+ * sa_check_wait_expiry - self-check of failure detection on the current
+ * device, without a fault. It launches one warp that waits, through the same
+ * bounded-wait helper every tensor-core kernel uses, on a barrier that nothing
+ * ever arrives at. After `limit_us` microseconds (1 .. 1000000) the wait gives
+ * up and latches SA_ERR_TIMEOUT in the device status word, exactly as an
+ * expired pipeline wait would, and the kernel returns: the next
+ * sa_get_last_device_status() on `stream` must report SA_ERR_TIMEOUT, and the
+ * context stays usable. (The pages have no counterpart: this checks the
+ * library's boundary contract for deferred device errors.)
+ * Errors: SA_ERR_INVALID_ARG for a limit out of range; SA_ERR_UNSUPPORTED
+ * without an sm_103a device; SA_ERR_CUDA if the launch fails.
+ */
+sa_status sa_check_wait_expiry(int64_t limit_us, sa_stream_t stream);
+
+/*
  * bigbird_attn_fwd_noalloc - bigbird_attn_fwd for callers that must not
  * allocate device memory. (The pages have no counterpart: this is a
  * deployment variant of the same computation.)

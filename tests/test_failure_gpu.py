@@ -1,6 +1,8 @@
 """Failure detection and the scratch-sharing contract, on the GPU, without a
-fault: a pipeline wait is made to run out by a very short time limit, and the
-kernel must end with SA_ERR_TIMEOUT latched and the context usable.
+fault: a wait is made to run out (a barrier nothing arrives at, through the
+kernels' own bounded-wait helper; and a very short pipeline limit on a real
+call), and the device must end with SA_ERR_TIMEOUT latched, or nothing
+latched, and a usable context whose next call is exact.
 
 The pages define no such path; it belongs to the library's boundary (bounded
 waits, a latched device status word, scratch shared by the calls of a device).
@@ -61,26 +63,28 @@ def test_wait_limit_expiry_is_clean_and_the_next_call_is_exact():
 
 
 @pytest.mark.gpu
-def test_wait_limit_expiry_reports_timeout():
-    # A 1-microsecond limit on the n = 4096 workload: some wait (a copy from
-    # HBM, a unit hand-over) takes longer, so the call must report a timeout.
-    B, H, n, d, b, g, w, r = 8, 12, 4096, 64, 64, 2, 3, 3
-    dev = torch.device("cuda:0")
-    Q, K, V = (t.to(dev) for t in make_qkv(B, H, n, d, "bf16", cfg_id=121))
-    tab = pattern_table(0, H, n, b, g, w, r).to(dev)
+def test_expired_wait_latches_timeout_and_the_context_stays_usable():
+    # The self-check waits, through the kernels' own bounded-wait helper, on a
+    # barrier that nothing arrives at: the wait must give up and latch
+    # SA_ERR_TIMEOUT, and an ordinary call afterwards must be exact.
     assert sa.get_last_device_status() == 0
-    sa.set_option(sa.SA_OPT_WAIT_LIMIT, 1)
-    try:
-        sa.bigbird_attn_fwd(Q, K, V, b, g, w, r, tab)
-        torch.cuda.synchronize()
-    finally:
-        sa.set_option(sa.SA_OPT_WAIT_LIMIT, 0)
+    sa.check_wait_expiry(2000)  # 2 ms
     assert sa.get_last_device_status() == _lib.SA_ERR_TIMEOUT
-    ref = sa.bigbird_attn_fwd(Q, K, V, b, g, w, r, tab)
-    again = sa.bigbird_attn_fwd(Q, K, V, b, g, w, r, tab)
+    assert sa.get_last_device_status() == 0  # reading clears it
+    B, H, n, d, b, g, w, r = 2, 2, 2048, 64, 64, 2, 3, 3
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=122)
+    table = pattern_table(0, H, n, b, g, w, r)
+    dev = torch.device("cuda:0")
+    O = sa.bigbird_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), b, g, w, r, table.to(dev))
     torch.cuda.synchronize()
     assert sa.get_last_device_status() == 0
-    assert torch.equal(ref, again)
+    _check_rows(O, Q, K, V, b, g, w, table, None, [(0, 0), (1, 1)], np.arange(n))
+
+
+def test_wait_expiry_self_check_rejects_bad_limits():
+    lib = _lib.lib()
+    assert lib.sa_check_wait_expiry(0, None) == _lib.SA_ERR_INVALID_ARG
+    assert lib.sa_check_wait_expiry(2000001, None) == _lib.SA_ERR_INVALID_ARG
 
 
 @pytest.mark.gpu
