@@ -966,7 +966,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             float m, l;
             uint32_t ob, g_last;
         };
-        Pend pe;
+        Pend pe = {};  // every field defined: the epilogue reads them all
         pe.kind = kUnitEnd;
 
         // `wait_pv` false: the caller already saw PV of step g_last complete.
@@ -1110,7 +1110,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 lpat = 1ull;  // bits 0, s, 2s, ...: doubled until the word is full
                 for (int sh = lstride; sh < 64; sh *= 2) lpat |= lpat << sh;
             }
-            Pend cur;
+            Pend cur = {};
             cur.kind = ui.kind;
             cur.bh = ui.bh;
             cur.row = srow;
