@@ -7,7 +7,7 @@ b=64, g=2, w=3, r=3, bf16). The `*_bwd_*` workloads time one
 `bigbird_attn_bwd` / `longformer_attn_bwd` call instead (10*d useful FLOPs
 per attended pair). Prints one JSON line on rank 0.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference|blockified]
 
 Metric: useful TFLOP/s = 4*d * attended (valid query, allowed valid key)
 pairs / time. Inputs are resident in HBM before the timed region; L2 is
@@ -17,6 +17,10 @@ flushed (256 MiB write) between timed steps, outside the timed events.
 every host->device copy of Q, K, V (and the tables) and the device->host copy
 of O is inside the timed region; the library pipelines them against the
 computation chunk by chunk. `--impl reference` times the float64 CPU oracle instead.
+`--impl blockified` times the pages' own dense-operation formulation in plain
+PyTorch on the same GPU (``baselines/blockified.py``: BigBird App. D Eq. (13),
+Longformer App. A chunks) on the same inputs and work count; the default line
+also carries that baseline's time in `blockified_baseline`.
 Multi-GPU (torchrun): every rank runs its own batch of B sequences drawn
 from its own seeds, so the global batch is world x B (weak scaling, no
 collective on the data path); the step time is the max over ranks.
@@ -55,10 +59,11 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "blockified"])
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-blockified", action="store_true", help="skip the dense-formulation baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline time budget")
     return ap.parse_args(argv)
 
@@ -354,6 +359,105 @@ def run_reference(args):
     return 0
 
 
+def blockified_unsupported(wl):
+    """Why the dense-formulation baseline cannot run `wl`, or None."""
+    if wl.grad:
+        return "the pages give the dense formulation for the forward only"
+    if wl.kind == "longformer" and (wl.dilation and any(wl.dilation)):
+        return "the chunks formulation (Longformer App. A) supports only the non-dilated window"
+    if wl.gproj:
+        return "the chunks formulation has no separate global projections"
+    return None
+
+
+def blockified_call(wl, dev_t):
+    from baselines.blockified import bigbird_blockified, longformer_chunks
+
+    if wl.kind == "bigbird":
+        return bigbird_blockified(dev_t["Q"], dev_t["K"], dev_t["V"], wl.b, wl.g, wl.w, wl.r, dev_t.get("table"),
+                                  dev_t.get("key_mask"))
+    return longformer_chunks(dev_t["Q"], dev_t["K"], dev_t["V"], wl.window, dev_t["gidx"], dev_t.get("key_mask"),
+                             causal=wl.causal)
+
+
+def time_blockified(wl, dev_t, flush, stream, steps, warmup):
+    """CUDA-event time of the dense-formulation baseline, same protocol as the
+    library's timed steps (L2 flushed between steps, outside the events)."""
+    import torch
+
+    for _ in range(max(3, warmup)):
+        blockified_call(wl, dev_t)
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        blockified_call(wl, dev_t)
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms.append(s.elapsed_time(e))
+    return ms
+
+
+def run_blockified(args):
+    """The pages' dense formulation on this GPU, as its own bench line."""
+    import torch
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    wl = WORKLOADS[args.workload]
+    why = blockified_unsupported(wl)
+    if why:
+        print(json.dumps({"impl": "blockified", "unavailable": why}), flush=True)
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    prob = make_problem(wl)
+    dev_t = {k: v.to(dev) for k, v in prob.items() if hasattr(v, "to") and v is not None}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    with ClockSampler(local) as clocks:
+        ms = time_blockified(wl, dev_t, flush, stream, args.steps, args.warmup)
+    t = sum(ms) / len(ms)
+    # end to end: pinned host inputs copied in, the dense formulation, the output copied back
+    ins = [k for k in ("Q", "K", "V", "table", "gidx", "key_mask") if prob.get(k) is not None]
+    host = {k: prob[k].pin_memory() for k in ins}
+    O = blockified_call(wl, dev_t)
+    out_h = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    e_ms = []
+    for i in range(max(2, args.warmup) + args.steps):
+        flush.fill_(i & 0xFF)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for k in ins:
+            dev_t[k].copy_(host[k], non_blocking=True)
+        out_h.copy_(blockified_call(wl, dev_t), non_blocking=True)
+        e.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= max(2, args.warmup):
+            e_ms.append(s.elapsed_time(e))
+    e_t = sum(e_ms) / len(e_ms)
+    peaks, peak_src = read_peaks()
+    value = prob["flops"] / (t * 1e-3) / 1e12
+    line = {
+        "impl": "blockified", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded torch.randn inputs, pattern seed 0)", "config": workload_config(wl),
+        "frac_of_bf16_peak": value / peaks["bf16_tflops"],
+        "e2e": {"value": prob["flops"] / (e_t * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_t,
+                "h2d_bytes_per_step": sum(host[k].numel() * host[k].element_size() for k in ins),
+                "d2h_bytes_per_step": out_h.numel() * out_h.element_size()},
+        "clocks": clocks.summary(), "per_step_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
+        "note": "plain PyTorch dense operations (cuBLAS batched products, fp32 softmax); useful FLOPs as for "
+                "the library: 4*d per attended pair",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(wl):
     cfg = {"workload": f"{wl.name}: {wl.kind}{' backward' if wl.grad else ''} B={wl.B} H={wl.H} n={wl.n} d={wl.d}",
            "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "dtype": wl.dtype,
@@ -377,6 +481,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.impl == "blockified":
+        return run_blockified(args)
 
     import torch
 
@@ -525,6 +631,22 @@ def main(argv=None):
                "api": "device call with stream-ordered copies" if (wl.grad or wl.gproj)
                else f"{wl.kind}_attn_fwd_host (host buffers, copies pipelined in the library)"}
 
+    blk = None
+    if rank == 0 and world == 1 and not args.no_blockified:
+        why = blockified_unsupported(wl)
+        if why:
+            blk = {"unavailable": why}
+        else:
+            try:
+                b_ms = time_blockified(wl, dev_t, flush, stream, args.steps, args.warmup)
+                b_t = sum(b_ms) / len(b_ms)
+                blk = {"value": prob["flops"] / (b_t * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": b_t,
+                       "what": "the pages' dense formulation in plain PyTorch on this GPU, same inputs "
+                               "(baselines/blockified.py)"}
+            except torch.cuda.OutOfMemoryError as exc:
+                blk = {"unavailable": f"out of memory: {str(exc).splitlines()[0]}"}
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(wl, prob, args.cpu_seconds)
@@ -539,7 +661,7 @@ def main(argv=None):
             "tokens_per_s": agg["tokens_per_s"],
             "useful_gflop_per_step": prob["flops"] / 1e9,
             "frac_of_bf16_peak": agg["tflops"] / world / peaks["bf16_tflops"],
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "blockified_baseline": blk,
             "gpu_launches": launches, "clocks": clocks.summary(),
             "per_step_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
         }
