@@ -14,6 +14,7 @@ from . import _lib
 from ._lib import (  # noqa: F401
     SA_BF16,
     SA_FP32,
+    SA_OPT_CHUNK_KEYS,
     SA_OPT_FORCE_SIMT,
     SA_OPT_GRID_CTAS,
     SA_OPT_MAX_SPLITS,

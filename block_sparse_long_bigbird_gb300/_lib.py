@@ -30,6 +30,7 @@ SA_OPT_FORCE_SIMT = 1
 SA_OPT_WAIT_LIMIT = 2
 SA_OPT_MAX_SPLITS = 3
 SA_OPT_GRID_CTAS = 4
+SA_OPT_CHUNK_KEYS = 5
 
 # Exported symbol -> (restype, argtypes).
 _VP = ctypes.c_void_p

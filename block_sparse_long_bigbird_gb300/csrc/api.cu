@@ -45,6 +45,7 @@ std::atomic<int> g_force_simt{0};
 std::atomic<long long> g_wait_limit{2000000};  // microseconds
 std::atomic<int> g_max_splits{16};
 std::atomic<int> g_grid_ctas{0};
+std::atomic<int> g_chunk_keys{0};
 thread_local int g_last_launches = 0;
 
 sa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
@@ -111,6 +112,7 @@ sa::TcConfig tc_config(const DeviceState *st) {
     const int grid = g_grid_ctas.load();
     cfg.grid_ctas = grid > 0 ? grid : (st ? st->num_sms : 148);
     cfg.max_splits = g_max_splits.load();
+    cfg.chunk_keys = g_chunk_keys.load();
     cfg.wait_limit = g_wait_limit.load();
     return cfg;
 }
@@ -667,6 +669,7 @@ sa_status sa_set_option(int option, int64_t value) {
         case SA_OPT_WAIT_LIMIT: g_wait_limit = value > 0 ? (long long)value : 2000000; return SA_OK;
         case SA_OPT_MAX_SPLITS: g_max_splits = value < 1 ? 1 : (value > 64 ? 64 : (int)value); return SA_OK;
         case SA_OPT_GRID_CTAS: g_grid_ctas = value < 0 ? 0 : (int)value; return SA_OK;
+        case SA_OPT_CHUNK_KEYS: g_chunk_keys = value <= 0 ? 0 : (value > (1 << 20) ? (1 << 20) : (int)value); return SA_OK;
     }
     return SA_ERR_INVALID_ARG;
 }

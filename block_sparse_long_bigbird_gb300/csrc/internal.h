@@ -66,6 +66,7 @@ cudaError_t launch_simt_bwd(const Problem &p, sa_dtype dtype, cudaStream_t strea
 struct TcConfig {
     int grid_ctas;     // persistent grid size
     int max_splits;    // split-KV upper bound for global row tiles
+    int chunk_keys;    // split-KV target keys per chunk (0: the kernel's default)
     long long wait_limit;
 };
 // Tensor-core backward (bf16): row pass then key pass, two launches.

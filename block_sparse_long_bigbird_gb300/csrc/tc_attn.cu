@@ -19,13 +19,18 @@ Geometry bigbird_geometry(const Problem &p, const TcConfig &cfg) {
     G.tiles = (p.n + kBM - 1) / kBM;
     G.gtiles = (p.g * p.b + kBM - 1) / kBM;
     if (G.gtiles > G.tiles) G.gtiles = G.tiles;
-    const int kb = keys_per_step(p.d), target_steps = kTargetChunkKeys / kb;
+    const int kb = keys_per_step(p.d);
     G.steps_full = (p.n + kb - 1) / kb;
-    int s0 = (G.steps_full + target_steps - 1) / target_steps;
-    if (s0 > cfg.max_splits) s0 = cfg.max_splits;
-    if (s0 < 1) s0 = 1;
-    G.steps_per_chunk = (G.steps_full + s0 - 1) / s0;
-    G.splits = (G.steps_full + G.steps_per_chunk - 1) / G.steps_per_chunk;
+    {
+        // a local tile walks the union of its query blocks' lists
+        const int qb = kBM / p.b > 1 ? kBM / p.b : 1;
+        long long blocks = (long long)p.g + (p.w - 1 + qb) + (long long)qb * p.r;
+        if (blocks > G.nb) blocks = G.nb;
+        const long long per_tile = (blocks * p.b + kb - 1) / kb;
+        const int nt = p.d == 64 ? Cfg<64>::NT : Cfg<128>::NT;
+        choose_splits(G, (long long)p.B * p.H * (G.tiles - G.gtiles) * per_tile, kb, nt, cfg.chunk_keys,
+                      cfg.max_splits);
+    }
     const long long BH = (long long)p.B * p.H;
     G.n_split_units = (int)(BH * G.gtiles * G.splits);
     G.total_units = G.n_split_units + (int)(BH * (G.tiles - G.gtiles));

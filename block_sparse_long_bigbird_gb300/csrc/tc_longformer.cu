@@ -77,13 +77,16 @@ Geometry longformer_geometry(const Problem &p, const TcConfig &cfg) {
     G.causal = p.causal;
     G.gtiles = (p.n_global + kBM - 1) / kBM;
     G.nkb = (p.n + 63) / 64;
-    const int kb = keys_per_step(p.d), target_steps = kTargetChunkKeys / kb;
+    const int kb = keys_per_step(p.d);
     G.steps_full = (p.n + kb - 1) / kb;
-    int s0 = (G.steps_full + target_steps - 1) / target_steps;
-    if (s0 > cfg.max_splits) s0 = cfg.max_splits;
-    if (s0 < 1) s0 = 1;
-    G.steps_per_chunk = (G.steps_full + s0 - 1) / s0;
-    G.splits = (G.steps_full + G.steps_per_chunk - 1) / G.steps_per_chunk;
+    {
+        // a band tile: its window around 128 rows, plus a step of global keys
+        long long keys = 2LL * G.half + kBM;
+        if (keys > p.n) keys = p.n;
+        const long long per_tile = (keys + kb - 1) / kb + (p.n_global > 0 ? 1 : 0);
+        const int nt = p.d == 64 ? Cfg<64>::NT : Cfg<128>::NT;
+        choose_splits(G, (long long)p.B * p.H * G.tiles * per_tile, kb, nt, cfg.chunk_keys, cfg.max_splits);
+    }
     const long long BH = (long long)p.B * p.H;
     G.n_split_units = (int)(BH * G.gtiles * G.splits);
     G.total_units = G.n_split_units + (int)(BH * G.tiles);

@@ -369,9 +369,17 @@ const char *sa_status_string(sa_status status);
  *  SA_OPT_MAX_SPLITS   upper bound on split-KV chunks per global row tile
  *                      (default 16, 1 disables splitting).
  *  SA_OPT_GRID_CTAS    persistent-grid size (0 = one CTA per SM).
+ *  SA_OPT_CHUNK_KEYS   keys per split-KV chunk of a global row tile, before
+ *                      the SA_OPT_MAX_SPLITS bound (value <= 0: the default,
+ *                      described in the kernel notes; at most 2^20). Shorter
+ *                      chunks shorten the longest unit of a call (a global
+ *                      row sweeps every key) at the cost of more partial
+ *                      results to merge. The output does not depend on it
+ *                      beyond rounding order.
  * Returns SA_ERR_INVALID_ARG for an unknown option.
  */
-enum { SA_OPT_FORCE_SIMT = 1, SA_OPT_WAIT_LIMIT = 2, SA_OPT_MAX_SPLITS = 3, SA_OPT_GRID_CTAS = 4 };
+enum { SA_OPT_FORCE_SIMT = 1, SA_OPT_WAIT_LIMIT = 2, SA_OPT_MAX_SPLITS = 3, SA_OPT_GRID_CTAS = 4,
+       SA_OPT_CHUNK_KEYS = 5 };
 sa_status sa_set_option(int option, int64_t value);
 
 /* Number of kernel launches issued by the calling thread's last successful

@@ -156,8 +156,8 @@ def test_longformer_every_token_global(path):
 
 @pytest.mark.parametrize("path", PATHS)
 def test_longformer_split_global_rows(path):
-    # 12288 keys = 96 steps of 128: the global rows sweep in two split-KV chunks;
-    # 131 global rows span two global tiles
+    # 12288 keys: the global rows sweep in split-KV chunks (2 heads leave most
+    # SMs idle, so the chunks are short); 131 global rows span two global tiles
     from block_sparse_long_bigbird_gb300.inputs import make_global_positions
 
     n = 12288
@@ -459,3 +459,29 @@ def test_longformer_gproj_n4096_workload(path):
     rows = np.concatenate([np.arange(0, 200), np.arange(2000, 2100), np.arange(wl.n - 100, wl.n)])
     _gproj_case(wl.B, wl.H, wl.n, wl.d, wl.window, torch.arange(wl.n_global, dtype=torch.int32), path,
                 rows=rows, heads=[(0, 0), (3, 11)], cfg_id=wl.cfg_id)
+
+
+@pytest.mark.parametrize("chunk_keys,max_splits", [(0, 1), (512, 64), (2048, 16), (1 << 20, 16)])
+def test_split_options_keep_the_result(chunk_keys, max_splits):
+    # The split-KV chunking of the global tiles changes only the order in which
+    # partial results are summed: every setting must match the oracle, the
+    # global rows must stay within rounding of the default setting's, and the
+    # local tiles must not change at all.
+    B, H, n, d, b, g, w, r = 1, 2, 16384, 64, 64, 2, 3, 3
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=140)
+    table = pattern_table(0, H, n, b, g, w, r)
+    km = make_key_mask(B, n, seed=23)
+    base = gpu_bigbird(Q, K, V, b, g, w, r, table, km).float()
+    sa.set_option(sa.SA_OPT_CHUNK_KEYS, chunk_keys)
+    sa.set_option(sa.SA_OPT_MAX_SPLITS, max_splits)
+    try:
+        rows = sampled_bigbird_rows(n, b, g, n_random_blocks=3, seed=9)
+        bigbird_case(B, H, n, d, b, g, w, r, cfg_id=140, key_mask=km, rows=rows, heads=[(0, 1)])
+        O = gpu_bigbird(Q, K, V, b, g, w, r, table, km).float()
+        longformer_case(1, 2, 12288, 64, 256, torch.arange(40, dtype=torch.int32), cfg_id=141,
+                        rows=np.concatenate([np.arange(40), np.arange(5000, 5100)]))
+    finally:
+        sa.set_option(sa.SA_OPT_CHUNK_KEYS, 0)
+        sa.set_option(sa.SA_OPT_MAX_SPLITS, 16)
+    assert (O - base).abs().max().item() <= 2e-2
+    assert torch.equal(O[:, :, g * b:], base[:, :, g * b:])

@@ -39,7 +39,7 @@ def _noalloc(Q, K, V, O, b, g, w, r, table, key_mask):
 CASES = [
     # B, H, n,     d,   b,   padded
     (2, 4, 4096, 64, 64, False),    # one unit per tile, scheduler counters only
-    (1, 2, 16384, 64, 64, True),    # global tiles split in two: partials + merge counters
+    (1, 2, 16384, 64, 64, True),    # global tiles split into chunks: partials + merge counters
     (1, 2, 16384, 128, 128, False),  # d = 128, split global tiles
 ]
 
@@ -77,14 +77,15 @@ def test_noalloc_matches_bigbird_attn_fwd(case):
 
 
 def test_noalloc_rejects_oversize_before_touching_the_device():
-    # 8 x 16 heads of n = 65536, d = 128 need ~137 MB of split partials, far
-    # beyond the fixed array. The check runs on the host before any CUDA call,
-    # so the (never dereferenced) pointers below are safe even without a GPU.
+    # 2 heads of n = 65536, d = 128 with 64 global blocks: 128 global tiles
+    # whose sweeps are cut into split-KV chunks, tens of MB of partials, beyond
+    # the fixed array. The check runs on the host before any CUDA call, so the
+    # (never dereferenced) pointers below are safe even without a GPU.
     fake = 0x7f0000000000
     lib = _lib.lib()
-    need = lib.sa_bigbird_workspace_bytes(8, 16, 65536, 128, 128, 2)
+    need = lib.sa_bigbird_workspace_bytes(1, 2, 65536, 128, 128, 64)
     assert need > _lib.NOALLOC_SCRATCH_BYTES
     st = lib.bigbird_attn_fwd_noalloc(fake, fake + 0x1000000, fake + 0x2000000, fake + 0x3000000,
-                                      8, 16, 65536, 128, 128, 2, 3, 3, fake + 0x4000000, None, None)
+                                      1, 2, 65536, 128, 128, 64, 3, 3, fake + 0x4000000, None, None)
     assert st == _lib.SA_ERR_UNSUPPORTED
     assert np.isfinite(need)
