@@ -121,7 +121,12 @@ struct Cfg {
     static constexpr int UNIT_OFF = (B_COUNT * 8 + 15) & ~15;
     static constexpr int STEP_OFF = UNIT_OFF + kNU * 64;
     static constexpr int LIST_OFF = STEP_OFF + SI * 32;  // two lists: the next unit is decoded early
-    static constexpr int SMALL = LIST_OFF + 2 * 32 * 4;
+    // key-validity bits of each list entry (two 64-key words; with a key mask),
+    // kept for d = 64 only (d = 128 has no shared memory left for them and
+    // reads the key mask per step)
+    static constexpr bool KBITS = (D == 64);
+    static constexpr int KBITS_OFF = LIST_OFF + 2 * 32 * 4;
+    static constexpr int SMALL = KBITS_OFF + (KBITS ? 2 * 32 * 16 : 0);
     static constexpr int SMALL_OFF = NT * BIG;
     static constexpr int MISC_OFF = SMALL_OFF + NT * SMALL;  // TMEM address, abort flag, last-CTA flag
     static constexpr int SMEM_BYTES = MISC_OFF + 16;
@@ -264,6 +269,24 @@ __device__ __forceinline__ bool block_has_valid_lane(const uint8_t *km, int kb, 
     return any != 0;
 }
 
+// Validity bits of the keys of block kb (per lane, 16-byte loads): bit i of
+// word h is key kb * b + 64 h + i. Blocks lie inside [0, n) (n is a multiple
+// of b), so no bound check is needed.
+__device__ __forceinline__ void block_key_bits_lane(const uint8_t *km, int kb, int b, uint64_t (&bits)[2]) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(km + (size_t)kb * b);
+    bits[0] = bits[1] = 0ull;
+    for (int i = 0; i < b / 16; ++i) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m |= (((w[k] >> (8 * j)) & 0xFFu) != 0u ? 1u : 0u) << (4 * k + j);
+        bits[i >> 2] |= (uint64_t)m << (16 * (i & 3));
+    }
+}
+
 // Any valid key in block kb (warp-uniform answer).
 __device__ __forceinline__ bool block_has_valid_warp(const uint8_t *km, int kb, int b) {
     const int lane = threadIdx.x & 31;
@@ -289,9 +312,12 @@ __device__ __forceinline__ uint64_t key_bits64(const uint8_t *km, int k0, int n)
 // random block), duplicates and padded blocks drop out, and each survivor's
 // rank among the survivors is its position. list[pos] = block | allow bits
 // (bit 30: query block j0 sees it, bit 31: j1 sees it). Returns the number of
-// blocks, or -1 when the candidates do not fit in one warp.
+// blocks, or -1 when the candidates do not fit in one warp. With a key mask,
+// kbits[2 pos + h] receives the validity bits of the entry's keys (word h),
+// so the per-step records need no global loads.
 __device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1, const int32_t *r0,
-                                                const int32_t *r1, const uint8_t *km, uint32_t *list) {
+                                                const int32_t *r1, const uint8_t *km, uint32_t *list,
+                                                uint64_t *kbits) {
     const Geometry &G = p.geo;
     const int lane = threadIdx.x & 31;
     const int nglob = min(G.g, G.nb);
@@ -320,7 +346,11 @@ __device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1,
     const bool in_r0 = (__ballot_sync(kFull, src == 3) & same) != 0;
     const bool in_r1 = (__ballot_sync(kFull, src == 4) & same) != 0;
     bool valid = v < G.nb && (same & ((1u << lane) - 1u)) == 0;  // first lane holding this block
-    if (valid && km) valid = block_has_valid_lane(km, v, G.b);
+    uint64_t kb2[2] = {~0ull, ~0ull};
+    if (valid && km) {
+        block_key_bits_lane(km, v, G.b, kb2);
+        valid = (kb2[0] | kb2[1]) != 0ull;
+    }
     const bool a0 = valid && (j0 < G.g || v < G.g || abs(v - j0) <= G.half || in_r0);
     const bool a1 = valid && j1 >= 0 && (j1 < G.g || v < G.g || abs(v - j1) <= G.half || in_r1);
     const unsigned vm = __ballot_sync(kFull, valid);
@@ -343,7 +373,13 @@ __device__ __forceinline__ int build_local_list(const Params &p, int j0, int j1,
     }
     // survivors that no query half sees (possible only with a key mask) go last
     if (!a0 && !a1) pos = nboth + n0 + n1 + __popc(vm & ~(m_both | m_0 | m_1) & below);
-    if (valid) list[pos] = (uint32_t)v | (a0 ? (1u << 30) : 0u) | (a1 ? (1u << 31) : 0u);
+    if (valid) {
+        list[pos] = (uint32_t)v | (a0 ? (1u << 30) : 0u) | (a1 ? (1u << 31) : 0u);
+        if (km && kbits) {
+            kbits[2 * pos] = kb2[0];
+            kbits[2 * pos + 1] = kb2[1];
+        }
+    }
     __syncwarp();
     return __popc(vm);
 }
@@ -479,6 +515,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     UnitInfo *ring = reinterpret_cast<UnitInfo *>(small + C::UNIT_OFF);
     StepInfo *steps = reinterpret_cast<StepInfo *>(small + C::STEP_OFF);
     uint32_t *list = reinterpret_cast<uint32_t *>(small + C::LIST_OFF);
+    uint64_t *kbits = C::KBITS ? reinterpret_cast<uint64_t *>(small + C::KBITS_OFF) : nullptr;  // [2][32][2]
     const uint32_t tmem = *tmem_holder + x * C::TILE_COLS;  // this tile's TMEM columns
 
     if (role == 0) {
@@ -604,7 +641,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 }
                 int nlist = 0;
                 if (any_row) {
-                    nlist = build_local_list(p, ui.j0, ui.j1, up.r0, up.r1, up.km, lbuf);
+                    nlist = build_local_list(p, ui.j0, ui.j1, up.r0, up.r1, up.km, lbuf,
+                                             C::KBITS ? kbits + (lbuf - list) * 2 : nullptr);
                     if (nlist < 0) {  // wide pattern: the union is generated block by block later
                         slow_out = true;
                         nlist = 0;
@@ -628,6 +666,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         UnitInfo cur = decode_next(0, list, slow_cur);
         for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
             uint32_t *lcur = list + (ui_idx & 1) * 32;
+            const uint64_t *kcur = C::KBITS ? kbits + (ui_idx & 1) * 64 : nullptr;
             // The next unit is decoded one unit ahead. With loader warps it is
             // decoded once this unit's first steps are out (the loaders then
             // run ahead meanwhile); otherwise first, because this warp's own
@@ -743,6 +782,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         const int part = (G.b == 64) ? 0 : (u & 1);
                         int kb = -1, y = G.n;
                         bool a0 = false, a1 = false;
+                        bool have_bits = false;  // list entry: its key bits were taken at decode
+                        uint64_t lbits = 0ull;
                         if (cur.step0 >= 0) {  // full sweep of a global tile
                             const int yy = (C::SUB * cur.step0) * 64 + u * 64;
                             if (yy < G.n) {
@@ -759,6 +800,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                 a0 = (e >> 30) & 1u;
                                 a1 = (G.b == 64) ? ((e >> 31) & 1u) : a0;
                                 y = kb * G.b + part * 64;
+                                if (C::KBITS && up.km) {
+                                    lbits = kcur[2 * li + part];
+                                    have_bits = true;
+                                }
                             }
                         } else {
                             if (part == 0) {
@@ -776,7 +821,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         si.y[s] = y;
                         if (kb < 0) continue;
                         if (up.km) {
-                            const uint64_t bits = key_bits64(up.km, y, G.n);
+                            const uint64_t bits = have_bits ? lbits : key_bits64(up.km, y, G.n);
                             si.kmask[s] = bits;
                             if (bits == 0) continue;
                         }
@@ -1240,13 +1285,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                 }
                             }
                         } else if (PADDED) {
-                            // padded row: nothing allowed; padded keys: -inf
+                            // padded row: nothing allowed; padded keys: -inf (skipped
+                            // when the whole warp keeps every key, the common case
+                            // for prefix masks)
                             const uint64_t kmh = row_valid ? (half ? km1 : km0) : 0ull;
-                            const uint32_t lo = (uint32_t)kmh, hi = (uint32_t)(kmh >> 32);
+                            if (!__all_sync(kFull, kmh == ~0ull)) {
+                                const uint32_t lo = (uint32_t)kmh, hi = (uint32_t)(kmh >> 32);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                s0[i] = ((lo >> i) & 1u) ? s0[i] : -CUDART_INF_F;
-                                s1[i] = ((hi >> i) & 1u) ? s1[i] : -CUDART_INF_F;
+                                for (int i = 0; i < 32; ++i) {
+                                    s0[i] = ((lo >> i) & 1u) ? s0[i] : -CUDART_INF_F;
+                                    s1[i] = ((hi >> i) & 1u) ? s1[i] : -CUDART_INF_F;
+                                }
                             }
                         }
                         float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
