@@ -1190,6 +1190,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             cur.nchunks = ui.nchunks;
             cur.have = ui.n_steps > 0;
             cur.row_valid = row_valid;
+            // a warp none of whose rows is valid (rows past n, padded rows, the
+            // unused rows of a Longformer global-row unit) writes zero P and skips
+            // the step's arithmetic
+            const bool warp_rows = __any_sync(kFull, row_valid);
             cur.ob = qcnt & 1;
             if (ui.n_steps == 0) {
                 if (pe.kind != kUnitEnd && !(ok = epilogue(pe, true))) break;
@@ -1251,7 +1255,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 float lsum = 0.f;
 #pragma unroll 1
                 for (int half = 0; half < C::SUB; ++half) {
-                    const bool w_ok = (allow >> (2 * half + hf)) & 1u;  // warp-uniform
+                    const bool w_ok = warp_rows && ((allow >> (2 * half + hf)) & 1u);  // warp-uniform
                     uint32_t pk[32];
                     if (w_ok) {
                         float s0[32], s1[32];

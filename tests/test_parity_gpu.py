@@ -254,6 +254,15 @@ def test_bigbird_n4096_workload(path):
                  rows=rows, heads=[(0, 0), (3, 7), (7, 11)])
 
 
+def test_bigbird_n4096_workload_full_heads():
+    # The headline workload through the tensor-core path in the bench's launch
+    # configuration, two (batch, head) pairs compared on every row (all 64
+    # query blocks: global tiles, window edges, every random block).
+    wl = WORKLOADS["bigbird_bf16_n4096"]
+    bigbird_case(wl.B, wl.H, wl.n, wl.d, wl.b, wl.g, wl.w, wl.r, cfg_id=wl.cfg_id, path="tc",
+                 heads=[(2, 5), (6, 10)])
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_longformer_n4096_workload(path):
     wl = WORKLOADS["longformer_bf16_n4096"]
