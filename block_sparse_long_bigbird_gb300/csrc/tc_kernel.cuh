@@ -771,7 +771,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                             si.y[s] = y;
                             si.kmask[s] = kv;
                             gm2[s] = gm;
-                            if (kv & (band ? ~0ull : gm)) si.allow |= 3u << (2 * s);
+                            if (kv & gm) {
+                                si.allow |= 3u << (2 * s);  // global keys: every row sees them
+                            } else if (band && kv) {
+                                // a 64-row half sees a band block only when the block
+                                // meets its rows' windows [i - reach, i + reach]
+                                const int reach = cur.pad[2];
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int lo = cur.q0 + 64 * h - reach;
+                                    const int hi = cur.q0 + 64 * h + 63 + (G.causal ? 0 : reach);
+                                    if (y + 63 >= lo && y <= hi) si.allow |= 1u << (2 * s + h);
+                                }
+                            }
                             if (band) si.masked |= 1u << s;
                         }
                     } else {
@@ -1025,7 +1037,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // ================================================================ softmax / epilogue (tile x)
         const int tid = (warp & 3) * 32 + lane;  // query row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const int hf = (!LF && G.b == 64) ? (tid >> 6) : 0;
+        // 64-row half of this thread's row: BigBird b = 64 tiles hold two query
+        // blocks; Longformer band units skip band blocks a half's windows miss
+        const int hf = (LF || G.b == 64) ? (tid >> 6) : 0;
         const uint64_t *gmk = reinterpret_cast<const uint64_t *>(list);  // Longformer: global-key bits per step
         const float sl2 = G.scale_log2;
 
