@@ -1,6 +1,7 @@
 // BigBird-ITC host side of the tensor-core forward: geometry of the units
 // (local 128-row tiles and split global tiles), scratch layout, launch.
 #include "tc_kernel.cuh"
+#include "tc_split.h"
 
 namespace sa {
 namespace {

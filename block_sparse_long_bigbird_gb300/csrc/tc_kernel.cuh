@@ -58,7 +58,6 @@ using namespace tcsync;
 
 constexpr int kBM = 128;           // query rows per tile = TMEM lanes
 constexpr int kNU = 4;             // unit-info ring depth
-constexpr int kSplitRefSms = 152;  // GB300 SMs: the split choice below assumes a full-chip grid
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (factor 256)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzled region
@@ -158,32 +157,6 @@ struct Geometry {
     float scale_log2;
     unsigned long long wait_ns;
 };
-
-// Split-KV chunks of a global tile. A global tile sweeps every key in one unit,
-// so unsplit it can outlast the rest of the call; it is cut into chunks when
-// its sweep is longer than half the average work of one tile slot (tiles in
-// flight on a full-chip grid), each chunk about that half. `local_steps`:
-// estimated steps of all other units. The choice depends only on the sizes and
-// the options (not on the grid actually launched), so the scratch a call needs
-// is known before the device is queried. SA_OPT_CHUNK_KEYS overrides the
-// chunk length, SA_OPT_MAX_SPLITS bounds the count.
-inline void choose_splits(Geometry &G, long long local_steps, int kb, int tiles_per_cta, int chunk_keys,
-                          int max_splits) {
-    const long long BH = (long long)G.B * G.H;
-    int target = G.steps_full;
-    if (chunk_keys > 0) {
-        target = chunk_keys / kb;
-    } else {
-        const long long avg = (local_steps + BH * G.gtiles * G.steps_full) / ((long long)kSplitRefSms * tiles_per_cta);
-        if (2LL * G.steps_full > avg) target = (int)(avg / 2);
-    }
-    if (target < 8) target = 8;
-    int s0 = (G.steps_full + target - 1) / target;
-    if (s0 > max_splits) s0 = max_splits;
-    if (s0 < 1) s0 = 1;
-    G.steps_per_chunk = (G.steps_full + s0 - 1) / s0;
-    G.splits = (G.steps_full + G.steps_per_chunk - 1) / G.steps_per_chunk;
-}
 
 struct Workspace {
     unsigned *counters;   // [0] next unit, [1] finished CTAs

@@ -5,6 +5,7 @@
 // kernel then runs the global-row units (split-KV sweeps over all keys) and
 // one band unit per 128-row tile.
 #include "tc_kernel.cuh"
+#include "tc_split.h"
 
 namespace sa {
 namespace {

@@ -77,15 +77,20 @@ def test_noalloc_matches_bigbird_attn_fwd(case):
 
 
 def test_noalloc_rejects_oversize_before_touching_the_device():
-    # 2 heads of n = 65536, d = 128 with 64 global blocks: 128 global tiles
-    # whose sweeps are cut into split-KV chunks, tens of MB of partials, beyond
-    # the fixed array. The check runs on the host before any CUDA call, so the
-    # (never dereferenced) pointers below are safe even without a GPU.
+    # 2 heads of n = 65536, d = 128 with 64 global blocks (128 global tiles),
+    # their sweeps cut into 1024-key split-KV chunks (capped at 16 per tile):
+    # about 134 MB of partials, far beyond the fixed array. The check runs on
+    # the host before any CUDA call, so the (never dereferenced) pointers below
+    # are safe even without a GPU.
     fake = 0x7f0000000000
     lib = _lib.lib()
-    need = lib.sa_bigbird_workspace_bytes(1, 2, 65536, 128, 128, 64)
-    assert need > _lib.NOALLOC_SCRATCH_BYTES
-    st = lib.bigbird_attn_fwd_noalloc(fake, fake + 0x1000000, fake + 0x2000000, fake + 0x3000000,
-                                      1, 2, 65536, 128, 128, 64, 3, 3, fake + 0x4000000, None, None)
+    assert lib.sa_set_option(_lib.SA_OPT_CHUNK_KEYS, 1024) == _lib.SA_OK
+    try:
+        need = lib.sa_bigbird_workspace_bytes(1, 2, 65536, 128, 128, 64)
+        assert need > _lib.NOALLOC_SCRATCH_BYTES
+        st = lib.bigbird_attn_fwd_noalloc(fake, fake + 0x1000000, fake + 0x2000000, fake + 0x3000000,
+                                          1, 2, 65536, 128, 128, 64, 3, 3, fake + 0x4000000, None, None)
+    finally:
+        lib.sa_set_option(_lib.SA_OPT_CHUNK_KEYS, 0)
     assert st == _lib.SA_ERR_UNSUPPORTED
     assert np.isfinite(need)
