@@ -164,6 +164,13 @@ sa_status run(const sa::Problem &prob_in, sa_dtype dtype, cudaStream_t stream) {
     } else {
         const sa::TcConfig cfg = tc_config(st);
         void *ws = nullptr;
+        // Dilated Longformer heads run on residue-class copies of Q, K, V when
+        // the call has no global tokens, key mask or separate projections and
+        // the scratch can hold the copies (always for the library's own).
+        if (prob.kind == sa::kLongformer && prob.dilation && prob.n_global == 0 && !prob.key_mask && !prob.Qg) {
+            prob.class_perm = 1;
+            if (st->user_ws && st->user_ws_bytes < sa::tc_workspace_bytes(prob, cfg)) prob.class_perm = 0;
+        }
         const size_t need = sa::tc_workspace_bytes(prob, cfg);
         s = get_workspace(*st, need, &ws);
         if (s != SA_OK) return s;

@@ -49,6 +49,10 @@ struct Problem {
     // Longformer backward with separate global projections: which query rows
     // take part (0 all, 1 the non-global rows, 2 the global rows only)
     int row_set;
+    // Longformer forward: the scratch holds room for residue-class copies of
+    // Q, K and V (3 * B * H * n * d elements), so dilated heads whose stride
+    // divides n run as plain windows on those copies
+    int class_perm;
 };
 
 // Row stride of the backward's per-row statistics: n rounded up to 64, so that

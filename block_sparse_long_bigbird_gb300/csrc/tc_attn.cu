@@ -89,7 +89,7 @@ cudaError_t launch_bigbird(const Problem &p, const TcConfig &cfg, void *ws, size
     int grid = cfg.grid_ctas;
     if (grid > prm.geo.total_units) grid = prm.geo.total_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, mk, mv, prm);
+    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, mk, mv, mq, prm);
     return cudaGetLastError();
 }
 

@@ -178,6 +178,10 @@ struct Params {
     const __nv_bfloat16 *Q;
     const __nv_bfloat16 *Qg;  // Longformer: queries of the global-row units (Q, or the separate Qg)
     const int32_t *dilation;  // Longformer: per-head dilation [H] or NULL
+    // Longformer: dilated heads with n a multiple of their stride were gathered
+    // by residue class (class c's rows c, c + s, c + 2s, ... contiguous) into
+    // the copies tmQp / tmKg / tmVg read; their band units run on those copies
+    int class_perm;
     const int32_t *gidx;
     const unsigned long long *gbits;
     const int *gpre;
@@ -401,7 +405,8 @@ template <int D, bool PADDED, bool LF>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     sparse_tc_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKg,
-                   const __grid_constant__ CUtensorMap tmVg, const Params p) {
+                   const __grid_constant__ CUtensorMap tmVg, const __grid_constant__ CUtensorMap tmQp,
+                   const Params p) {
     using C = Cfg<D>;
     static_assert(C::SI * 2 * 8 <= 2 * 32 * 4, "Longformer global-key masks fit the list area");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -460,6 +465,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (LF) {
             prefetch_tmap(&tmKg);
             prefetch_tmap(&tmVg);
+            prefetch_tmap(&tmQp);
         }
     }
     tc_fence_before();
@@ -563,9 +569,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         if (lane == 0) atomicOr(p.status, kDevBadIndex);
                         dil = 0;
                     }
-                    const int reach = (int)min((long long)G.half * (dil + 1), (long long)G.n);
-                    ui.pad[1] = dil + 1;
+                    // residue-class unit: the head's rows were gathered by class, so
+                    // the dilated window is a plain window (stride 1, reach w/2) in
+                    // the gathered order, each row clipped to its own class
+                    const int cls = (p.class_perm && dil > 0 && G.n % (dil + 1) == 0) ? dil + 1 : 0;
+                    const int reach = cls ? G.half : (int)min((long long)G.half * (dil + 1), (long long)G.n);
+                    ui.pad[1] = cls ? 1 : dil + 1;
                     ui.pad[2] = reach;
+                    ui.pad[3] = cls;
                     const int blo = max(0, ui.q0 - reach) >> 6;
                     const int bhi = min(G.n - 1, ui.q0 + kBM - 1 + (G.causal ? 0 : reach)) >> 6;
                     int before = 0, after0 = 0, after = 0;
@@ -694,7 +705,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         mbar_arrive_expect_tx(bar(C::B_QF + qs), C::Q_BYTES);
                         for (int dc = 0; dc < D / 64; ++dc)
                             for (int rh = 0; rh < 2; ++rh)
-                                tma_load_3d(dst + dc * kRegionBytes + rh * 8192, &tmQ, bar(C::B_QF + qs), dc * 64,
+                                tma_load_3d(dst + dc * kRegionBytes + rh * 8192, (LF && cur.pad[3] > 0) ? &tmQp : &tmQ,
+                                            bar(C::B_QF + qs), dc * 64,
                                             cur.q0 + rh * 64, cur.bh);
                     }
                     q_tma_last = true;
@@ -844,7 +856,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                         const int kl = (int)((2u * g) & 31u);  // this step's K lane; V: the next one
                         const bool is_v = lane == kl + 1;
                         // global-row units read the global projections' keys and values
-                        const bool gsel = LF && cur.step0 >= 0;
+                        // (and residue-class units the gathered copies, passed in the same slots)
+                        const bool gsel = LF && (cur.step0 >= 0 || cur.pad[3] > 0);
                         const CUtensorMap *tm = is_v ? (gsel ? &tmVg : &tmV) : (gsel ? &tmKg : &tmK);
                         tma_load_3d_if(lane == kl || is_v, tbase + (is_v ? C::V_OFF : C::K_OFF) + sk * C::KV_BYTES, tm,
                                        bar((is_v ? C::B_VF : C::B_KF) + sk), 0, si.y[0], cur.bh, C::KV_BYTES);
@@ -980,7 +993,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
             const int kind = ring[slot].kind, n_steps = ring[slot].n_steps, bh = ring[slot].bh;
             // global-row units read the global projections' keys and values
-            const bool gsel = LF && ring[slot].step0 >= 0;
+            const bool gsel = LF && (ring[slot].step0 >= 0 || ring[slot].pad[3] > 0);
             const CUtensorMap *tmap = is_k ? (gsel ? &tmKg : &tmK) : (gsel ? &tmVg : &tmV);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_UE + slot));
@@ -1150,11 +1163,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             const int beta = ui.bh / G.H;
             // qpos: the query token of this thread's row; srow: where it is stored
             int qpos = ui.q0 + tid, srow = qpos;
+            // residue-class unit: qpos is a position in the gathered order; the
+            // row's class occupies [clo, chi] there, and its token is stored at
+            // c + s (qpos - clo)
+            bool cls_unit = false;
+            int clo = 0, chi = G.n - 1;
             if constexpr (LF) {
                 if (ui.step0 >= 0) {
                     qpos = srow = global_row(p.gidx, G.ng, G.n, ui.q0 + tid);
                 } else if (qpos < G.n && G.ng > 0 && ((__ldg(p.gbits + (qpos >> 6)) >> (qpos & 63)) & 1ull)) {
                     srow = G.n;  // a global row: its global-row unit stores it
+                }
+                if (ui.step0 < 0 && ui.pad[3] > 0) {
+                    const int s = ui.pad[3], M = G.n / s;
+                    const int c = min(qpos, G.n - 1) / M;
+                    cls_unit = true;
+                    clo = c * M;
+                    chi = clo + M - 1;
+                    srow = qpos < G.n ? c + s * (qpos - clo) : G.n;
                 }
             }
             const bool row_valid = qpos < G.n && (!PADDED || p.key_mask[(size_t)beta * G.n + qpos] != 0);
@@ -1263,6 +1289,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                         const int c0 = ((qpos - yh) % lstride + lstride) % lstride;
                                         bandm &= lpat << c0;
                                     }
+                                    if (cls_unit)  // gathered order: keys of the row's own class only
+                                        bandm &= bits_below(chi - yh + 1) & ~bits_below(clo - yh);
                                 }
                                 kmh = (half ? km1 : km0) & ((half ? gm1 : gm0) | bandm);
                                 if (G.causal) kmh &= bits_below(qpos - yh + 1);  // nothing after the query

@@ -66,6 +66,38 @@ __global__ void __launch_bounds__(kPrepThreads) longformer_prep(const int32_t *g
     if (tid == kPrepThreads - 1) gpre[nkb] = base;
 }
 
+// Residue-class gather of the dilated heads ("Longformer", Sec. 3.1: a dilated
+// window of stride s = dilation + 1 joins only tokens of one residue class
+// mod s). For each (batch, head) whose dilation is in range, nonzero and
+// whose stride divides n, row m of class c (token c + s m) is copied to
+// position c (n / s) + m of Q, K and V's copies; the attention kernel then runs
+// those heads as plain windows on the copies. Other heads are not touched.
+constexpr int kGatherThreads = 256;
+__global__ void __launch_bounds__(kGatherThreads) longformer_class_gather(const uint4 *Q, const uint4 *K,
+                                                                          const uint4 *V, uint4 *Qp, uint4 *Kp,
+                                                                          uint4 *Vp, const int32_t *dilation, int BH,
+                                                                          int H, int n, int cpr) {
+    for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+        const int dil = __ldg(dilation + bh % H);
+        if (dil <= 0 || dil > kMaxDilation) continue;  // out-of-range values are latched by the attention kernel
+        const int s = dil + 1;
+        if (n % s != 0) continue;
+        const int M = n / s;
+        const size_t head = (size_t)bh * n * cpr;
+        const long long total = (long long)n * cpr;
+        for (long long i = (long long)blockIdx.x * kGatherThreads + threadIdx.x; i < total;
+             i += (long long)gridDim.x * kGatherThreads) {
+            const int pos = (int)(i / cpr), cq = (int)(i - (long long)pos * cpr);
+            const int c = pos / M;
+            const size_t src = head + ((size_t)(c + s * (pos - c * M))) * cpr + cq;
+            const size_t dst = head + (size_t)pos * cpr + cq;
+            Qp[dst] = __ldg(Q + src);
+            Kp[dst] = __ldg(K + src);
+            Vp[dst] = __ldg(V + src);
+        }
+    }
+}
+
 Geometry longformer_geometry(const Problem &p, const TcConfig &cfg) {
     Geometry G = {};
     G.B = p.B;
@@ -99,10 +131,10 @@ Geometry longformer_geometry(const Problem &p, const TcConfig &cfg) {
 // Scratch: counters and per-row merge counters (zero at entry, left zero),
 // then split partials and the prep outputs (rewritten by every call).
 struct LfLayout {
-    size_t row_cnt, part_o, part_ml, gbits, gpre, glist, total;
+    size_t row_cnt, part_o, part_ml, gbits, gpre, glist, perm, total;
 };
 
-LfLayout lf_layout(const Geometry &G, int d) {
+LfLayout lf_layout(const Geometry &G, int d, bool class_perm) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     LfLayout L;
     const size_t tiles = (size_t)G.B * G.H * G.gtiles;
@@ -123,6 +155,11 @@ LfLayout lf_layout(const Geometry &G, int d) {
     off += up(((size_t)G.nkb + 1) * sizeof(int));
     L.glist = off;
     off += up((size_t)G.nkb * sizeof(int));
+    L.perm = 0;
+    if (class_perm) {  // residue-class copies of Q, K, V (rewritten by every call)
+        L.perm = off;
+        off += 3 * up((size_t)G.B * G.H * G.n * d * 2);
+    }
     L.total = off;
     return L;
 }
@@ -132,7 +169,7 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
                               int *launches) {
     Params prm = {};
     prm.geo = longformer_geometry(p, cfg);
-    const LfLayout L = lf_layout(prm.geo, D);
+    const LfLayout L = lf_layout(prm.geo, D, p.class_perm != 0);
     if (!ws || ws_bytes < L.total) return cudaErrorInvalidValue;
     uint8_t *base = static_cast<uint8_t *>(ws);
     prm.ws.counters = reinterpret_cast<unsigned *>(base);
@@ -157,10 +194,21 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
     prm.gpre = gpre;
     prm.glist = glist;
     const int BH = p.B * p.H;
-    CUtensorMap mq, mk, mv, mkg, mvg;
+    // residue-class copies (no global tokens, so the global-row key and value
+    // maps are free to point at them)
+    const bool cls = p.class_perm && p.dilation && prm.geo.ng == 0 && !sep && !p.key_mask;
+    const size_t tensor_bytes = (size_t)BH * p.n * D * 2;
+    const size_t cstride = (tensor_bytes + 255) & ~(size_t)255;
+    void *qp = cls ? base + L.perm : nullptr;
+    void *kp = cls ? base + L.perm + cstride : nullptr;
+    void *vp = cls ? base + L.perm + 2 * cstride : nullptr;
+    prm.class_perm = cls ? 1 : 0;
+    CUtensorMap mq, mk, mv, mkg, mvg, mqp;
     if (!make_qkv_map(&mq, p.Q, BH, p.n, D) || !make_qkv_map(&mk, p.K, BH, p.n, D) ||
-        !make_qkv_map(&mv, p.V, BH, p.n, D) || !make_qkv_map(&mkg, sep ? p.Kg : p.K, BH, p.n, D) ||
-        !make_qkv_map(&mvg, sep ? p.Vg : p.V, BH, p.n, D))
+        !make_qkv_map(&mv, p.V, BH, p.n, D) ||
+        !make_qkv_map(&mkg, cls ? kp : (sep ? p.Kg : p.K), BH, p.n, D) ||
+        !make_qkv_map(&mvg, cls ? vp : (sep ? p.Vg : p.V), BH, p.n, D) ||
+        !make_qkv_map(&mqp, cls ? qp : p.Q, BH, p.n, D))
         return cudaErrorInvalidValue;
     auto kern = p.key_mask ? sparse_tc_fwd<D, true, true> : sparse_tc_fwd<D, false, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::ALLOC_BYTES);
@@ -171,10 +219,21 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         ++*launches;
     }
+    if (cls) {
+        const int cpr = D / 8;  // 16-byte chunks per row
+        long long chunks = ((long long)p.n * cpr + kGatherThreads - 1) / kGatherThreads;
+        const dim3 ggrid((unsigned)(chunks < 64 ? chunks : 64), (unsigned)(BH < 65535 ? BH : 65535));
+        longformer_class_gather<<<ggrid, kGatherThreads, 0, stream>>>(
+            static_cast<const uint4 *>(p.Q), static_cast<const uint4 *>(p.K), static_cast<const uint4 *>(p.V),
+            static_cast<uint4 *>(qp), static_cast<uint4 *>(kp), static_cast<uint4 *>(vp), p.dilation, BH, p.H, p.n,
+            cpr);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        ++*launches;
+    }
     int grid = cfg.grid_ctas;
     if (grid > prm.geo.total_units) grid = prm.geo.total_units;
     if (grid < 1) grid = 1;
-    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, mkg, mvg, prm);
+    kern<<<grid, Cfg<D>::THREADS, Cfg<D>::ALLOC_BYTES, stream>>>(mq, mk, mv, mkg, mvg, mqp, prm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ++*launches;
     return cudaSuccess;
@@ -183,11 +242,11 @@ cudaError_t launch_longformer(const Problem &p, const TcConfig &cfg, void *ws, s
 }  // namespace
 
 size_t tc_longformer_workspace_bytes(const Problem &p, const TcConfig &cfg) {
-    return lf_layout(longformer_geometry(p, cfg), p.d).total;
+    return lf_layout(longformer_geometry(p, cfg), p.d, p.class_perm != 0).total;
 }
 
 size_t tc_longformer_counter_bytes(const Problem &p, const TcConfig &cfg) {
-    const LfLayout L = lf_layout(longformer_geometry(p, cfg), p.d);
+    const LfLayout L = lf_layout(longformer_geometry(p, cfg), p.d, p.class_perm != 0);
     return L.part_o ? L.part_o : L.gbits;
 }
 

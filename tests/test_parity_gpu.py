@@ -219,6 +219,16 @@ def test_longformer_causal_no_globals(path):
     longformer_case(1, 2, 1536, 64, 256, None, path=path, causal=True, cfg_id=87)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n,causal", [(3000, False), (3000, True), (3002, False), (6000, True)])
+def test_longformer_dilated_residue_classes(d, n, causal):
+    # No global tokens, no key mask: dilated heads whose stride divides n run on
+    # residue-class copies of Q, K, V (plain windows clipped to each class);
+    # n = 3002 leaves strides 3 and 4 on the direct dilated path beside stride 2.
+    # Every row of every head is compared.
+    longformer_case(1, 4, n, d, 128, None, dilation=[0, 1, 2, 3], causal=causal, cfg_id=89)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_longformer_dilation_two_heads_n4096(path):
     # dilation on two heads only (Longformer Tab. 12), causal, sampled rows
