@@ -165,6 +165,14 @@ sa_status longformer_attn_fwd(const void *Q, const void *K, const void *V, void 
  * dilation: DEVICE int32 [H] or NULL (all heads 0). Values outside [0, 63]
  *   latch SA_ERR_BAD_INDEX and are taken as 0.
  * causal: 0 or 1.
+ * Scratch: with dilation set and no global tokens, key mask or separate
+ *   projections, the bf16 call also uses 3 * B * H * n * d elements of scratch
+ *   for residue-class copies of Q, K and V (a dilated head whose stride
+ *   dilation + 1 divides n then runs as a plain window on its copies). The
+ *   library-owned scratch grows to hold them; a caller-owned region
+ *   (sa_set_workspace) too small for them is used without them, at the cost of
+ *   computing those heads over their whole dilated reach. The result does not
+ *   depend on which is taken beyond rounding order.
  * Other arguments, layout, ownership and errors: as for longformer_attn_fwd,
  * which is this call with dilation NULL and causal 0.
  */
@@ -327,7 +335,10 @@ sa_status longformer_attn_bwd_gproj(const void *Q, const void *K, const void *V,
  * stream-ordered (see the conventions above). A call leaves the counters at
  * zero when it completes, also after a wait expired (the last CTA to finish
  * clears the split-merge counters an aborted CTA left set).
- * Returns the bytes one call with these sizes needs (0 if the sizes are invalid).
+ * Returns the bytes one call with these sizes needs (0 if the sizes are invalid):
+ * an upper bound over the window and random-block counts for BigBird. For a
+ * dilated Longformer call it is the need without the optional residue-class
+ * copies (see longformer_attn_fwd_ex), which add 3 * B * H * n * d elements.
  */
 size_t sa_bigbird_workspace_bytes(int B, int H, int n, int d, int b, int g);
 size_t sa_longformer_workspace_bytes(int B, int H, int n, int d, int n_global);
