@@ -504,3 +504,33 @@ def test_split_options_keep_the_result(chunk_keys, max_splits):
         sa.set_option(sa.SA_OPT_MAX_SPLITS, 16)
     assert (O - base).abs().max().item() <= 2e-2
     assert torch.equal(O[:, :, g * b:], base[:, :, g * b:])
+
+
+def test_dilated_heads_with_a_small_caller_workspace():
+    # A caller-owned scratch sized by sa_longformer_workspace_bytes leaves no
+    # room for the residue-class copies: the dilated heads then run over their
+    # whole dilated reach. Both ways must match the oracle, and agree closely.
+    B, H, n, d = 1, 4, 3000, 64
+    dil = [0, 1, 2, 3]
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=142)
+    dev = torch.device("cuda:0")
+    Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
+    dt = torch.tensor(dil, dtype=torch.int32, device=dev)
+    with_copies = sa.longformer_attn_fwd(Qd, Kd, Vd, 128, None, dilation=dt, causal=True)
+    torch.cuda.synchronize()
+    need = sa.longformer_workspace_bytes(B, H, n, d, 0)
+    ws = torch.zeros((need + 255) // 256 * 256, dtype=torch.uint8, device=dev)
+    sa.set_workspace(ws)
+    try:
+        without = sa.longformer_attn_fwd(Qd, Kd, Vd, 128, None, dilation=dt, causal=True)
+        torch.cuda.synchronize()
+        assert sa.get_last_device_status() == 0
+    finally:
+        sa.set_workspace(None)
+    from oracle import oracle_longformer
+    ref = oracle_longformer(Q, K, V, 128, np.zeros(0, np.int64), dilation=dil, causal=True)
+    for O in (with_copies, without):
+        err = np.abs(O.float().cpu().numpy() - ref)
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
+    assert (with_copies.float() - without.float()).abs().max().item() <= 2e-2
+    assert torch.equal(with_copies[:, 0], without[:, 0])  # dilation 0: the same kernel path
