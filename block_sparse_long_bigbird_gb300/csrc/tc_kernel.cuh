@@ -27,6 +27,11 @@
 //   * Longformer, global-row unit: up to 128 global query rows, gathered into
 //     the Q tile by the producer warp; they sweep all keys with split-KV as
 //     BigBird's global tiles do.
+//   * Longformer, residue-class band unit: a dilated head (stride s) of a
+//     call without global tokens or padding, whose rows the host-side launch
+//     gathered by residue class mod s; in that order its window is a plain
+//     window, so the unit is a band unit over the copies with each row's mask
+//     clipped to its class and its output stored back at its own token.
 // Roles (256 threads for one tile in flight, 384 for two): per tile, one warp
 // schedules units, builds the key-block lists and issues TMA loads (K and V
 // in separate rings: a K stage is free once its QK^T completed, a V stage
@@ -262,6 +267,25 @@ __device__ __forceinline__ void block_key_bits_lane(const uint8_t *km, int kb, i
             for (int j = 0; j < 4; ++j) m |= (((w[k] >> (8 * j)) & 0xFFu) != 0u ? 1u : 0u) << (4 * k + j);
         bits[i >> 2] |= (uint64_t)m << (16 * (i & 3));
     }
+}
+
+// Validity bits of the 64 keys [y, y + 64) (per lane, 16-byte loads; y is a
+// multiple of 64 inside [0, n), n a multiple of 64).
+__device__ __forceinline__ uint64_t key_bits64_lane(const uint8_t *km, int y) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(km + y);
+    uint64_t bits = 0ull;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m |= (((w[k] >> (8 * j)) & 0xFFu) != 0u ? 1u : 0u) << (4 * k + j);
+        bits |= (uint64_t)m << (16 * i);
+    }
+    return bits;
 }
 
 // Any valid key in block kb (warp-uniform answer).
@@ -650,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         UnitInfo cur = decode_next(0, list, slow_cur);
         for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
             uint32_t *lcur = list + (ui_idx & 1) * 32;
-            const uint64_t *kcur = C::KBITS ? kbits + (ui_idx & 1) * 64 : nullptr;
+            uint64_t *kcur = C::KBITS ? kbits + (ui_idx & 1) * 64 : nullptr;
             // The next unit is decoded one unit ahead. With loader warps it is
             // decoded once this unit's first steps are out (the loaders then
             // run ahead meanwhile); otherwise first, because this warp's own
@@ -715,6 +739,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                 // ---- key steps
                 int xs = -1;  // wide patterns: last block emitted
                 for (int t = 0; t < cur.n_steps; ++t, ++g) {
+                    if (!LF && C::KBITS && up.km && cur.step0 >= 0 && (t & 31) == 0) {
+                        // a global tile's sweep with a key mask: the validity bits of
+                        // the next 32 steps' keys, one step per lane (one global round
+                        // trip per 32 steps instead of one per step), in this unit's
+                        // key-bit buffer (a sweep has no block list)
+                        static_assert(!C::KBITS || C::SUB == 1, "one 64-key block per step");
+                        const int yy = (cur.step0 + t + lane) * 64;
+                        kcur[lane] = (t + lane < cur.n_steps && yy < G.n) ? key_bits64_lane(up.km, yy) : 0ull;
+                        __syncwarp();
+                    }
                     StepInfo si;
                     si.masked = up.km ? 1u : 0u;
                     si.allow = 0;
@@ -788,6 +822,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                                 kb = (G.b == 64) ? (yy >> 6) : (yy >> 7);
                                 a0 = block_allowed(p, up.r0, cur.j0, kb);
                                 a1 = (G.b == 64) ? block_allowed(p, up.r1, cur.j1, kb) : a0;
+                                if (C::KBITS && up.km) {
+                                    lbits = kcur[t & 31];
+                                    have_bits = true;
+                                }
                             }
                         } else if (!slow_cur) {
                             const int li = (G.b == 64) ? u : (u >> 1);
