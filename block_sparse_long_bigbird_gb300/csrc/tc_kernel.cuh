@@ -640,13 +640,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             auto list_steps = [&](int nlist) {
                 return G.b == 64 ? (nlist + C::SUB - 1) / C::SUB : nlist * (2 / C::SUB);
             };
-            if (ui.step0 < 0) {
-                bool any_row = true;
-                if (up.km) {
-                    bool a = false;
-                    for (int t = lane; t < kBM; t += 32) a |= (ui.q0 + t < G.n) && up.km[ui.q0 + t] != 0;
-                    any_row = __any_sync(kFull, a);
+            // with a key mask, the validity of the tile's 128 query rows as four
+            // 32-bit words in pad[] (the softmax reads them from the ring instead
+            // of loading the mask at the start of every unit)
+            bool any_row = true;
+            if (up.km) {
+                uint32_t any = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = ui.q0 + 32 * k + lane;
+                    const uint32_t w = __ballot_sync(kFull, t < G.n && up.km[t] != 0);
+                    ui.pad[k] = (int)w;
+                    any |= w;
                 }
+                any_row = any != 0;
+            }
+            if (ui.step0 < 0) {
                 int nlist = 0;
                 if (any_row) {
                     nlist = build_local_list(p, ui.j0, ui.j1, up.r0, up.r1, up.km, lbuf,
@@ -1196,6 +1205,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             const uint32_t slot = ui_idx % kNU;
             if (!(ok = wait_warp(bar(C::B_UF + slot), (ui_idx / kNU) & 1, ctl))) break;
             const UnitInfo ui = ring[slot];
+            // BigBird with a key mask: this thread's query-row validity word
+            // (read from shared memory before the slot is released)
+            const uint32_t rowbits = (PADDED && !LF) ? (uint32_t)ring[slot].pad[tid >> 5] : 0u;
             mbar_arrive(bar(C::B_UE + slot));
             if (ui.kind == kUnitEnd) break;
             const int beta = ui.bh / G.H;
@@ -1221,7 +1233,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     srow = qpos < G.n ? c + s * (qpos - clo) : G.n;
                 }
             }
-            const bool row_valid = qpos < G.n && (!PADDED || p.key_mask[(size_t)beta * G.n + qpos] != 0);
+            bool row_valid = qpos < G.n;
+            if constexpr (PADDED) {
+                if constexpr (LF)
+                    row_valid = row_valid && p.key_mask[(size_t)beta * G.n + qpos] != 0;
+                else  // BigBird: the producer's row bits (qpos = q0 + tid)
+                    row_valid = row_valid && ((rowbits >> (tid & 31)) & 1u);
+            }
             // Longformer band units: window stride, reach and the stride pattern
             // (bits 0, s, 2s, ... of a 64-key block)
             int lstride = 1, lreach = G.half;
