@@ -201,3 +201,30 @@ def _lfg(lib, **kw):
                                  dict(causal=3), dict(window=5)])
 def test_longformer_gproj_invalid_args(lib, bad):
     assert _lfg(lib, **bad) == 1
+
+
+def test_split_options_shape_the_workspace(lib):
+    from block_sparse_long_bigbird_gb300 import _lib
+
+    # A global tile's sweep is cut into split-KV chunks only when it is long
+    # against the call's other work; SA_OPT_CHUNK_KEYS forces a chunk length
+    # and SA_OPT_MAX_SPLITS bounds the count. The scratch need follows (host
+    # arithmetic only, no device).
+    args = (1, 2, 16384, 64, 64, 2)  # few heads: long global sweeps, split by default
+    base = lib.sa_bigbird_workspace_bytes(*args)
+    big = lib.sa_bigbird_workspace_bytes(8, 12, 4096, 64, 64, 2)  # upper bound over w, r
+    try:
+        assert lib.sa_set_option(_lib.SA_OPT_MAX_SPLITS, 1) == _lib.SA_OK
+        one = lib.sa_bigbird_workspace_bytes(*args)
+        assert one < base  # no partials
+        assert lib.sa_set_option(_lib.SA_OPT_MAX_SPLITS, 16) == _lib.SA_OK
+        assert lib.sa_set_option(_lib.SA_OPT_CHUNK_KEYS, 1 << 20) == _lib.SA_OK
+        assert lib.sa_bigbird_workspace_bytes(*args) == one  # one chunk covers every key
+        assert lib.sa_set_option(_lib.SA_OPT_CHUNK_KEYS, 512) == _lib.SA_OK
+        assert lib.sa_bigbird_workspace_bytes(*args) >= base  # 16 chunks of 8 steps at most
+        assert lib.sa_set_option(_lib.SA_OPT_CHUNK_KEYS, -5) == _lib.SA_OK  # back to the default
+        assert lib.sa_bigbird_workspace_bytes(*args) == base
+        assert lib.sa_bigbird_workspace_bytes(8, 12, 4096, 64, 64, 2) == big
+    finally:
+        lib.sa_set_option(_lib.SA_OPT_CHUNK_KEYS, 0)
+        lib.sa_set_option(_lib.SA_OPT_MAX_SPLITS, 16)
