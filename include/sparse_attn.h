@@ -381,12 +381,16 @@ const char *sa_status_string(sa_status status);
  *                      (default 16, 1 disables splitting).
  *  SA_OPT_GRID_CTAS    persistent-grid size (0 = one CTA per SM).
  *  SA_OPT_CHUNK_KEYS   keys per split-KV chunk of a global row tile, before
- *                      the SA_OPT_MAX_SPLITS bound (value <= 0: the default,
- *                      described in the kernel notes; at most 2^20). Shorter
- *                      chunks shorten the longest unit of a call (a global
- *                      row sweeps every key) at the cost of more partial
- *                      results to merge. The output does not depend on it
- *                      beyond rounding order.
+ *                      the SA_OPT_MAX_SPLITS bound (at most 2^20; chunks are
+ *                      at least 8 steps). value <= 0 restores the default: a
+ *                      tile's sweep is cut only when it exceeds three quarters
+ *                      of the call's average work per tile in flight on a
+ *                      full GB300 (estimated from the sizes and the pattern),
+ *                      into chunks of about half that work. Shorter chunks
+ *                      shorten the longest unit of a call (a global row
+ *                      sweeps every key) at the cost of more partial results
+ *                      to merge. The output does not depend on it beyond
+ *                      rounding order.
  * Returns SA_ERR_INVALID_ARG for an unknown option.
  */
 enum { SA_OPT_FORCE_SIMT = 1, SA_OPT_WAIT_LIMIT = 2, SA_OPT_MAX_SPLITS = 3, SA_OPT_GRID_CTAS = 4,
