@@ -5,7 +5,8 @@ for bf16 inputs each element's error stays within 2^-8 of the sum of the
 magnitudes of its terms plus its own magnitude, and the mean error within
 2^-9 of the terms' root-sum-square plus magnitude (term sizes from the
 oracle); fp32 inputs use 1e-4 of the reference gradient's RMS plus 1e-5
-relative (``FP32_GRAD_TOL``). Every case runs through the C ABI (the forward,
+relative (``FP32_GRAD_TOL``) per element and 1e-5 of the RMS on the mean
+(``FP32_GRAD_MEAN_TOL``). Every case runs through the C ABI (the forward,
 then the backward at the same inputs).
 """
 
