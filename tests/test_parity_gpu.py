@@ -99,6 +99,21 @@ def test_bigbird_padded_runs_few_ctas(d, b, grid):
         sa.set_option(sa.SA_OPT_GRID_CTAS, 0)
 
 
+@pytest.mark.parametrize("grid", [1, 2, 5])
+def test_few_ctas_split_sweeps_and_residue_classes(grid):
+    # Few persistent CTAs walk every unit kind in sequence: a padded BigBird
+    # call whose global tiles are cut into split-KV chunks (2 heads at n = 8192)
+    # and a dilated Longformer call on residue-class copies.
+    sa.set_option(sa.SA_OPT_GRID_CTAS, grid)
+    try:
+        km = make_key_mask(1, 8192, seed=41)
+        rows = sampled_bigbird_rows(8192, 64, 2, n_random_blocks=4, seed=8)
+        bigbird_case(1, 2, 8192, 64, 64, 2, 3, 3, key_mask=km, path="tc", cfg_id=143, rows=rows)
+        longformer_case(1, 3, 1200, 64, 96, None, dilation=[0, 1, 3], causal=True, cfg_id=144)
+    finally:
+        sa.set_option(sa.SA_OPT_GRID_CTAS, 0)
+
+
 # ------------------------------------------------------------- Longformer, small full compares
 
 LONGFORMER_SMALL = [
