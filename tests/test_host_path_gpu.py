@@ -55,3 +55,21 @@ def test_host_path_fp32():
     out = sa.bigbird_attn_fwd_host(Q.pin_memory(), K.pin_memory(), V.pin_memory(), b, g, w, r, table)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_longformer_host_path_residue_classes(B):
+    # Dilated heads, no global tokens, no padding: every chunk of the host path
+    # (heads of one entry for B = 1, whole entries for B = 3) runs its dilated
+    # heads on residue-class copies, with its slice of the dilation array.
+    dev = torch.device("cuda:0")
+    H, n, d = 8, 2400, 64
+    Q, K, V = make_qkv(B, H, n, d, "bf16", cfg_id=99)
+    dil = torch.tensor([0, 3, 1, 2, 0, 3, 6, 1], dtype=torch.int32)  # stride 7 does not divide 2400: direct path
+    ref = sa.longformer_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), 256, None, None,
+                                 dilation=dil.to(dev), causal=True).cpu()
+    Qh, Kh, Vh = (t.pin_memory() for t in (Q, K, V))
+    out = sa.longformer_attn_fwd_host(Qh, Kh, Vh, 256, None, None, dilation=dil, causal=True)
+    torch.cuda.synchronize()
+    assert sa.get_last_device_status() == 0
+    assert torch.equal(out, ref)
