@@ -523,22 +523,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
     if (role == 0) {
         // ================================================================ producer (tile x)
-        // Units are decoded (and their key/value blocks prefetched into L2)
-        // one unit ahead of the TMA loads that consume them.
+        // Units are decoded one unit ahead of the TMA loads that consume them.
         uint32_t g = 0, qcnt = 0;
         uint32_t issued = 0;  // steps whose K and V copies are out (drained on abort)
         bool q_tma_last = false;  // the latest Q fill was a TMA copy (drained on abort)
         uint64_t *gmk = reinterpret_cast<uint64_t *>(list);  // Longformer: global-key bits per step
         bool ok = true;
         unsigned u_next = 0;
-        if (lane == 0) u_next = atomicAdd(p.ws.counters, 1u);
         // decode the next unit from the work counter into ring slot `slot`
-        // and list buffer `lb`; returns its info (kind kUnitEnd when done)
+        // and list buffer `lb`; returns its info (kind kUnitEnd when done).
+        // The unit is claimed here, not earlier: a claim made ahead of need
+        // holds the unit back from a tile slot that may free sooner, which
+        // lengthens the call's tail (measured: the n = 4096 Longformer call 7%)
+        // more than the counter's latency costs off the critical path.
         auto decode_next = [&](uint32_t ui_idx, uint32_t *lbuf, bool &slow_out) -> UnitInfo {
             UnitInfo ui = {};
             slow_out = false;
+            if (lane == 0) u_next = atomicAdd(p.ws.counters, 1u);
             int u = (int)__shfl_sync(kFull, u_next, 0);
-            if (lane == 0 && u < G.total_units) u_next = atomicAdd(p.ws.counters, 1u);  // prefetch the next
             const uint32_t slot = ui_idx % kNU;
             if (ui_idx >= kNU && !(ok = wait_warp(bar(C::B_UE + slot), ((ui_idx / kNU) - 1) & 1, ctl))) {
                 ui.kind = kUnitEnd;
@@ -684,10 +686,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
             uint32_t *lcur = list + (ui_idx & 1) * 32;
             uint64_t *kcur = C::KBITS ? kbits + (ui_idx & 1) * 64 : nullptr;
-            // The next unit is decoded one unit ahead. With loader warps it is
-            // decoded once this unit's first steps are out (the loaders then
-            // run ahead meanwhile); otherwise first, because this warp's own
-            // copies and step records must not pause mid-unit.
+            // The next unit is decoded one unit ahead, once this unit's Q copy
+            // and its first two steps are out: the copies and the consumers'
+            // first steps then overlap the decode (its global loads and the
+            // work-counter claim), and the producer's few steps of lead absorb
+            // the pause (measured: +5% on full attention and the n = 4096
+            // Longformer call, +3% padded, against decoding first).
             UnitInfo nxt;
             bool have_nxt = false;
             auto decode_ahead = [&]() {
@@ -696,10 +700,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     have_nxt = true;
                 }
             };
-            if (!C::LOADERS) {
-                decode_ahead();
-                if (!ok) break;
-            }
             if (cur.n_steps > 0) {
                 const UnitPtrs up = unit_ptrs(p, cur);
                 const int nlist = cur.pad0;
