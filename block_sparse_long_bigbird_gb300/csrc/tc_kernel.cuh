@@ -686,12 +686,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (uint32_t ui_idx = 0; ok && cur.kind != kUnitEnd; ++ui_idx) {
             uint32_t *lcur = list + (ui_idx & 1) * 32;
             uint64_t *kcur = C::KBITS ? kbits + (ui_idx & 1) * 64 : nullptr;
-            // The next unit is decoded one unit ahead, once this unit's Q copy
-            // and its first two steps are out: the copies and the consumers'
-            // first steps then overlap the decode (its global loads and the
-            // work-counter claim), and the producer's few steps of lead absorb
-            // the pause (measured: +5% on full attention and the n = 4096
-            // Longformer call, +3% padded, against decoding first).
+            // The next unit is decoded one unit ahead. With loader warps it is
+            // decoded once this unit's first steps are out (the loaders then
+            // run ahead meanwhile); otherwise first, because this warp's own
+            // copies and step records must not pause mid-unit (decoding after
+            // the second step measured +3-5% for long units but -9% for the
+            // short units of the autoregressive char-LM call).
             UnitInfo nxt;
             bool have_nxt = false;
             auto decode_ahead = [&]() {
@@ -700,6 +700,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     have_nxt = true;
                 }
             };
+            if (!C::LOADERS) {
+                decode_ahead();
+                if (!ok) break;
+            }
             if (cur.n_steps > 0) {
                 const UnitPtrs up = unit_ptrs(p, cur);
                 const int nlist = cur.pad0;
