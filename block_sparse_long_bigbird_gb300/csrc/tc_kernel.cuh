@@ -539,7 +539,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         auto decode_next = [&](uint32_t ui_idx, uint32_t *lbuf, bool &slow_out) -> UnitInfo {
             UnitInfo ui = {};
             slow_out = false;
-            if (lane == 0) u_next = atomicAdd(p.ws.counters, 1u);
+            // A tile slot's first unit is fixed by the slot's index (the call's
+            // first copies wait for no counter round trip); later claims count
+            // on from there.
+            const unsigned slots = gridDim.x * C::NT;
+            if (lane == 0) u_next = ui_idx == 0 ? blockIdx.x * C::NT + x : atomicAdd(p.ws.counters, 1u) + slots;
             int u = (int)__shfl_sync(kFull, u_next, 0);
             const uint32_t slot = ui_idx % kNU;
             if (ui_idx >= kNU && !(ok = wait_warp(bar(C::B_UE + slot), ((ui_idx / kNU) - 1) & 1, ctl))) {
@@ -691,7 +695,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             // run ahead meanwhile); otherwise first, because this warp's own
             // copies and step records must not pause mid-unit (decoding after
             // the second step measured +3-5% for long units but -9% for the
-            // short units of the autoregressive char-LM call).
+            // short units of the autoregressive char-LM call). A BigBird call's
+            // first unit is the exception: nothing is in flight yet, so its
+            // first copies go out before the second unit's list is built
+            // (measured: padded n = 16384 +4%; the same order for Longformer,
+            // whose units need no list, cost the char-LM call 12%).
             UnitInfo nxt;
             bool have_nxt = false;
             auto decode_ahead = [&]() {
@@ -700,7 +708,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                     have_nxt = true;
                 }
             };
-            if (!C::LOADERS) {
+            if (!C::LOADERS && (LF || ui_idx > 0)) {
                 decode_ahead();
                 if (!ok) break;
             }
