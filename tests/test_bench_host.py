@@ -81,3 +81,35 @@ def test_workload_configs_name_the_workload_and_no_model():
         assert "model" not in cfg
         for key in ("B", "H", "n", "d", "dtype", "l2"):
             assert key in cfg, (name, key)
+
+
+def test_reference_arm_times_the_oracle_without_the_library():
+    # `bench.py --impl reference` times the float64 oracle on the host cores
+    # and prints the contract's JSON line; it must not load the CUDA library
+    # (a fresh interpreter, since other tests in this process load it).
+    import subprocess
+
+    code = (
+        "import sys, runpy, io, contextlib\n"
+        "sys.argv = ['bench.py', '--impl', 'reference', '--workload', 'bigbird_fp32_n1024',\n"
+        "            '--steps', '1', '--warmup', '0', '--cpu-seconds', '1']\n"
+        "buf = io.StringIO()\n"
+        "with contextlib.redirect_stdout(buf):\n"
+        "    try:\n"
+        "        runpy.run_path('bench.py', run_name='__main__')\n"
+        "    except SystemExit:\n"
+        "        pass\n"
+        "print(buf.getvalue().strip().splitlines()[-1])\n"
+        "print('libsparse_attn' in open('/proc/self/maps').read())\n"
+    )
+    res = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    out = res.stdout.strip().splitlines()
+    line, loaded = json.loads(out[-2]), out[-1]
+    assert loaded == "False", "the reference arm loaded the CUDA library"
+    assert line["impl"] == "reference" and line["dtype"] == "f64"
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"].startswith("bigbird_fp32_n1024")
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
