@@ -33,11 +33,13 @@
 //     window, so the unit is a band unit over the copies with each row's mask
 //     clipped to its class and its output stored back at its own token.
 // Roles (256 threads for one tile in flight, 384 for two): per tile, one warp
-// schedules units, builds the key-block lists and issues TMA loads (K and V
-// in separate rings: a K stage is free once its QK^T completed, a V stage
-// once its PV completed); one warp issues tcgen05 MMAs (lane 0); a warpgroup
-// runs the softmax (thread t owns query row t = TMEM lane t), the lazy O
-// rescale and the epilogue. The softmax writes P (bf16) over the first half
+// claims and decodes units, builds the key-block lists, writes the step
+// records and loads Q (for d = 64 it also issues the K and V copies; for
+// d = 128 two loader warps do); one warp runs the MMA loop converged, one
+// elected lane issuing the tcgen05 MMAs and commits; a warpgroup runs the
+// softmax (thread t owns query row t = TMEM lane t), the lazy O rescale and
+// the epilogue, and releases K/V stages once the S of a later step shows
+// the MMAs that read them complete (MMAs of one thread complete in order). The softmax writes P (bf16) over the first half
 // of its S buffer and the PV product reads A straight from TMEM. O is double
 // buffered in TMEM so a unit's epilogue runs while the next unit computes.
 // Every wait is bounded in time: on expiry the CTA records SA_ERR_TIMEOUT,
